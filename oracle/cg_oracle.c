@@ -1,0 +1,463 @@
+/*
+ * cg_oracle.c - CPU oracle for the CacheGen KV-cache codec.
+ *
+ * TEST INFRASTRUCTURE ONLY (see cg_oracle.h): slow, single-threaded, written
+ * to be read against the page and the codec specification in cg_oracle.h.
+ * Compiled with -O2 -ffp-contract=off so every binary32 operation is rounded
+ * on its own.
+ *
+ * Each step follows the order the page gives: quantise [CG §2.3(1)], count
+ * and build the CDF [CG §2.3(2)], code per chunk [CG §2.3(3), §1.2(3)], decode
+ * [CG §2.4(1)] and dequantise [CG §2.4(2)].
+ */
+#include "cg_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_M 65536u
+
+float orc_half_to_float(uint16_t h)
+{
+    /* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    float mag;
+    if (e == 0)
+        mag = ldexpf((float)f, -24); /* subnormal: f * 2^-24, exact */
+    else if (e == 31)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexpf((float)(f | 0x400), e - 25); /* 1.f * 2^(e-15) */
+    return sign ? -mag : mag;
+}
+
+/* [CG §2.3(1)] torch_quant_vectorized on one group: MAX = bins // 2 - 1,
+ * max1 = amax |x| over the group, factor = MAX / max1,
+ * xq = round(x * factor + MAX). Arithmetic in binary32 (specification Q). */
+int orc_quantize_group(const uint16_t *x, int64_t C, int bins, uint8_t *q,
+                       uint16_t *max1_out)
+{
+    if (bins < 4 || bins > 256 || C < 1)
+        return ORC_ERR_ARG;
+    int MAX = bins / 2 - 1;
+    float max1 = 0.0f;
+    uint16_t max1_bits = 0;
+    for (int64_t c = 0; c < C; c++) {
+        float xv = orc_half_to_float(x[c]);
+        if (!isfinite(xv))
+            return ORC_ERR_NONFINITE;
+        float a = fabsf(xv);
+        if (a > max1) {
+            max1 = a;
+            max1_bits = (uint16_t)(x[c] & 0x7FFF);
+        }
+    }
+    *max1_out = max1_bits;
+    if (max1 == 0.0f) {
+        /* all-zero group: every value sits at the offset MAX */
+        for (int64_t c = 0; c < C; c++)
+            q[c] = (uint8_t)MAX;
+        return ORC_OK;
+    }
+    float factor = (float)MAX / max1;
+    for (int64_t c = 0; c < C; c++) {
+        float xv = orc_half_to_float(x[c]);
+        float scaled = xv * factor;
+        float y = scaled + (float)MAX;
+        float r = rintf(y);
+        if (r < 0.0f)
+            r = 0.0f;
+        if (r > (float)(2 * MAX))
+            r = (float)(2 * MAX);
+        q[c] = (uint8_t)r;
+    }
+    return ORC_OK;
+}
+
+/* [CG §2.4(2)] do_dequantize: t - MAX, to float, divide by MAX, times max1. */
+float orc_dequantize_value(uint8_t q, int bins, uint16_t max1)
+{
+    int MAX = bins / 2 - 1;
+    float centred = (float)((int)q - MAX);
+    float unit = centred / (float)MAX;
+    return unit * orc_half_to_float(max1);
+}
+
+/* [CG §2.3(2)] symbol frequencies -> CDF, normalised to a 16-bit total with
+ * every symbol given a frequency of at least one (specification F). */
+int orc_cdf_from_counts(const uint32_t *n, int A, uint32_t Tk, uint16_t *cdf)
+{
+    if (A < 2 || A > 256 || Tk < 1)
+        return ORC_ERR_ARG;
+    uint32_t f[256];
+    uint64_t sum = 0;
+    int best = 0;
+    for (int s = 0; s < A; s++) {
+        f[s] = 1u + (uint32_t)(((uint64_t)n[s] * (ORC_M - (uint32_t)A)) / Tk);
+        sum += f[s];
+        if (n[s] > n[best])
+            best = s;
+    }
+    if (sum > ORC_M)
+        return ORC_ERR_ARG; /* counts do not add up to Tk */
+    f[best] += (uint32_t)(ORC_M - sum);
+    uint32_t acc = 0;
+    for (int s = 0; s < A; s++) {
+        cdf[s] = (uint16_t)acc;
+        acc += f[s];
+    }
+    return acc == ORC_M ? ORC_OK : ORC_ERR_ARG;
+}
+
+/* Carry into the bytes already emitted: the last byte gets +1; a 0xFF byte
+ * turns into 0x00 and passes the carry on to the byte before it. */
+static void orc_propagate_carry(uint8_t *out, int64_t pos)
+{
+    int64_t i = pos - 1;
+    while (i >= 0 && out[i] == 0xFF) {
+        out[i] = 0x00;
+        i--;
+    }
+    if (i >= 0)
+        out[i] = (uint8_t)(out[i] + 1);
+}
+
+static uint32_t orc_cdf_at(const uint16_t *row, int A, int s)
+{
+    return s >= A ? ORC_M : (uint32_t)row[s];
+}
+
+/* [CG §1.2(3)] arithmetic coding, in the range-coder form of specification R. */
+int64_t orc_encode_stream(const uint8_t *sym, int64_t n, const uint16_t *cdf,
+                          int64_t row_stride, int A, uint8_t *out, int64_t cap)
+{
+    if (A < 2 || n < 0 || cap < 0)
+        return -1;
+    uint32_t low = 0, range = 0xFFFFFFFFu;
+    int64_t pos = 0;
+    for (int64_t i = 0; i < n; i++) {
+        const uint16_t *row = cdf + i * row_stride;
+        int s = sym[i];
+        if (s >= A)
+            return -1;
+        uint32_t lo = orc_cdf_at(row, A, s);
+        uint32_t f = orc_cdf_at(row, A, s + 1) - lo;
+        uint32_t r = range >> 16;
+        uint32_t t = low + r * lo;
+        if (t < low)
+            orc_propagate_carry(out, pos);
+        low = t;
+        range = r * f;
+        while (range < (1u << 24)) {
+            if (pos >= cap)
+                return -1;
+            out[pos++] = (uint8_t)(low >> 24);
+            low <<= 8;
+            range <<= 8;
+        }
+    }
+    uint32_t v = low + 0x00FFFFFFu;
+    if (v < low)
+        orc_propagate_carry(out, pos);
+    if (pos >= cap)
+        return -1;
+    out[pos++] = (uint8_t)(v >> 24);
+    return pos;
+}
+
+/* [CG §2.4(1)] decode_function_gpu: recover the integer symbols of one
+ * stream with the CDFs sent alongside it (specification R, decoder side). */
+int orc_decode_stream(const uint8_t *in, int64_t len, int64_t n,
+                      const uint16_t *cdf, int64_t row_stride, int A,
+                      uint8_t *sym, int64_t *consumed)
+{
+    if (A < 2 || n < 0 || len < 0)
+        return ORC_ERR_ARG;
+    int64_t pos = 0;
+    uint32_t range = 0xFFFFFFFFu, code = 0;
+    for (int b = 0; b < 4; b++) {
+        uint32_t byte = pos < len ? in[pos] : 0;
+        pos++;
+        code = (code << 8) | byte;
+    }
+    for (int64_t i = 0; i < n; i++) {
+        const uint16_t *row = cdf + i * row_stride;
+        uint32_t r = range >> 16;
+        int s = 0;
+        for (int c = 1; c < A; c++)
+            if ((uint64_t)r * row[c] <= code)
+                s = c;
+        uint32_t lo = orc_cdf_at(row, A, s);
+        uint32_t f = orc_cdf_at(row, A, s + 1) - lo;
+        sym[i] = (uint8_t)s;
+        code -= r * lo;
+        range = r * f;
+        while (range < (1u << 24)) {
+            uint32_t byte = pos < len ? in[pos] : 0;
+            pos++;
+            code = (code << 8) | byte;
+            range <<= 8;
+        }
+    }
+    if (consumed)
+        *consumed = pos;
+    return pos == len + 3 ? ORC_OK : ORC_ERR_CORRUPT;
+}
+
+int64_t orc_num_streams(int L, int T) { return 2 * (int64_t)L * T; }
+
+static int orc_chunk_tokens(int T, int Tc, int k)
+{
+    int rest = T - k * Tc;
+    return rest < Tc ? rest : Tc;
+}
+
+int64_t orc_cdf_elems(int L, int T, int C, int Tc, int A_k, int A_v)
+{
+    int64_t nch = (T + Tc - 1) / Tc;
+    return nch * (int64_t)L * C * (A_k + A_v);
+}
+
+int64_t orc_cdf_offset(int L, int C, int A_k, int A_v, int k, int kv, int l,
+                       int c)
+{
+    int64_t chunk = (int64_t)k * L * C * (A_k + A_v);
+    int64_t tensor = kv ? (int64_t)L * C * A_k : 0;
+    int A = kv ? A_v : A_k;
+    return chunk + tensor + ((int64_t)l * C + c) * A;
+}
+
+int64_t orc_stream_id(int L, int T, int Tc, int k, int kv, int l, int tl)
+{
+    int Tck = orc_chunk_tokens(T, Tc, k);
+    return 2 * (int64_t)L * Tc * k + ((int64_t)kv * L + l) * Tck + tl;
+}
+
+int orc_alphabet(const int32_t *bins, int L)
+{
+    int a = 0;
+    for (int l = 0; l < L; l++)
+        if (bins[l] > a)
+            a = bins[l];
+    return a;
+}
+
+static int orc_check_shape(int L, int T, int C)
+{
+    return L >= 1 && T >= 1 && C >= 1;
+}
+
+/* [CG §2.3(1)] with the layer-wise bins of [CG §2.2]: every (kv, l, t) group
+ * is quantised with its layer's bins. */
+int orc_quantize(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                 int64_t layer_stride, const int32_t *bins_k,
+                 const int32_t *bins_v, uint8_t *sym, uint16_t *max1)
+{
+    if (!orc_check_shape(L, T, C))
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    for (int kv = 0; kv < 2; kv++) {
+        const uint16_t *x = kv ? v : k;
+        const int32_t *bins = kv ? bins_v : bins_k;
+        for (int l = 0; l < L; l++)
+            for (int t = 0; t < T; t++) {
+                int64_t g = ((int64_t)kv * L + l) * T + t;
+                int st = orc_quantize_group(
+                    x + (int64_t)l * layer_stride + (int64_t)t * C, C, bins[l],
+                    sym + g * C, max1 + g);
+                if (st != ORC_OK)
+                    return st;
+            }
+    }
+    return ORC_OK;
+}
+
+/* [CG §2.3(2)] calculate_cdf, scoped per (chunk, kv, layer, channel) over the
+ * chunk's tokens [CG §2.3(3)]. */
+int orc_calculate_cdf(const uint8_t *sym, int L, int T, int C, int Tc,
+                      int A_k, int A_v, uint16_t *cdf)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1)
+        return ORC_ERR_ARG;
+    int nch = (T + Tc - 1) / Tc;
+    uint32_t n[256];
+    for (int k = 0; k < nch; k++) {
+        int Tk = orc_chunk_tokens(T, Tc, k);
+        for (int kv = 0; kv < 2; kv++) {
+            int A = kv ? A_v : A_k;
+            for (int l = 0; l < L; l++)
+                for (int c = 0; c < C; c++) {
+                    memset(n, 0, sizeof n);
+                    for (int tl = 0; tl < Tk; tl++) {
+                        int64_t t = (int64_t)k * Tc + tl;
+                        uint8_t s = sym[(((int64_t)kv * L + l) * T + t) * C + c];
+                        if (s >= A)
+                            return ORC_ERR_ARG;
+                        n[s]++;
+                    }
+                    int st = orc_cdf_from_counts(
+                        n, A, (uint32_t)Tk,
+                        cdf + orc_cdf_offset(L, C, A_k, A_v, k, kv, l, c));
+                    if (st != ORC_OK)
+                        return st;
+                }
+        }
+    }
+    return ORC_OK;
+}
+
+/* [CG §2.3(3), §1.2(3)] code every (chunk, kv, layer, token) stream over its
+ * channels and pack the streams in stream-id order. */
+int orc_encode(const uint8_t *sym, const uint16_t *cdf, int L, int T, int C,
+               int Tc, int A_k, int A_v, uint8_t *packed, uint64_t capacity,
+               uint32_t *len, uint64_t *off)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1)
+        return ORC_ERR_ARG;
+    int nch = (T + Tc - 1) / Tc;
+    int64_t cap = 2 * (int64_t)C + 8;
+    uint8_t *buf = (uint8_t *)malloc((size_t)cap);
+    if (!buf)
+        return ORC_ERR_NOMEM;
+    uint64_t total = 0;
+    int status = ORC_OK;
+    for (int k = 0; k < nch; k++) {
+        int Tk = orc_chunk_tokens(T, Tc, k);
+        for (int kv = 0; kv < 2; kv++) {
+            int A = kv ? A_v : A_k;
+            for (int l = 0; l < L; l++) {
+                const uint16_t *rows =
+                    cdf + orc_cdf_offset(L, C, A_k, A_v, k, kv, l, 0);
+                for (int tl = 0; tl < Tk; tl++) {
+                    int64_t t = (int64_t)k * Tc + tl;
+                    int64_t sid = orc_stream_id(L, T, Tc, k, kv, l, tl);
+                    const uint8_t *s =
+                        sym + (((int64_t)kv * L + l) * T + t) * C;
+                    int64_t n = orc_encode_stream(s, C, rows, A, A, buf, cap);
+                    if (n < 0) {
+                        free(buf);
+                        return ORC_ERR_ARG;
+                    }
+                    off[sid] = total;
+                    len[sid] = (uint32_t)n;
+                    /* bytes at or past capacity are not written */
+                    if (total + (uint64_t)n <= capacity) {
+                        memcpy(packed + total, buf, (size_t)n);
+                    } else {
+                        if (total < capacity)
+                            memcpy(packed + total, buf, (size_t)(capacity - total));
+                        status = ORC_ERR_CAPACITY;
+                    }
+                    total += (uint64_t)n;
+                }
+            }
+        }
+    }
+    off[orc_num_streams(L, T)] = total;
+    free(buf);
+    return status;
+}
+
+int orc_decode(const uint8_t *packed, const uint64_t *off, const uint32_t *len,
+               const uint16_t *cdf, int L, int T, int C, int Tc, int A_k,
+               int A_v, uint8_t *sym)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1)
+        return ORC_ERR_ARG;
+    int nch = (T + Tc - 1) / Tc;
+    int status = ORC_OK;
+    for (int k = 0; k < nch; k++) {
+        int Tk = orc_chunk_tokens(T, Tc, k);
+        for (int kv = 0; kv < 2; kv++) {
+            int A = kv ? A_v : A_k;
+            for (int l = 0; l < L; l++) {
+                const uint16_t *rows =
+                    cdf + orc_cdf_offset(L, C, A_k, A_v, k, kv, l, 0);
+                for (int tl = 0; tl < Tk; tl++) {
+                    int64_t t = (int64_t)k * Tc + tl;
+                    int64_t sid = orc_stream_id(L, T, Tc, k, kv, l, tl);
+                    int64_t used = 0;
+                    int st = orc_decode_stream(
+                        packed + off[sid], len[sid], C, rows, A, A,
+                        sym + (((int64_t)kv * L + l) * T + t) * C, &used);
+                    if (st != ORC_OK)
+                        status = st;
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/* [CG §2.4(2)] do_dequantize over the whole tensor, output binary32. */
+int orc_dequantize(const uint8_t *sym, const uint16_t *max1, int L, int T,
+                   int C, const int32_t *bins_k, const int32_t *bins_v,
+                   float *out_k, float *out_v)
+{
+    if (!orc_check_shape(L, T, C))
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    for (int kv = 0; kv < 2; kv++) {
+        float *out = kv ? out_v : out_k;
+        const int32_t *bins = kv ? bins_v : bins_k;
+        for (int l = 0; l < L; l++)
+            for (int t = 0; t < T; t++) {
+                int64_t g = ((int64_t)kv * L + l) * T + t;
+                for (int c = 0; c < C; c++)
+                    out[((int64_t)l * T + t) * C + c] = orc_dequantize_value(
+                        sym[g * C + c], bins[l], max1[g]);
+            }
+    }
+    return ORC_OK;
+}
+
+int orc_compress(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                 int Tc, int64_t layer_stride, const int32_t *bins_k,
+                 const int32_t *bins_v, uint16_t *max1, uint16_t *cdf,
+                 uint8_t *packed, uint64_t capacity, uint32_t *len,
+                 uint64_t *off)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1)
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
+    if (!sym)
+        return ORC_ERR_NOMEM;
+    int st = orc_quantize(k, v, L, T, C, layer_stride, bins_k, bins_v, sym,
+                          max1);
+    int A_k = orc_alphabet(bins_k, L), A_v = orc_alphabet(bins_v, L);
+    if (st == ORC_OK)
+        st = orc_calculate_cdf(sym, L, T, C, Tc, A_k, A_v, cdf);
+    if (st == ORC_OK)
+        st = orc_encode(sym, cdf, L, T, C, Tc, A_k, A_v, packed, capacity, len,
+                        off);
+    free(sym);
+    return st;
+}
+
+int orc_decompress(const uint8_t *packed, const uint64_t *off,
+                   const uint32_t *len, const uint16_t *cdf,
+                   const uint16_t *max1, int L, int T, int C, int Tc,
+                   const int32_t *bins_k, const int32_t *bins_v, float *out_k,
+                   float *out_v)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1)
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
+    if (!sym)
+        return ORC_ERR_NOMEM;
+    int A_k = orc_alphabet(bins_k, L), A_v = orc_alphabet(bins_v, L);
+    int st = orc_decode(packed, off, len, cdf, L, T, C, Tc, A_k, A_v, sym);
+    if (st == ORC_OK)
+        st = orc_dequantize(sym, max1, L, T, C, bins_k, bins_v, out_k, out_v);
+    free(sym);
+    return st;
+}

@@ -1,0 +1,160 @@
+/*
+ * cg_oracle.h - CPU oracle for the CacheGen KV-cache codec.
+ *
+ * TEST INFRASTRUCTURE ONLY. This is the plain, slow, single-threaded reference
+ * the CUDA library is checked against. Only the test suite, the smoke check and
+ * the CPU-baseline leg of the benchmark may load it. The product library never
+ * links it, calls it or falls back to it, and it shares no source with it.
+ *
+ * Citation key used throughout:
+ *   [CG] = web page "CacheGen 技术详解：KV Cache 的高效压缩与流式传输"
+ *          (CacheGen as implemented in LMCache, forceinjection.github.io).
+ *   [CG §2.3(1)] quantisation (torch_quant_vectorized), [CG §2.3(2)] CDF
+ *   (calculate_cdf), [CG §2.3(3)] 256-token chunks, [CG §1.2(3)] arithmetic
+ *   coding, [CG §2.4(1)] GPU decoding, [CG §2.4(2)] dequantisation
+ *   (do_dequantize), [CG §2.2] layer-wise bins (QuantizationSpec).
+ *
+ * The page states the quantisation and dequantisation formulas but gives no
+ * bit-stream format, CDF precision or coder constants. Those are fixed by the
+ * codec specification restated below; both this oracle and the CUDA library
+ * implement it independently.
+ *
+ * ---------------------------------------------------------------------------
+ * Codec specification (format version 1)
+ * ---------------------------------------------------------------------------
+ * Shapes: K and V are fp16 [L][T][C]; tokens are cut into chunks of Tc tokens
+ * (the last chunk may be shorter: Tc_k = min(Tc, T - k*Tc)); nch = ceil(T/Tc).
+ *
+ * Q  (quantise, per group (kv, layer l, token t), IEEE binary32, every
+ *    operation rounded to nearest-even on its own, no fused multiply-add):
+ *    MAX = bins_l / 2 - 1 (integer division); max1 = max_c |x_c| (an fp16
+ *    value, stored as fp16); factor = (float)MAX / max1;
+ *    y = (x * factor) + (float)MAX; q = rint(y) (ties to even), clamped to
+ *    [0, 2*MAX]. A group with max1 == 0 gives q = MAX everywhere. Non-finite
+ *    input is rejected. bins_l must lie in [4, 256].
+ *
+ * A  (alphabet width) A_K = max_l bins_k[l], A_V = max_l bins_v[l]; every
+ *    CDF of that tensor has A symbols 0..A-1.
+ *
+ * F  (CDF, per (chunk k, kv, l, channel c), over the chunk's Tc_k tokens):
+ *    n_s = count of q == s; f_s = 1 + floor(n_s * (65536 - A) / Tc_k);
+ *    R = 65536 - sum f_s (0 <= R < A) is added to the symbol with the largest
+ *    n_s (smallest s on ties); cdf[0] = 0, cdf[s+1] = cdf[s] + f_s; the A
+ *    entries cdf[0..A-1] are stored as uint16 (cdf[A] = 65536 is implicit).
+ *    Layout: cdf[k] = { K: [L][C][A_K], then V: [L][C][A_V] }.
+ *
+ * R  (range coder, one stream per (k, kv, l, t) over c = 0..C-1 ascending,
+ *    each symbol coded with cdf[k][kv][l][c]):
+ *    state low = 0, range = 0xFFFFFFFF (uint32).
+ *    encode s: r = range >> 16; low' = low + r*cdf[s] (mod 2^32); if low' <
+ *    low a carry adds one to the bytes already emitted (last byte first, 0xFF
+ *    becomes 0x00 and the carry moves on); low = low'; range = r * f_s;
+ *    while range < 2^24: emit low >> 24, low <<= 8, range <<= 8.
+ *    flush: v = low + 0x00FFFFFF (carry as above if it wraps); emit v >> 24.
+ *    decode: range = 0xFFFFFFFF, code = first 4 bytes big-endian; bytes at or
+ *    past the stream's length read as 0. Per symbol: r = range >> 16;
+ *    s = largest s with r*cdf[s] <= code; code -= r*cdf[s]; range = r*f_s;
+ *    while range < 2^24: code = (code << 8) | next byte, range <<= 8.
+ *    A valid stream of len bytes is consumed in exactly len + 3 bytes.
+ *
+ * P  (packing) stream id sid(k, kv, l, tl) = 2*L*Tc*k + (kv*L + l)*Tc_k + tl;
+ *    streams are stored back to back in sid order, len[] is uint32 per
+ *    stream, off[] the uint64 exclusive scan of len with off[nstreams] the
+ *    total; nstreams = 2*L*T. With a capacity below the total, exactly the
+ *    bytes at positions < capacity are written.
+ *
+ * D  (dequantise, binary32, no FMA): x^ = ((float)(q - MAX) / (float)MAX)
+ *    * (float)max1.
+ */
+#ifndef CG_ORACLE_H
+#define CG_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    ORC_OK = 0,
+    ORC_ERR_ARG = 1,
+    ORC_ERR_NONFINITE = 2,
+    ORC_ERR_CAPACITY = 3,
+    ORC_ERR_CORRUPT = 4,
+    ORC_ERR_NOMEM = 5
+};
+
+/* fp16 bits -> binary32 (exact). */
+float orc_half_to_float(uint16_t h);
+
+/* [CG §2.3(1)] one group of C fp16 values -> C symbols and the group's max1. */
+int orc_quantize_group(const uint16_t *x, int64_t C, int bins, uint8_t *q,
+                       uint16_t *max1);
+
+/* [CG §2.4(2)] one symbol -> binary32, given the group's max1 (fp16 bits). */
+float orc_dequantize_value(uint8_t q, int bins, uint16_t max1);
+
+/* [CG §2.3(2)] counts of A symbols over Tk tokens -> A uint16 CDF entries. */
+int orc_cdf_from_counts(const uint32_t *n, int A, uint32_t Tk, uint16_t *cdf);
+
+/* [CG §1.2(3)] encode n symbols; symbol i uses the CDF row cdf + i*row_stride
+ * (A entries). Writes at most cap bytes; returns the stream length or -1 when
+ * cap is too small or an argument is bad. */
+int64_t orc_encode_stream(const uint8_t *sym, int64_t n, const uint16_t *cdf,
+                          int64_t row_stride, int A, uint8_t *out, int64_t cap);
+
+/* [CG §2.4(1)] decode n symbols from a stream of len bytes. *consumed gets
+ * the number of bytes the decoder read (len + 3 for a valid stream). */
+int orc_decode_stream(const uint8_t *in, int64_t len, int64_t n,
+                      const uint16_t *cdf, int64_t row_stride, int A,
+                      uint8_t *sym, int64_t *consumed);
+
+/* Size helpers. */
+int64_t orc_num_streams(int L, int T);
+int64_t orc_cdf_elems(int L, int T, int C, int Tc, int A_k, int A_v);
+int64_t orc_cdf_offset(int L, int C, int A_k, int A_v, int k, int kv, int l,
+                       int c);
+int64_t orc_stream_id(int L, int T, int Tc, int k, int kv, int l, int tl);
+int orc_alphabet(const int32_t *bins, int L);
+
+/* Whole-tensor steps. k and v are fp16 [L][T][C] with layers layer_stride
+ * elements apart (tokens C apart, channels contiguous). sym is uint8
+ * [2][L][T][C], max1 fp16 [2][L][T]. bins_v == NULL means bins_v = bins_k. */
+int orc_quantize(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                 int64_t layer_stride, const int32_t *bins_k,
+                 const int32_t *bins_v, uint8_t *sym, uint16_t *max1);
+
+int orc_calculate_cdf(const uint8_t *sym, int L, int T, int C, int Tc,
+                      int A_k, int A_v, uint16_t *cdf);
+
+int orc_encode(const uint8_t *sym, const uint16_t *cdf, int L, int T, int C,
+               int Tc, int A_k, int A_v, uint8_t *packed, uint64_t capacity,
+               uint32_t *len, uint64_t *off);
+
+int orc_decode(const uint8_t *packed, const uint64_t *off, const uint32_t *len,
+               const uint16_t *cdf, int L, int T, int C, int Tc, int A_k,
+               int A_v, uint8_t *sym);
+
+int orc_dequantize(const uint8_t *sym, const uint16_t *max1, int L, int T,
+                   int C, const int32_t *bins_k, const int32_t *bins_v,
+                   float *out_k, float *out_v);
+
+/* Quantise -> CDF -> encode in one call (symbols kept in host scratch). */
+int orc_compress(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                 int Tc, int64_t layer_stride, const int32_t *bins_k,
+                 const int32_t *bins_v, uint16_t *max1, uint16_t *cdf,
+                 uint8_t *packed, uint64_t capacity, uint32_t *len,
+                 uint64_t *off);
+
+/* Decode -> dequantise in one call. */
+int orc_decompress(const uint8_t *packed, const uint64_t *off,
+                   const uint32_t *len, const uint16_t *cdf,
+                   const uint16_t *max1, int L, int T, int C, int Tc,
+                   const int32_t *bins_k, const int32_t *bins_v, float *out_k,
+                   float *out_v);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
