@@ -1,0 +1,358 @@
+#!/usr/bin/env python3
+"""Benchmark of the CacheGen KV codec on GB300: one step = compress
+(quantise -> CDF -> range-encode -> pack) plus decompress (decode fused with
+dequantisation) of one synthetic KV workload, resident in HBM.
+
+Prints one JSON line. Default workload: K and V fp16 [32, 4096, 1024] in 16
+chunks of 256 tokens (Llama-3.1-8B / Mistral-7B KV shape), bins 32 for layers
+0-9 and 16 for 10-31, AR(1) rho=0.9 values with 2% outlier channels, seed 2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU; each rank codes its own copy of
+the workload (seed + rank) with no collective on the data path (weak
+scaling); rank 0 prints the line with the max over ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV encode & decode GB/s (fp16 in) at 1 GB300, % of HBM roofline; compression ratio"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+KERNELS_PER_STEP = 6  # quantize, code_slices, tile_sums, scan_partials, offsets_and_pack, decode
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="ctx4096")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        self.out.flush()
+        with open(self.out.name) as fh:
+            rows = [r.strip().split(", ") for r in fh if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (IndexError, ValueError):
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "shape_per_kv": [w.L, w.T, w.C], "chunk_tokens": w.chunk_tokens,
+           "bins_k": sorted(set(w.bins_k)), "bins_layer_split": sum(1 for b in w.bins_k if b == max(w.bins_k)),
+           "values": w.describe(), "l2": "inputs > L2 and an L2-sized buffer written between timed steps"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, single thread, on a bounded sample
+# ---------------------------------------------------------------------------
+def oracle_step_time(k, v, w, tokens):
+    import oracle
+    ks = k[:, :tokens].copy()
+    vs = v[:, :tokens].copy()
+    t0 = time.perf_counter()
+    r = oracle.compress(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v)
+    oracle.decompress(r["packed"], r["off"], r["len"], r["cdf"], r["max1"], w.L, tokens, w.C,
+                      w.chunk_tokens, w.bins_k, w.bins_v)
+    dt = time.perf_counter() - t0
+    return dt, ks.nbytes + vs.nbytes
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle (the only reference implementation of
+    this method here) timed on the host cores, on bounded samples."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from kv_cache_compression_cg_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    tokens = min(w.T, w.chunk_tokens)
+    k, v = synth.generate(w, T=tokens)
+    for _ in range(args.warmup):
+        oracle_step_time(k, v, w, tokens)
+    times = []
+    nbytes = 0
+    for _ in range(args.steps):
+        dt, nbytes = oracle_step_time(k, v, w, tokens)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = nbytes / (ms * 1e-3) / 1e9
+    sample = f"first chunk ({tokens} tokens x {w.L} layers x {w.C} channels, K and V) per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, {"sample": sample}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from kv_cache_compression_cg_gb300 import build as cuda_build
+    if rank == 0:
+        cuda_build.build()
+    if world > 1:
+        dist.barrier()
+    from kv_cache_compression_cg_gb300 import codec, synth
+    import dataclasses
+
+    base = synth.WORKLOADS[args.workload]
+    w = dataclasses.replace(base, seed=base.seed + 1000 * rank) if rank else base
+    k_h, v_h = synth.generate(w)
+    fp16_bytes = k_h.nbytes + v_h.nbytes
+    k_pin = torch.from_numpy(k_h).pin_memory()
+    v_pin = torch.from_numpy(v_h).pin_memory()
+    k = k_pin.cuda()
+    v = v_pin.cuda()
+    stream = torch.cuda.current_stream()
+    cd = codec.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step():
+        cd.compress(k, v)
+        cd.decompress()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    out = cd.out
+    total = out.total_bytes()
+    status = int(out.status.item()) | int(cd.dstatus.item())
+
+    # timed region
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        cd.compress(k, v)
+        ev[i][1].record(stream)
+        cd.decompress()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    comp_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = sum(comp_ms) / len(comp_ms) + sum(dec_ms) / len(dec_ms)
+    region_ms = sum(comp_ms) + sum(dec_ms)
+    if world > 1:
+        t = torch.tensor([region_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        region_ms = float(t.item())
+        dist.barrier()
+    hbm, peak_kind = peaks()
+
+    # dominant kernel: decode fused with dequantisation (the only kernel of
+    # cg_decompress_chunk), timed alone with events on the launching stream
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in kev:
+        flush.zero_()
+        a.record(stream)
+        cd.decompress()
+        b.record(stream)
+    torch.cuda.synchronize()
+    dec_kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    n_el = 2 * w.L * w.T * w.C
+    cdf_bytes = 2 * cd.cdf_elems
+    side = cdf_bytes + 2 * 2 * w.L * w.T + 4 * cd.nstreams + 8 * (cd.nstreams + 1)
+    dec_alg_bytes = total + side + 4 * n_el
+    comp_alg_bytes = fp16_bytes + total + side
+    achieved = dec_alg_bytes / (dec_kernel_ms * 1e-3) / 1e9
+
+    comp_gbs = fp16_bytes / (statistics.mean(comp_ms) * 1e-3) / 1e9
+    dec_gbs = fp16_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9
+    value = world * fp16_bytes / (region_ms / args.steps * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": workload_config(w, {"parallelism": f"chunk-sharded x{world}" if world > 1 else "1 GPU"}),
+        "compress_gbs": comp_gbs, "decompress_gbs": dec_gbs,
+        "compress_ms": statistics.mean(comp_ms), "decompress_ms": statistics.mean(dec_ms),
+        "compress_frac_of_hbm": {"fp16_in": comp_gbs / hbm,
+                                 "algorithmic": comp_alg_bytes / (statistics.mean(comp_ms) * 1e-3) / 1e9 / hbm},
+        "decompress_frac_of_hbm": {"fp16_in": dec_gbs / hbm,
+                                   "algorithmic": dec_alg_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9 / hbm},
+        "compression_ratio": {"total": fp16_bytes / (total + side), "payload": fp16_bytes / total,
+                              "bits_per_symbol": 8 * total / n_el},
+        "roofline": {"kernel": "k_decode (decode + dequantise)", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None},
+        "status_word": status, "clocks": clocks, "wall_s_timed_region": wall,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = e2e(args, cd, k_pin, v_pin, k, v, fp16_bytes, stream)
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens))
+        reps = max(1, int(10.0 / max(cpu_dt, 1e-3)))
+        times = [cpu_dt]
+        for _ in range(min(reps, 20) - 1):
+            times.append(oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens))[0])
+        cpu_gbs = cpu_bytes / statistics.mean(times) / 1e9
+        result["cpu_baseline"] = {
+            "value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {min(w.T, 2 * w.chunk_tokens)} tokens (compress + decompress), "
+                      f"{len(times)} repetitions"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def e2e(args, cd, k_pin, v_pin, k, v, fp16_bytes, stream):
+    """Through the public API with host buffers: the sender copies fp16 K/V in,
+    compresses and copies the compressed chunk out; the receiver copies it in,
+    decompresses, and reads the status word back."""
+    import torch
+    o = cd.out
+    total = o.total_bytes()
+    host_packed = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    host_len = torch.empty_like(o.len, device="cpu").pin_memory()
+    host_off = torch.empty_like(o.off, device="cpu").pin_memory()
+    host_cdf = torch.empty_like(o.cdf, device="cpu").pin_memory()
+    host_max1 = torch.empty_like(o.max1, device="cpu").pin_memory()
+    host_status = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    from kv_cache_compression_cg_gb300 import codec as codec_mod
+    rx = codec_mod.Compressed(o.L, o.T, o.C, o.chunk_tokens, o.bins_k, o.bins_v,
+                              max1=torch.empty_like(o.max1), cdf=torch.empty_like(o.cdf),
+                              packed=torch.empty(max(total, 16), dtype=torch.uint8, device="cuda"),
+                              len=torch.empty_like(o.len), off=torch.empty_like(o.off),
+                              status=torch.zeros_like(o.status))
+    h2d = d2h = 0
+    times = []
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        k.copy_(k_pin, non_blocking=True)
+        v.copy_(v_pin, non_blocking=True)
+        cd.compress(k, v)
+        n = cd.out.total_bytes()  # 8-byte read, needed to size the copy
+        host_packed[:n].copy_(o.packed[:n], non_blocking=True)
+        for h, dsrc in ((host_len, o.len), (host_off, o.off), (host_cdf, o.cdf), (host_max1, o.max1)):
+            h.copy_(dsrc, non_blocking=True)
+        rx.packed[:n].copy_(host_packed[:n], non_blocking=True)
+        for dd, h in ((rx.len, host_len), (rx.off, host_off), (rx.cdf, host_cdf), (rx.max1, host_max1)):
+            dd.copy_(h, non_blocking=True)
+        cd.decompress(rx)
+        host_status.copy_(cd.dstatus, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+        side = (host_len.numel() * 4 + host_off.numel() * 8 + host_cdf.numel() * 2 +
+                host_max1.numel() * 2)
+        h2d = fp16_bytes + n + side
+        d2h = 8 + n + side + 4
+    sec = statistics.mean(times)
+    return {"value": fp16_bytes / sec / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": sec * 1e3,
+            "path": "pinned host fp16 K,V -> compress -> compressed chunk to host -> back to "
+                    "device -> decompress -> status word to host"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

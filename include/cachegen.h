@@ -1,0 +1,198 @@
+/*
+ * cachegen.h - C ABI of the GB300 (sm_103a) CacheGen KV-cache codec.
+ *
+ * Citation key: [CG] = web page "CacheGen 技术详解：KV Cache 的高效压缩与流式传输"
+ * (CacheGen as implemented in LMCache). Sections cited: §2.2 layer-wise bins
+ * (QuantizationSpec), §2.3(1) vectorised adaptive quantisation
+ * (torch_quant_vectorized), §2.3(2) CDF computation (calculate_cdf),
+ * §2.3(3) 256-token chunks, §1.2(3) GPU-parallel arithmetic coding,
+ * §2.4(1) GPU-parallel decoding (decode_function_gpu), §2.4(2)
+ * dequantisation (do_dequantize), §3.2 the (layers, 2, tokens, heads,
+ * head_dim) fp16 KV layout.
+ *
+ * Conventions
+ *  - Every data pointer is DEVICE memory owned by the caller, except the
+ *    bins arrays (HOST int32, read during the call and not kept).
+ *  - The library allocates nothing. Scratch comes from the caller through a
+ *    workspace pointer sized with cg_workspace_bytes().
+ *  - Every call is asynchronous on the caller's stream; nothing synchronises.
+ *  - fp16 values are passed as their IEEE binary16 bit patterns (uint16_t).
+ *  - The return value reports argument and launch errors, detected on the
+ *    host before (or at) launch. Errors that depend on the data are OR-ed as
+ *    CG_FLAG_* bits into an optional device int32 status word, which the
+ *    caller zeroes beforehand and reads after synchronising. Kernels never
+ *    assert or trap.
+ *
+ * Codec specification (format version 1; the page gives the quantisation and
+ * dequantisation formulas, this header fixes the rest):
+ *  Q  per group (kv, layer l, token t): MAX = bins_l / 2 - 1;
+ *     max1 = max_c |x_c| (kept as fp16); factor = (float)MAX / max1;
+ *     q = rint((x * factor) + (float)MAX) in binary32 with every operation
+ *     rounded on its own (ties to even), clamped to [0, 2*MAX]; a group with
+ *     max1 = 0 gives q = MAX. bins_l in [4, 256].
+ *  A  alphabet width A_K = max_l bins_k[l], A_V = max_l bins_v[l].
+ *  F  per (chunk k, kv, l, channel c) over the chunk's Tc_k tokens: counts
+ *     n_s; f_s = 1 + floor(n_s * (65536 - A) / Tc_k); the remainder
+ *     65536 - sum f_s goes to the symbol with the largest count (smallest s
+ *     on ties); cdf[s] = f_0 + ... + f_{s-1}, stored as uint16 cdf[0..A-1].
+ *     Layout per chunk: K rows [L][C][A_K] then V rows [L][C][A_V].
+ *  R  range coder, one stream per (k, kv, l, t) over channels c = 0..C-1,
+ *     symbol c coded with row (k, kv, l, c): low = 0, range = 0xFFFFFFFF;
+ *     r = range >> 16; low += r*cdf[s] (a wrap adds one to the bytes
+ *     already emitted, 0xFF bytes turning to 0x00); range = r*f_s; while
+ *     range < 2^24 emit low >> 24, shift low and range left by 8. Flush:
+ *     emit (low + 0x00FFFFFF) >> 24 (carrying as above). The decoder reads
+ *     bytes at or past the stream's length as 0 and consumes exactly
+ *     len + 3 bytes of a valid stream.
+ *  P  stream id sid(k, kv, l, tl) = 2*L*Tc*k + (kv*L + l)*Tc_k + tl with
+ *     Tc_k = min(Tc, T - k*Tc); streams stored back to back in sid order;
+ *     len[] uint32 per stream; off[] uint64 exclusive scan (off[nstreams]
+ *     = total); nstreams = 2*L*T.
+ *  D  x^ = ((float)(q - MAX) / (float)MAX) * (float)max1 in binary32.
+ */
+#ifndef CACHEGEN_GB300_H
+#define CACHEGEN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t cg_status;
+
+/* Return codes. */
+#define CG_OK 0
+#define CG_ERR_INVALID_ARG 1 /* null pointer, bad shape or bins, misaligned */
+#define CG_ERR_WORKSPACE 2   /* workspace smaller than cg_workspace_bytes() */
+#define CG_ERR_CUDA 3        /* a kernel launch failed (cudaGetLastError) */
+
+/* Device status bits (OR-ed into *status when status != NULL). */
+#define CG_FLAG_NONFINITE 0x1 /* an input value was Inf or NaN (Q) */
+#define CG_FLAG_CAPACITY 0x2  /* packed total exceeded capacity (P) */
+#define CG_FLAG_CORRUPT 0x4   /* a stream did not decode in len + 3 bytes,
+                                 or off/len point outside the buffer (R) */
+#define CG_FLAG_BAD_SYMBOL 0x8 /* encode input symbol >= A */
+
+/* Limits of this implementation. */
+#define CG_MAX_LAYERS 1024
+#define CG_MAX_CHUNK_TOKENS 1024
+#define CG_MAX_CHANNELS 65536
+
+/* Shape of one K (or V) tensor, fp16 [L][T][C]: channels contiguous, tokens
+ * C elements apart, layers layer_stride elements apart (layer_stride = T*C
+ * when contiguous; 2*T*C for K and V views of the [layers][2][tokens][heads]
+ * [head_dim] layout of [CG §3.2], where C = heads*head_dim and V starts T*C
+ * elements after K). chunk_tokens is the CDF and streaming unit [CG §2.3(3)]
+ * (256 by default); the last chunk may be shorter. */
+typedef struct cg_shape {
+    int32_t L;
+    int32_t T;
+    int32_t C;
+    int32_t chunk_tokens;
+    int64_t layer_stride;
+} cg_shape;
+
+/* ---- sizes (host only, no device work) --------------------------------- */
+
+/* 2*L*T, or 0 for an invalid shape. */
+uint64_t cg_num_streams(const cg_shape *shape);
+
+/* Number of uint16 CDF entries: nch * L * C * (A_K + A_V), or 0 when the
+ * shape or the bins are invalid. bins_v == NULL means bins_v = bins_k. */
+uint64_t cg_cdf_elems(const cg_shape *shape, const int32_t *bins_k,
+                      const int32_t *bins_v);
+
+/* Upper bound of the packed size: nstreams * (2*C + 8) bytes. With
+ * capacity >= this bound CG_FLAG_CAPACITY cannot occur. */
+uint64_t cg_max_compressed_bytes(const cg_shape *shape);
+
+/* Bytes of device workspace cg_encode / cg_compress_chunk need (per-stream
+ * staging plus scan partials); 0 for an invalid shape. */
+uint64_t cg_workspace_bytes(const cg_shape *shape);
+
+/* ---- steps ------------------------------------------------------------- */
+
+/* [CG §2.3(1), §2.2] Quantise K and V (fp16 bits, see cg_shape) with the
+ * layer-wise bins. Outputs: sym uint8 [2][L][T][C] (K then V), max1 fp16
+ * bits [2][L][T]. k, v must be 2-byte aligned. Sets CG_FLAG_NONFINITE in
+ * *status on Inf/NaN input (outputs then unspecified for those groups). */
+cg_status cg_quantize(const uint16_t *k, const uint16_t *v,
+                      const cg_shape *shape, const int32_t *bins_k,
+                      const int32_t *bins_v, uint8_t *sym, uint16_t *max1,
+                      int32_t *status, cudaStream_t stream);
+
+/* [CG §2.3(2)] Per (chunk, kv, layer, channel) CDFs of the symbols
+ * sym [2][L][T][C] (symbols must be < the tensor's A); output cdf has
+ * cg_cdf_elems() uint16 entries in the layout of F above. */
+cg_status cg_calculate_cdf(const uint8_t *sym, const cg_shape *shape,
+                           const int32_t *bins_k, const int32_t *bins_v,
+                           uint16_t *cdf, int32_t *status,
+                           cudaStream_t stream);
+
+/* [CG §1.2(3), §2.3(3)] Range-code every (chunk, kv, layer, token) stream of
+ * sym with the given CDFs and pack them. Outputs: packed bytes (only
+ * positions < capacity are written), len uint32 [nstreams], off uint64
+ * [nstreams + 1] (the total is off[nstreams], on the device). workspace
+ * must hold cg_workspace_bytes(shape) bytes, 256-byte aligned. */
+cg_status cg_encode(const uint8_t *sym, const uint16_t *cdf,
+                    const cg_shape *shape, const int32_t *bins_k,
+                    const int32_t *bins_v, uint8_t *packed, uint64_t capacity,
+                    uint32_t *len, uint64_t *off, void *workspace,
+                    uint64_t workspace_bytes, int32_t *status,
+                    cudaStream_t stream);
+
+/* [CG §2.4(1)] Decode every stream back to symbols sym [2][L][T][C].
+ * packed_bytes is the readable size of packed; bytes a stream would read at
+ * or past its len (or past packed_bytes) read as 0. A stream not consumed in
+ * exactly len + 3 bytes, or lying outside packed_bytes, sets
+ * CG_FLAG_CORRUPT. */
+cg_status cg_decode(const uint8_t *packed, uint64_t packed_bytes,
+                    const uint64_t *off, const uint32_t *len,
+                    const uint16_t *cdf, const cg_shape *shape,
+                    const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym,
+                    int32_t *status, cudaStream_t stream);
+
+/* [CG §2.4(2)] Dequantise sym [2][L][T][C] with max1 [2][L][T] into binary32
+ * out_k, out_v, each [L][T][C] contiguous. */
+cg_status cg_dequantize(const uint8_t *sym, const uint16_t *max1,
+                        const cg_shape *shape, const int32_t *bins_k,
+                        const int32_t *bins_v, float *out_k, float *out_v,
+                        int32_t *status, cudaStream_t stream);
+
+/* ---- fused ------------------------------------------------------------- */
+
+/* Quantise -> CDF -> encode -> pack in one call (the serializer's to_bytes
+ * [CG §2.1, §3.2]); same outputs as the steps above, without a symbol
+ * tensor. workspace must hold cg_compress_workspace_bytes(shape) bytes,
+ * 256-byte aligned. */
+uint64_t cg_compress_workspace_bytes(const cg_shape *shape);
+
+cg_status cg_compress_chunk(const uint16_t *k, const uint16_t *v,
+                            const cg_shape *shape, const int32_t *bins_k,
+                            const int32_t *bins_v, uint16_t *max1,
+                            uint16_t *cdf, uint8_t *packed, uint64_t capacity,
+                            uint32_t *len, uint64_t *off, void *workspace,
+                            uint64_t workspace_bytes, int32_t *status,
+                            cudaStream_t stream);
+
+/* Decode fused with dequantisation (the deserializer [CG §2.4]): packed
+ * streams -> binary32 out_k, out_v [L][T][C]. */
+cg_status cg_decompress_chunk(const uint8_t *packed, uint64_t packed_bytes,
+                              const uint64_t *off, const uint32_t *len,
+                              const uint16_t *cdf, const uint16_t *max1,
+                              const cg_shape *shape, const int32_t *bins_k,
+                              const int32_t *bins_v, float *out_k,
+                              float *out_v, int32_t *status,
+                              cudaStream_t stream);
+
+/* Library version string ("cachegen-gb300 <format> <build>"). */
+const char *cg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

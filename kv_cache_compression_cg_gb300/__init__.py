@@ -1,0 +1,18 @@
+"""CacheGen KV-cache codec for GB300 (sm_103a).
+
+The codec itself is the C ABI in include/cachegen.h, implemented by the CUDA
+library libcachegen_gb300.so built from csrc/ (``python -m
+kv_cache_compression_cg_gb300.build``). ``capi`` is the ctypes binding with the
+same function names; ``codec`` wraps it for PyTorch tensors (PyTorch supplies
+device memory and streams only). ``synth`` is the seeded input generator.
+"""
+from __future__ import annotations
+
+__all__ = ["capi", "codec", "synth", "build"]
+
+
+def __getattr__(name):
+    import importlib
+    if name in ("capi", "codec", "synth", "build"):
+        return importlib.import_module(f"{__name__}.{name}")
+    raise AttributeError(name)

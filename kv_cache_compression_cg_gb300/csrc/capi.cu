@@ -1,0 +1,254 @@
+// capi.cu - the C ABI of include/cachegen.h: argument checks on the host,
+// workspace carving, and kernel launches on the caller's stream. Nothing here
+// allocates or synchronises.
+#include <cstring>
+
+#include "cg_internal.cuh"
+
+namespace {
+
+using cg::Dims;
+using cg::MaxTab;
+
+constexpr uint64_t kAlign = 256;
+
+uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+bool shape_ok(const cg_shape *s) {
+    if (!s) return false;
+    if (s->L < 1 || s->L > CG_MAX_LAYERS) return false;
+    if (s->T < 0) return false;
+    if (s->C < 1 || s->C > CG_MAX_CHANNELS) return false;
+    if (s->chunk_tokens < 1 || s->chunk_tokens > CG_MAX_CHUNK_TOKENS) return false;
+    if (s->layer_stride < (int64_t)s->T * s->C) return false;
+    return true;
+}
+
+bool bins_ok(const int32_t *b, int L) {
+    if (!b) return false;
+    for (int l = 0; l < L; l++)
+        if (b[l] < 4 || b[l] > 256) return false;
+    return true;
+}
+
+int alphabet(const int32_t *b, int L) {
+    int a = 0;
+    for (int l = 0; l < L; l++) a = b[l] > a ? b[l] : a;
+    return a;
+}
+
+uint64_t stage_bytes_per_stream(int C) {
+    // longest stream is 2*C + 8 bytes; the last word store may run 3 past it
+    return round_up(2ull * (uint64_t)C + 12ull, 16);
+}
+
+// Fill dims and the MAX table; false on invalid shape/bins.
+bool prepare(const cg_shape *s, const int32_t *bins_k, const int32_t *bins_v, Dims &d, MaxTab *mt) {
+    if (!shape_ok(s)) return false;
+    if (!bins_v) bins_v = bins_k;
+    if (!bins_ok(bins_k, s->L) || !bins_ok(bins_v, s->L)) return false;
+    d.L = s->L;
+    d.T = s->T;
+    d.C = s->C;
+    d.Tc = s->chunk_tokens;
+    d.nch = (s->T + s->chunk_tokens - 1) / s->chunk_tokens;
+    d.A[0] = alphabet(bins_k, s->L);
+    d.A[1] = alphabet(bins_v, s->L);
+    d.layer_stride = s->layer_stride;
+    d.nstreams = 2LL * s->L * s->T;
+    d.stage_bytes = (long long)stage_bytes_per_stream(s->C);
+    if (mt) {
+        std::memset(mt, 0, sizeof(*mt));
+        for (int l = 0; l < s->L; l++) {
+            mt->v[0][l] = (unsigned char)(bins_k[l] / 2 - 1);
+            mt->v[1][l] = (unsigned char)(bins_v[l] / 2 - 1);
+        }
+    }
+    return true;
+}
+
+struct Workspace {
+    uint8_t *stage;
+    unsigned long long *partials;
+    uint8_t *sym;
+};
+
+uint64_t encode_ws_bytes(const Dims &d) {
+    const uint64_t stage = round_up((uint64_t)d.nstreams * (uint64_t)d.stage_bytes, kAlign);
+    const uint64_t parts = round_up(8ull * (uint64_t)(cg::scan_tiles(d.nstreams) + 1), kAlign);
+    return stage + parts;
+}
+
+uint64_t sym_bytes(const Dims &d) { return round_up(2ull * d.L * (uint64_t)d.T * d.C, kAlign); }
+
+Workspace carve(void *ws, const Dims &d, bool with_sym) {
+    Workspace w;
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    w.stage = p;
+    p += round_up((uint64_t)d.nstreams * (uint64_t)d.stage_bytes, kAlign);
+    w.partials = reinterpret_cast<unsigned long long *>(p);
+    p += round_up(8ull * (uint64_t)(cg::scan_tiles(d.nstreams) + 1), kAlign);
+    w.sym = with_sym ? p : nullptr;
+    return w;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cg_status launched(cudaError_t e) { return e == cudaSuccess ? CG_OK : CG_ERR_CUDA; }
+
+// Empty token range: only off[0] = 0 has to be written.
+cg_status empty_offsets(uint64_t *off, cudaStream_t stream) {
+    if (!off) return CG_OK;
+    return launched(cudaMemsetAsync(off, 0, sizeof(uint64_t), stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+uint64_t cg_num_streams(const cg_shape *shape) {
+    return shape_ok(shape) ? 2ull * (uint64_t)shape->L * (uint64_t)shape->T : 0;
+}
+
+uint64_t cg_cdf_elems(const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v) {
+    Dims d;
+    if (!prepare(shape, bins_k, bins_v, d, nullptr)) return 0;
+    return (uint64_t)d.nch * d.L * (uint64_t)d.C * (uint64_t)(d.A[0] + d.A[1]);
+}
+
+uint64_t cg_max_compressed_bytes(const cg_shape *shape) {
+    if (!shape_ok(shape)) return 0;
+    return 2ull * shape->L * (uint64_t)shape->T * (2ull * shape->C + 8ull);
+}
+
+uint64_t cg_workspace_bytes(const cg_shape *shape) {
+    if (!shape_ok(shape)) return 0;
+    Dims d;
+    int32_t b[CG_MAX_LAYERS];
+    for (int l = 0; l < shape->L; l++) b[l] = 4;
+    prepare(shape, b, b, d, nullptr);
+    return encode_ws_bytes(d);
+}
+
+uint64_t cg_compress_workspace_bytes(const cg_shape *shape) {
+    if (!shape_ok(shape)) return 0;
+    Dims d;
+    int32_t b[CG_MAX_LAYERS];
+    for (int l = 0; l < shape->L; l++) b[l] = 4;
+    prepare(shape, b, b, d, nullptr);
+    return encode_ws_bytes(d) + sym_bytes(d);
+}
+
+const char *cg_version(void) { return "cachegen-gb300 format-1 sm_103a"; }
+
+cg_status cg_quantize(const uint16_t *k, const uint16_t *v, const cg_shape *shape,
+                      const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym, uint16_t *max1,
+                      int32_t *status, cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
+    if (!k || !v || !sym || !max1 || !aligned(k, 2) || !aligned(v, 2) || !aligned(max1, 2))
+        return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    return launched(cg::launch_quantize(k, v, d, mt, sym, max1, status, stream));
+}
+
+cg_status cg_calculate_cdf(const uint8_t *sym, const cg_shape *shape, const int32_t *bins_k,
+                           const int32_t *bins_v, uint16_t *cdf, int32_t *status,
+                           cudaStream_t stream) {
+    Dims d;
+    if (!prepare(shape, bins_k, bins_v, d, nullptr)) return CG_ERR_INVALID_ARG;
+    if (!sym || !cdf || !aligned(cdf, 2)) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    return launched(cg::launch_code_slices(sym, nullptr, cdf, nullptr, nullptr, d, 0, status, stream));
+}
+
+cg_status cg_encode(const uint8_t *sym, const uint16_t *cdf, const cg_shape *shape,
+                    const int32_t *bins_k, const int32_t *bins_v, uint8_t *packed,
+                    uint64_t capacity, uint32_t *len, uint64_t *off, void *workspace,
+                    uint64_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    Dims d;
+    if (!prepare(shape, bins_k, bins_v, d, nullptr)) return CG_ERR_INVALID_ARG;
+    if (!off) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return empty_offsets(off, stream);
+    if (!sym || !cdf || !len || !workspace || (!packed && capacity > 0)) return CG_ERR_INVALID_ARG;
+    if (!aligned(cdf, 2) || !aligned(len, 4) || !aligned(off, 8) || !aligned(workspace, kAlign))
+        return CG_ERR_INVALID_ARG;
+    if (workspace_bytes < encode_ws_bytes(d)) return CG_ERR_WORKSPACE;
+    Workspace w = carve(workspace, d, false);
+    cudaError_t e = cg::launch_code_slices(sym, cdf, nullptr, w.stage, len, d, 1, status, stream);
+    if (e != cudaSuccess) return CG_ERR_CUDA;
+    return launched(cg::launch_scan_and_pack(len, off, w.stage, packed, capacity, w.partials, d,
+                                             status, stream));
+}
+
+cg_status cg_decode(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
+                    const uint32_t *len, const uint16_t *cdf, const cg_shape *shape,
+                    const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym, int32_t *status,
+                    cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    if (!packed || !off || !len || !cdf || !sym) return CG_ERR_INVALID_ARG;
+    if (!aligned(packed, 4) || !aligned(off, 8) || !aligned(len, 4) || !aligned(cdf, 2))
+        return CG_ERR_INVALID_ARG;
+    return launched(cg::launch_decode(packed, packed_bytes, off, len, cdf, nullptr, d, mt, 0, sym,
+                                      nullptr, nullptr, status, stream));
+}
+
+cg_status cg_dequantize(const uint8_t *sym, const uint16_t *max1, const cg_shape *shape,
+                        const int32_t *bins_k, const int32_t *bins_v, float *out_k, float *out_v,
+                        int32_t *status, cudaStream_t stream) {
+    (void)status;
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    if (!sym || !max1 || !out_k || !out_v || !aligned(max1, 2) || !aligned(out_k, 16) ||
+        !aligned(out_v, 16) || !aligned(sym, 4))
+        return CG_ERR_INVALID_ARG;
+    return launched(cg::launch_dequantize(sym, max1, d, mt, out_k, out_v, stream));
+}
+
+cg_status cg_compress_chunk(const uint16_t *k, const uint16_t *v, const cg_shape *shape,
+                            const int32_t *bins_k, const int32_t *bins_v, uint16_t *max1,
+                            uint16_t *cdf, uint8_t *packed, uint64_t capacity, uint32_t *len,
+                            uint64_t *off, void *workspace, uint64_t workspace_bytes,
+                            int32_t *status, cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
+    if (!off) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return empty_offsets(off, stream);
+    if (!k || !v || !max1 || !cdf || !len || !workspace || (!packed && capacity > 0))
+        return CG_ERR_INVALID_ARG;
+    if (!aligned(k, 2) || !aligned(v, 2) || !aligned(max1, 2) || !aligned(cdf, 2) ||
+        !aligned(len, 4) || !aligned(off, 8) || !aligned(workspace, kAlign))
+        return CG_ERR_INVALID_ARG;
+    if (workspace_bytes < encode_ws_bytes(d) + sym_bytes(d)) return CG_ERR_WORKSPACE;
+    Workspace w = carve(workspace, d, true);
+    if (cg::launch_quantize(k, v, d, mt, w.sym, max1, status, stream) != cudaSuccess) return CG_ERR_CUDA;
+    if (cg::launch_code_slices(w.sym, nullptr, cdf, w.stage, len, d, 2, status, stream) != cudaSuccess)
+        return CG_ERR_CUDA;
+    return launched(cg::launch_scan_and_pack(len, off, w.stage, packed, capacity, w.partials, d,
+                                             status, stream));
+}
+
+cg_status cg_decompress_chunk(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
+                              const uint32_t *len, const uint16_t *cdf, const uint16_t *max1,
+                              const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v,
+                              float *out_k, float *out_v, int32_t *status, cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    if (!packed || !off || !len || !cdf || !max1 || !out_k || !out_v) return CG_ERR_INVALID_ARG;
+    if (!aligned(packed, 4) || !aligned(off, 8) || !aligned(len, 4) || !aligned(cdf, 2) ||
+        !aligned(max1, 2) || !aligned(out_k, 16) || !aligned(out_v, 16))
+        return CG_ERR_INVALID_ARG;
+    return launched(cg::launch_decode(packed, packed_bytes, off, len, cdf, max1, d, mt, 1, nullptr,
+                                      out_k, out_v, status, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// cg_internal.cuh - shared device-side definitions of the sm_103a codec.
+//
+// Layouts follow the codec specification in include/cachegen.h (format 1).
+// Citation key: [CG] = web page "CacheGen 技术详解：KV Cache 的高效压缩与流式传输".
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/cachegen.h"
+
+namespace cg {
+
+// Per-call geometry, passed by value to every kernel.
+struct Dims {
+    int L, T, C, Tc;       // layers, tokens, channels, tokens per chunk
+    int nch;               // number of chunks
+    int A[2];              // alphabet width of K and V
+    long long layer_stride;  // elements between layers of the fp16 input
+    long long nstreams;      // 2*L*T
+    long long stage_bytes;   // per-stream staging bytes in the workspace
+};
+
+// MAX = bins / 2 - 1 per (kv, layer) [CG §2.3(1)], in kernel parameter space.
+struct MaxTab {
+    unsigned char v[2][CG_MAX_LAYERS];
+};
+
+__host__ __device__ inline int chunk_tokens(const Dims &d, int k) {
+    int rest = d.T - k * d.Tc;
+    return rest < d.Tc ? rest : d.Tc;
+}
+
+// First stream id of chunk k; stream (k, kv, l, tl) = base + (kv*L + l)*Tc_k + tl.
+__host__ __device__ inline long long chunk_stream_base(const Dims &d, int k) {
+    return 2LL * d.L * d.Tc * k;
+}
+
+// First CDF entry of (k, kv, l); row c follows at + c*A[kv].
+__host__ __device__ inline long long cdf_slice_offset(const Dims &d, int k, int kv, int l) {
+    long long per_chunk = (long long)d.L * d.C * (d.A[0] + d.A[1]);
+    long long tensor = kv ? (long long)d.L * d.C * d.A[0] : 0;
+    return per_chunk * k + tensor + (long long)l * d.C * d.A[kv];
+}
+
+// Symbols [2][L][T][C] and max1 [2][L][T].
+__host__ __device__ inline long long group_index(const Dims &d, int kv, int l, long long t) {
+    return ((long long)kv * d.L + l) * d.T + t;
+}
+
+// Work unit of the coders: one (chunk, kv, layer) slice of Tc_k streams.
+__host__ __device__ inline void slice_coords(const Dims &d, long long b, int &k, int &kv, int &l) {
+    l = (int)(b % d.L);
+    long long r = b / d.L;
+    kv = (int)(r % 2);
+    k = (int)(r / 2);
+}
+
+// Scan helper sizes.
+constexpr int kScanBlock = 1024;      // threads per scan block
+constexpr int kScanItems = 2;         // items per thread
+constexpr int kScanTile = kScanBlock * kScanItems;
+
+__host__ __device__ inline long long scan_tiles(long long n) {
+    return (n + kScanTile - 1) / kScanTile;
+}
+
+// ---- launchers (each returns cudaGetLastError()) --------------------------
+cudaError_t launch_quantize(const uint16_t *k, const uint16_t *v, const Dims &d,
+                            const MaxTab &mt, uint8_t *sym, uint16_t *max1,
+                            int32_t *status, cudaStream_t s);
+
+// mode: 0 = count + build CDF only (cdf_out), 1 = encode with cdf_in,
+//       2 = count + build CDF (cdf_out) + encode.
+cudaError_t launch_code_slices(const uint8_t *sym, const uint16_t *cdf_in,
+                               uint16_t *cdf_out, uint8_t *stage, uint32_t *len,
+                               const Dims &d, int mode, int32_t *status,
+                               cudaStream_t s);
+
+cudaError_t launch_scan_and_pack(const uint32_t *len, uint64_t *off,
+                                 const uint8_t *stage, uint8_t *packed,
+                                 uint64_t capacity, unsigned long long *partials,
+                                 const Dims &d, int32_t *status, cudaStream_t s);
+
+// mode: 0 = symbols out (sym), 1 = dequantised binary32 out (out_k, out_v).
+cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes,
+                          const uint64_t *off, const uint32_t *len,
+                          const uint16_t *cdf, const uint16_t *max1,
+                          const Dims &d, const MaxTab &mt, int mode, uint8_t *sym,
+                          float *out_k, float *out_v, int32_t *status,
+                          cudaStream_t s);
+
+cudaError_t launch_dequantize(const uint8_t *sym, const uint16_t *max1,
+                              const Dims &d, const MaxTab &mt, float *out_k,
+                              float *out_v, cudaStream_t s);
+
+}  // namespace cg
