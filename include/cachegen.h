@@ -189,6 +189,37 @@ cg_status cg_decompress_chunk(const uint8_t *packed, uint64_t packed_bytes,
                               float *out_v, int32_t *status,
                               cudaStream_t stream);
 
+/* Compress without a workspace argument. The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory at all,
+ * such as code living inside a host framework whose memory pool owns every
+ * device byte and hands the codec only the tensors it works on, or a
+ * latency-critical path that must not take cudaMalloc's implicit device
+ * synchronisation. Inputs and outputs are as in cg_compress_chunk; the
+ * scratch is a static device array inside the library of
+ * CG_NOALLOC_WORKSPACE_BYTES (64 MiB, enough for one 256-token chunk of a
+ * 32-layer, 1024-channel KV cache), which every GPU that loads the library
+ * holds until the process exits.
+ *  - Returns CG_ERR_WORKSPACE, doing nothing, when the shape needs more than
+ *    CG_NOALLOC_WORKSPACE_BYTES (cg_compress_workspace_bytes(shape) >
+ *    CG_NOALLOC_WORKSPACE_BYTES); CG_ERR_INVALID_ARG for an invalid shape.
+ *  - Calls no allocating routine. The first call on each device looks the
+ *    array's device address up (cudaGetSymbolAddress, with that device
+ *    current) and caches it; make that first call before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents (no byte of it is read before the same call wrote it). Calls
+ *    that overlap on the GPU (other streams, other host threads) race on it:
+ *    serialise them. */
+#define CG_NOALLOC_WORKSPACE_BYTES (64ull << 20)
+
+cg_status cg_compress_chunk_noalloc(const uint16_t *k, const uint16_t *v,
+                                    const cg_shape *shape,
+                                    const int32_t *bins_k,
+                                    const int32_t *bins_v, uint16_t *max1,
+                                    uint16_t *cdf, uint8_t *packed,
+                                    uint64_t capacity, uint32_t *len,
+                                    uint64_t *off, int32_t *status,
+                                    cudaStream_t stream);
+
 /* Library version string ("cachegen-gb300 <format> <build>"). */
 const char *cg_version(void);
 

@@ -15,6 +15,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "cachegen.h")
 CG_OK, CG_ERR_INVALID_ARG, CG_ERR_WORKSPACE, CG_ERR_CUDA = 0, 1, 2, 3
 CG_FLAG_NONFINITE, CG_FLAG_CAPACITY, CG_FLAG_CORRUPT, CG_FLAG_BAD_SYMBOL = 0x1, 0x2, 0x4, 0x8
 CG_MAX_LAYERS, CG_MAX_CHUNK_TOKENS, CG_MAX_CHANNELS = 1024, 1024, 65536
+CG_NOALLOC_WORKSPACE_BYTES = 64 << 20
 
 _ERRORS = {CG_ERR_INVALID_ARG: "invalid argument", CG_ERR_WORKSPACE: "workspace too small",
            CG_ERR_CUDA: "CUDA launch failed"}
@@ -47,6 +48,7 @@ SIGNATURES = {
     "cg_compress_chunk": (_i32, [_p, _p, _SHAPE, _p, _p, _p, _p, _p, _u64, _p, _p, _p, _u64,
                                  _p, _p]),
     "cg_decompress_chunk": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, _p, _p, _p, _p]),
+    "cg_compress_chunk_noalloc": (_i32, [_p, _p, _SHAPE, _p, _p, _p, _p, _p, _u64, _p, _p, _p, _p]),
     "cg_version": (C.c_char_p, []),
 }
 
