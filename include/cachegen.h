@@ -76,6 +76,8 @@ typedef int32_t cg_status;
 #define CG_FLAG_CORRUPT 0x4   /* a stream did not decode in len + 3 bytes,
                                  or off/len point outside the buffer (R) */
 #define CG_FLAG_BAD_SYMBOL 0x8 /* encode input symbol >= A */
+#define CG_FLAG_TIMEOUT 0x10   /* a bounded wait for another CTA ran out;
+                                  offsets and packed bytes are not valid */
 
 /* Limits of this implementation. */
 #define CG_MAX_LAYERS 1024

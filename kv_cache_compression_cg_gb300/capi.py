@@ -14,6 +14,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "cachegen.h")
 
 CG_OK, CG_ERR_INVALID_ARG, CG_ERR_WORKSPACE, CG_ERR_CUDA = 0, 1, 2, 3
 CG_FLAG_NONFINITE, CG_FLAG_CAPACITY, CG_FLAG_CORRUPT, CG_FLAG_BAD_SYMBOL = 0x1, 0x2, 0x4, 0x8
+CG_FLAG_TIMEOUT = 0x10
 CG_MAX_LAYERS, CG_MAX_CHUNK_TOKENS, CG_MAX_CHANNELS = 1024, 1024, 65536
 CG_NOALLOC_WORKSPACE_BYTES = 64 << 20
 

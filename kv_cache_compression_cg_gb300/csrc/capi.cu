@@ -38,8 +38,9 @@ int alphabet(const int32_t *b, int L) {
 }
 
 uint64_t stage_bytes_per_stream(int C) {
-    // longest stream is 2*C + 8 bytes; the last word store may run 3 past it
-    return round_up(2ull * (uint64_t)C + 12ull, 16);
+    // slack prefix, then up to 2*C + 8 stream bytes; the last word store may
+    // run 3 bytes past the stream's end
+    return cg::kStagePrefix + round_up(2ull * (uint64_t)C + 12ull, 16);
 }
 
 // Fill dims and the MAX table; false on invalid shape/bins.
@@ -71,6 +72,7 @@ struct Workspace {
     uint8_t *stage;
     unsigned long long *partials;
     uint8_t *sym;
+    unsigned long long *state;  // fused compress: ticket + one look-back slot per slice
 };
 
 uint64_t encode_ws_bytes(const Dims &d) {
@@ -81,6 +83,8 @@ uint64_t encode_ws_bytes(const Dims &d) {
 
 uint64_t sym_bytes(const Dims &d) { return round_up(2ull * d.L * (uint64_t)d.T * d.C, kAlign); }
 
+uint64_t state_bytes(const Dims &d) { return round_up(8ull * (2ull * d.L * d.nch + 1), kAlign); }
+
 Workspace carve(void *ws, const Dims &d, bool with_sym) {
     Workspace w;
     uint8_t *p = static_cast<uint8_t *>(ws);
@@ -89,6 +93,8 @@ Workspace carve(void *ws, const Dims &d, bool with_sym) {
     w.partials = reinterpret_cast<unsigned long long *>(p);
     p += round_up(8ull * (uint64_t)(cg::scan_tiles(d.nstreams) + 1), kAlign);
     w.sym = with_sym ? p : nullptr;
+    if (with_sym) p += sym_bytes(d);
+    w.state = with_sym ? reinterpret_cast<unsigned long long *>(p) : nullptr;
     return w;
 }
 
@@ -136,7 +142,7 @@ uint64_t cg_compress_workspace_bytes(const cg_shape *shape) {
     int32_t b[CG_MAX_LAYERS];
     for (int l = 0; l < shape->L; l++) b[l] = 4;
     prepare(shape, b, b, d, nullptr);
-    return encode_ws_bytes(d) + sym_bytes(d);
+    return encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d);
 }
 
 const char *cg_version(void) { return "cachegen-gb300 format-1 sm_103a"; }
@@ -226,8 +232,11 @@ cg_status cg_compress_chunk(const uint16_t *k, const uint16_t *v, const cg_shape
     if (!aligned(k, 2) || !aligned(v, 2) || !aligned(max1, 2) || !aligned(cdf, 2) ||
         !aligned(len, 4) || !aligned(off, 8) || !aligned(workspace, kAlign))
         return CG_ERR_INVALID_ARG;
-    if (workspace_bytes < encode_ws_bytes(d) + sym_bytes(d)) return CG_ERR_WORKSPACE;
+    if (workspace_bytes < encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d)) return CG_ERR_WORKSPACE;
     Workspace w = carve(workspace, d, true);
+    if (cg::compress_fused_applies(d, k, v))
+        return launched(cg::launch_compress_fused(k, v, d, mt, max1, cdf, w.stage, len, off, packed,
+                                                  capacity, w.state, status, stream));
     if (cg::launch_quantize(k, v, d, mt, w.sym, max1, status, stream) != cudaSuccess) return CG_ERR_CUDA;
     if (cg::launch_code_slices(w.sym, nullptr, cdf, w.stage, len, d, 2, status, stream) != cudaSuccess)
         return CG_ERR_CUDA;

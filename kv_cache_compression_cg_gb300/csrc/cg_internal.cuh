@@ -56,6 +56,15 @@ __host__ __device__ inline void slice_coords(const Dims &d, long long b, int &k,
     k = (int)(r / 2);
 }
 
+// Per-stream staging area: kStagePrefix bytes of slack, then the stream's
+// words (the encoder parks a placeholder word in the slack before the first
+// real one, which keeps its store path free of a branch).
+constexpr int kStagePrefix = 16;
+
+__host__ __device__ inline uint8_t *stage_stream(uint8_t *stage, long long sid, const Dims &d) {
+    return stage + sid * d.stage_bytes + kStagePrefix;
+}
+
 // Scan helper sizes.
 constexpr int kScanBlock = 1024;      // threads per scan block
 constexpr int kScanItems = 2;         // items per thread
@@ -82,6 +91,18 @@ cudaError_t launch_scan_and_pack(const uint32_t *len, uint64_t *off,
                                  uint64_t capacity, unsigned long long *partials,
                                  const Dims &d, int32_t *status, cudaStream_t s);
 
+// Fused quantise + CDF + encode straight from fp16 (chunks <= 256 tokens,
+// A <= 64, C % 8 == 0, 16-byte aligned rows); compress_fused_applies says when.
+bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v);
+// Writes max1, cdf, len, off (incl. off[nstreams]) and packed; `state` holds
+// 1 + nslices zeroed-per-call uint64 words (ticket counter, look-back slots).
+cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d,
+                                  const MaxTab &mt, uint16_t *max1, uint16_t *cdf,
+                                  uint8_t *stage, uint32_t *len, uint64_t *off,
+                                  uint8_t *packed, uint64_t capacity,
+                                  unsigned long long *state, int32_t *status,
+                                  cudaStream_t s);
+
 // mode: 0 = symbols out (sym), 1 = dequantised binary32 out (out_k, out_v).
 cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes,
                           const uint64_t *off, const uint32_t *len,
@@ -89,6 +110,14 @@ cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes,
                           const Dims &d, const MaxTab &mt, int mode, uint8_t *sym,
                           float *out_k, float *out_v, int32_t *status,
                           cudaStream_t s);
+
+// Any chunk size up to CG_MAX_CHUNK_TOKENS (used by launch_decode beyond 256).
+cudaError_t launch_decode_generic(const uint8_t *packed, uint64_t packed_bytes,
+                                  const uint64_t *off, const uint32_t *len,
+                                  const uint16_t *cdf, const uint16_t *max1,
+                                  const Dims &d, const MaxTab &mt, int mode,
+                                  uint8_t *sym, float *out_k, float *out_v,
+                                  int32_t *status, cudaStream_t s);
 
 cudaError_t launch_dequantize(const uint8_t *sym, const uint16_t *max1,
                               const Dims &d, const MaxTab &mt, float *out_k,

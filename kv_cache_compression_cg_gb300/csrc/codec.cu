@@ -17,6 +17,7 @@
 #include <cuda_fp16.h>
 
 #include "cg_internal.cuh"
+#include "coder.cuh"
 
 namespace cg {
 namespace {
@@ -58,96 +59,6 @@ __host__ __device__ inline EncSmem enc_smem_layout(int NT, int A) {
     o += (size_t)(NT + 1) * 2;
     s.bytes = (o + 15) & ~(size_t)15;
     return s;
-}
-
-// ---- encoder state ------------------------------------------------------
-struct Enc {
-    uint32_t low, range;
-    uint64_t acc;   // pending output bits [0, nbits), plus a carry at bit nbits
-    int nbits;      // multiple of 8
-    uint32_t prev;  // last full word, not yet stored (absorbs carries)
-    int have_prev;
-    int nwords;     // words stored so far
-};
-
-__device__ __forceinline__ void enc_init(Enc &e) {
-    e.low = 0;
-    e.range = 0xFFFFFFFFu;
-    e.acc = 0;
-    e.nbits = 0;
-    e.prev = 0;
-    e.have_prev = 0;
-    e.nwords = 0;
-}
-
-// Add one to the bytes [0, nbytes) already stored (the carry rule).
-__device__ __noinline__ void carry_into_stored(uint8_t *stream, int nbytes) {
-    int i = nbytes - 1;
-    while (i >= 0 && stream[i] == 0xFF) {
-        stream[i] = 0;
-        i--;
-    }
-    if (i >= 0) stream[i] = (uint8_t)(stream[i] + 1);
-}
-
-__device__ __forceinline__ void store_be(uint8_t *stream, int nwords, uint32_t w) {
-    reinterpret_cast<uint32_t *>(stream)[nwords] = __byte_perm(w, 0, 0x0123);
-}
-
-// Move the oldest 32 pending bits out of the accumulator (needs nbits >= 32).
-__device__ __forceinline__ void enc_flush_word(Enc &e, uint8_t *stream) {
-    const uint32_t ovf = (uint32_t)(e.acc >> e.nbits) & 1u;
-    const uint32_t word = (uint32_t)(e.acc >> (e.nbits - 32));
-    e.nbits -= 32;
-    e.acc &= (1ull << e.nbits) - 1ull;
-    if (ovf) {
-        e.prev += 1u;
-        if (e.prev == 0u) carry_into_stored(stream, 4 * e.nwords);
-    }
-    if (e.have_prev) {
-        store_be(stream, e.nwords, e.prev);
-        e.nwords++;
-    }
-    e.prev = word;
-    e.have_prev = 1;
-}
-
-// Code one symbol given its packed CDF entry (lo | f << 16).
-__device__ __forceinline__ void enc_symbol(Enc &e, uint32_t entry) {
-    const uint32_t r = e.range >> 16;
-    const uint64_t t = (uint64_t)e.low + (uint64_t)(r * (entry & 0xFFFFu));
-    e.low = (uint32_t)t;
-    e.acc += t >> 32;
-    e.range = r * (entry >> 16);
-    const int sh = __clz(e.range) & 24;  // bytes to shift out: 0, 1 or 2
-    e.acc = (e.acc << sh) | ((uint64_t)e.low >> (32 - sh));
-    e.low <<= sh;
-    e.range <<= sh;
-    e.nbits += sh;
-}
-
-// Flush byte and final words; returns the stream length in bytes.
-__device__ __forceinline__ uint32_t enc_finish(Enc &e, uint8_t *stream) {
-    if (e.nbits >= 32) enc_flush_word(e, stream);
-    const uint32_t v = e.low + 0x00FFFFFFu;
-    e.acc += (v < e.low) ? 1u : 0u;
-    e.acc = (e.acc << 8) | (v >> 24);
-    e.nbits += 8;
-    if (e.nbits >= 32) enc_flush_word(e, stream);
-    const uint32_t ovf = (uint32_t)(e.acc >> e.nbits) & 1u;
-    if (ovf) {
-        e.prev += 1u;
-        if (e.prev == 0u) carry_into_stored(stream, 4 * e.nwords);
-    }
-    if (e.have_prev) {
-        store_be(stream, e.nwords, e.prev);
-        e.nwords++;
-    }
-    if (e.nbits > 0) {
-        const uint64_t bits = e.acc & ((1ull << e.nbits) - 1ull);
-        store_be(stream, e.nwords, (uint32_t)(bits << (32 - e.nbits)));
-    }
-    return (uint32_t)(4 * e.nwords + e.nbits / 8);
 }
 
 // ---- CDF normalisation of one channel (specification F), one warp -------
@@ -217,7 +128,7 @@ __global__ void __launch_bounds__(1024, 1) k_code_slices(const uint8_t *__restri
     const uint8_t *rows = sym + group_index(d, kv, l, t0) * d.C;
     const long long cdf_base = cdf_slice_offset(d, k, kv, l);
     const long long sid = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk + tid;
-    uint8_t *stream = stage + (tid < Tk ? sid : 0) * d.stage_bytes;
+    uint8_t *stream = stage_stream(stage, tid < Tk ? sid : 0, d);
     // vec_rows: C % 16 == 0 and sym 16-byte aligned, so with W % 16 == 0 a
     // 16-byte vector never straddles a window
     const int vshift = (W == 64) ? 2 : (W == 32) ? 1 : 0;  // log2(W / 16)
@@ -554,10 +465,10 @@ cudaError_t launch_code_slices(const uint8_t *sym, const uint16_t *cdf_in, uint1
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
-                          const uint32_t *len, const uint16_t *cdf, const uint16_t *max1,
-                          const Dims &d, const MaxTab &mt, int mode, uint8_t *sym, float *out_k,
-                          float *out_v, int32_t *status, cudaStream_t s) {
+cudaError_t launch_decode_generic(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
+                                  const uint32_t *len, const uint16_t *cdf, const uint16_t *max1,
+                                  const Dims &d, const MaxTab &mt, int mode, uint8_t *sym,
+                                  float *out_k, float *out_v, int32_t *status, cudaStream_t s) {
     const long long nslices = 2LL * d.L * d.nch;
     const int NT = block_threads(d);
     const size_t s0 = dec_smem_layout(NT, d.A[0]).bytes, s1 = dec_smem_layout(NT, d.A[1]).bytes;

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kScanBlock) k_offsets_and_pack(
     for (long long li = warp; li < nt; li += blockDim.x >> 5) {
         const unsigned long long dst = offs[li];
         const uint32_t L = lens[li];
-        const uint8_t *src = stage + (tile0 + li) * stage_bytes;
+        const uint8_t *src = stage + (tile0 + li) * stage_bytes + kStagePrefix;
         for (uint32_t b = 4u * lane; b < L; b += 128u) {
             const uint32_t w = *reinterpret_cast<const uint32_t *>(src + b);
             const uint32_t nb = min(4u, L - b);
