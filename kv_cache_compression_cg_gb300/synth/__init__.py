@@ -107,8 +107,15 @@ WORKLOADS = {
 }
 
 
+_CORE = os.path.join(_HERE, "synth_core.h")
+_GPU_SRC = os.path.join(_HERE, "synth_gpu.cu")
+_GPU_SO = os.path.join(_HERE, "libcg_synth_gpu.so")
+_GPU_LIB = None
+
+
 def build(force: bool = False) -> str:
-    stale = (not os.path.exists(_SO)) or os.path.getmtime(_SO) < os.path.getmtime(_SRC)
+    stale = (not os.path.exists(_SO)) or os.path.getmtime(_SO) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(_CORE))
     if force or stale:
         tmp = _SO + f".{os.getpid()}.tmp"
         subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
@@ -127,6 +134,11 @@ def lib() -> C.CDLL:
             L.syn_generate.restype = C.c_int
             L.syn_generate.argtypes = [C.POINTER(_Params), C.c_void_p, C.c_void_p,
                                        C.c_int64, C.c_int]
+            L.syn_generate_slice_range.restype = C.c_int
+            L.syn_generate_slice_range.argtypes = [C.POINTER(_Params), C.c_int, C.c_int, C.c_int,
+                                                   C.c_int, C.c_void_p]
+            L.syn_slice_sigma.restype = C.c_int
+            L.syn_slice_sigma.argtypes = [C.POINTER(_Params), C.c_int, C.c_int, C.c_void_p]
             L.syn_generate_slice.restype = C.c_int
             L.syn_generate_slice.argtypes = [C.POINTER(_Params), C.c_int, C.c_int,
                                              C.c_void_p]
@@ -184,3 +196,78 @@ def generate_slice(w: Workload | str, kv: int, layer: int, T: int | None = None)
     if lib().syn_generate_slice(C.byref(p), kv, layer, C.c_void_p(out.ctypes.data)) != 0:
         raise RuntimeError("synthetic generator failed")
     return out
+
+
+def generate_slice_range(w: Workload | str, kv: int, layer: int, t0: int, t1: int) -> np.ndarray:
+    """Tokens [t0, t1) of one (kv, layer) slice, [t1 - t0][C] float16."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    out = np.empty((t1 - t0, w.C), np.float16)
+    p = w.params(T=max(t1, 1))
+    if lib().syn_generate_slice_range(C.byref(p), kv, layer, t0, t1, C.c_void_p(out.ctypes.data)) != 0:
+        raise RuntimeError("synthetic generator failed")
+    return out
+
+
+def sigmas(w: Workload) -> np.ndarray:
+    """Per-channel sigma_c of every slice, float64 [2][L][C]."""
+    out = np.zeros((2, w.L, w.C), np.float64)
+    if w.kind == UNIFORM:
+        return out
+    p = w.params()
+    for kv in range(2):
+        for layer in range(w.L):
+            if lib().syn_slice_sigma(C.byref(p), kv, layer, C.c_void_p(out[kv, layer].ctypes.data)) != 0:
+                raise RuntimeError("synthetic generator failed")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# device generator (same bytes as the host one, for the full-size workloads)
+# ---------------------------------------------------------------------------
+def build_device(force: bool = False) -> str:
+    stale = (not os.path.exists(_GPU_SO)) or os.path.getmtime(_GPU_SO) < max(
+        os.path.getmtime(_GPU_SRC), os.path.getmtime(_CORE))
+    if force or stale:
+        import shutil
+        nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+        tmp = _GPU_SO + f".{os.getpid()}.tmp"
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false",
+                        "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared", _GPU_SRC, "-o", tmp],
+                       check=True)
+        os.replace(tmp, _GPU_SO)
+    return _GPU_SO
+
+
+def _gpu_lib() -> C.CDLL:
+    global _GPU_LIB
+    with _LOCK:
+        if _GPU_LIB is None:
+            build_device()
+            L = C.CDLL(_GPU_SO)
+            L.syn_generate_device.restype = C.c_int
+            L.syn_generate_device.argtypes = [C.POINTER(_Params), C.c_void_p, C.c_void_p, C.c_void_p,
+                                              C.c_int64, C.c_void_p]
+            _GPU_LIB = L
+    return _GPU_LIB
+
+
+def generate_device(w: Workload | str, T: int | None = None, device="cuda"):
+    """K and V as torch float16 CUDA tensors [L][T][C], generated on the
+    device with the host generator's arithmetic (identical bytes)."""
+    import torch
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    Tn = T or w.T
+    lib()  # host library (sigmas)
+    k = torch.empty((w.L, Tn, w.C), dtype=torch.float16, device=device)
+    v = torch.empty((w.L, Tn, w.C), dtype=torch.float16, device=device)
+    sig = torch.from_numpy(sigmas(w).reshape(-1)).to(device)
+    p = w.params(T=Tn)
+    stream = torch.cuda.current_stream(k.device).cuda_stream
+    rc = _gpu_lib().syn_generate_device(C.byref(p), C.c_void_p(sig.data_ptr()), C.c_void_p(k.data_ptr()),
+                                        C.c_void_p(v.data_ptr()), Tn * w.C, C.c_void_p(stream))
+    if rc != 0:
+        raise RuntimeError("device generator launch failed")
+    torch.cuda.current_stream(k.device).synchronize()
+    return k, v

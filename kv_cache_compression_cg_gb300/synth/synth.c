@@ -27,159 +27,38 @@
  *   STUDENT_T: x_t = sigma_c * Z / sqrt((Z1^2 + Z2^2 + Z3^2) / 3) (nu = 3)
  *   UNIFORM:   x_t ~ U[0, 1) (no sigma)
  */
-#include <math.h>
 #include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
-enum { SYN_AR1 = 0, SYN_STUDENT_T = 1, SYN_UNIFORM = 2 };
+#include "synth_core.h"
 
-typedef struct syn_params {
-    int32_t kind;
-    int32_t L, T, C;
-    uint64_t seed;
-    double rho;
-    double sigma_log;
-    double outlier_frac;
-    double outlier_scale;
-} syn_params;
-
-/* ---------------------------------------------------------------- RNG */
-static uint64_t sm64(uint64_t key, uint64_t i)
+/* sigma_c of one (kv, layer) slice: LogNormal(0, sigma_log) per channel, and
+ * round(outlier_frac * C) channels drawn without replacement (partial
+ * Fisher-Yates) scaled by outlier_scale. */
+int syn_slice_sigma(const syn_params *p, int kv, int layer, double *sigma)
 {
-    uint64_t z = key + (i + 1) * 0x9E3779B97F4A7C15ULL;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
-    return z ^ (z >> 31);
-}
-
-/* uniform in (0, 1]: 53 random bits */
-static double u01_open0(uint64_t x) { return ((double)(x >> 11) + 1.0) * 0x1p-53; }
-/* uniform in [0, 1) */
-static double u01(uint64_t x) { return (double)(x >> 11) * 0x1p-53; }
-
-/* ------------------------------------------------- elementary functions */
-static const double LN2_HI = 6.93147180369123816490e-01; /* 0x3FE62E42FEE00000 */
-static const double LN2_LO = 1.90821492927058770002e-10;
-
-/* ln(x), x > 0: x = m 2^e with m in [sqrt(1/2), sqrt(2)); with
- * s = (m-1)/(m+1), ln m = 2 (s + s^3/3 + s^5/5 + ...). */
-static double syn_log(double x)
-{
-    int e;
-    double m = frexp(x, &e); /* m in [0.5, 1) */
-    if (m < 0.70710678118654752440) {
-        m *= 2.0;
-        e -= 1;
+    const int C = p->C;
+    uint64_t key = slice_key(p, kv, layer);
+    uint64_t key_sigma = sm64(key, 1), key_out = sm64(key, 2);
+    int *perm = (int *)malloc(sizeof(int) * C);
+    if (!perm)
+        return -1;
+    for (int c = 0; c < C; c++) {
+        sigma[c] = syn_exp(p->sigma_log * syn_normal(key_sigma, (uint64_t)c));
+        perm[c] = c;
     }
-    double s = (m - 1.0) / (m + 1.0);
-    double s2 = s * s;
-    double term = s, sum = 0.0;
-    for (int k = 0; k < 14; k++) {
-        sum = sum + term / (double)(2 * k + 1);
-        term = term * s2;
+    int n_out = (int)nearbyint(p->outlier_frac * (double)C);
+    for (int i = 0; i < n_out; i++) {
+        uint64_t j = (uint64_t)i + sm64(key_out, (uint64_t)i) % (uint64_t)(C - i);
+        int tmp = perm[i];
+        perm[i] = perm[j];
+        perm[j] = tmp;
+        sigma[perm[i]] *= p->outlier_scale;
     }
-    return ((double)e * LN2_LO + 2.0 * sum) + (double)e * LN2_HI;
-}
-
-/* exp(x): x = n ln2 + r, |r| <= ln2/2, Taylor series of exp(r). */
-static double syn_exp(double x)
-{
-    double n = nearbyint(x / 0.69314718055994530942);
-    double r = (x - n * LN2_HI) - n * LN2_LO;
-    double term = 1.0, sum = 1.0;
-    for (int k = 1; k < 22; k++) {
-        term = term * r / (double)k;
-        sum = sum + term;
-    }
-    return ldexp(sum, (int)n);
-}
-
-/* sin and cos of pi/2 * f for f in [0, 1], Taylor series. */
-static void syn_sincos_quarter(double f, double *s, double *c)
-{
-    double x = f * 1.57079632679489661923;
-    double x2 = x * x;
-    double ts = x, tc = 1.0, ss = 0.0, cc = 0.0;
-    for (int k = 0; k < 14; k++) {
-        ss = ss + ts;
-        cc = cc + tc;
-        ts = -ts * x2 / (double)((2 * k + 2) * (2 * k + 3));
-        tc = -tc * x2 / (double)((2 * k + 1) * (2 * k + 2));
-    }
-    *s = ss;
-    *c = cc;
-}
-
-/* (cos 2 pi u, sin 2 pi u) for u in [0, 1), by quadrant. */
-static void syn_cis(double u, double *c, double *s)
-{
-    double v = u * 4.0; /* exact */
-    int q = (int)v;
-    double f = v - (double)q; /* exact */
-    double sq, cq;
-    syn_sincos_quarter(f, &sq, &cq);
-    switch (q & 3) {
-    case 0: *c = cq; *s = sq; break;
-    case 1: *c = -sq; *s = cq; break;
-    case 2: *c = -cq; *s = -sq; break;
-    default: *c = sq; *s = -cq; break;
-    }
-}
-
-/* Two independent N(0,1) from two uniforms (Box-Muller). */
-static void syn_normal2(uint64_t key, uint64_t i, double *z0, double *z1)
-{
-    double u1 = u01_open0(sm64(key, 2 * i));
-    double u2 = u01(sm64(key, 2 * i + 1));
-    double rad = sqrt(-2.0 * syn_log(u1));
-    double c, s;
-    syn_cis(u2, &c, &s);
-    *z0 = rad * c;
-    *z1 = rad * s;
-}
-
-static double syn_normal(uint64_t key, uint64_t i)
-{
-    double a, b;
-    syn_normal2(key, i, &a, &b);
-    return a;
-}
-
-/* ------------------------------------------------- double -> fp16 bits */
-static uint16_t syn_to_half(double x)
-{
-    uint16_t sign = signbit(x) ? 0x8000 : 0;
-    double a = fabs(x);
-    if (!(a < 65504.0))
-        return sign | 0x7BFF; /* saturate (also catches NaN, none produced) */
-    if (a < 0x1p-14) {
-        double r = nearbyint(ldexp(a, 24)); /* subnormal units of 2^-24 */
-        return sign | (uint16_t)r;          /* r == 1024 -> smallest normal */
-    }
-    int e;
-    double m = frexp(a, &e); /* a = m 2^e, m in [0.5, 1) */
-    int E = e - 1;           /* a = 1.f 2^E, E in [-14, 15] */
-    double r = nearbyint(ldexp(m, 11)); /* in [1024, 2048] */
-    if (r == 2048.0) {
-        r = 1024.0;
-        E += 1;
-    }
-    if (E > 15)
-        return sign | 0x7BFF;
-    return sign | (uint16_t)(((E + 15) << 10) | ((int)r - 1024));
-}
-
-/* ------------------------------------------------------------ slices */
-/* Per-element counter, independent of T so a token prefix of a tensor is the
- * prefix of the longer tensor. */
-static uint64_t elem_ctr(int c, int t) { return ((uint64_t)c << 32) | (uint64_t)t; }
-
-static uint64_t slice_key(const syn_params *p, int kv, int layer)
-{
-    uint64_t k0 = sm64(p->seed, 0);
-    return sm64(k0, ((uint64_t)kv << 32) | (uint64_t)layer);
+    free(perm);
+    return 0;
 }
 
 /* One (kv, layer) slice into out[t * C + c]. */
@@ -187,7 +66,6 @@ static int syn_fill_slice(const syn_params *p, int kv, int layer, uint16_t *out)
 {
     const int T = p->T, C = p->C;
     uint64_t key = slice_key(p, kv, layer);
-    uint64_t key_sigma = sm64(key, 1), key_out = sm64(key, 2);
     uint64_t key_val = sm64(key, 3);
 
     if (p->kind == SYN_UNIFORM) {
@@ -199,52 +77,25 @@ static int syn_fill_slice(const syn_params *p, int kv, int layer, uint16_t *out)
     }
 
     double *sigma = (double *)malloc(sizeof(double) * C);
-    int *perm = (int *)malloc(sizeof(int) * C);
     double *state = (double *)malloc(sizeof(double) * C);
-    if (!sigma || !perm || !state) {
-        free(sigma); free(perm); free(state);
+    if (!sigma || !state || syn_slice_sigma(p, kv, layer, sigma) != 0) {
+        free(sigma); free(state);
         return -1;
     }
-    for (int c = 0; c < C; c++) {
-        sigma[c] = syn_exp(p->sigma_log * syn_normal(key_sigma, (uint64_t)c));
-        perm[c] = c;
-    }
-    int n_out = (int)nearbyint(p->outlier_frac * (double)C);
-    for (int i = 0; i < n_out; i++) { /* partial Fisher-Yates */
-        uint64_t j = (uint64_t)i + sm64(key_out, (uint64_t)i) % (uint64_t)(C - i);
-        int tmp = perm[i];
-        perm[i] = perm[j];
-        perm[j] = tmp;
-        sigma[perm[i]] *= p->outlier_scale;
-    }
-
     if (p->kind == SYN_AR1) {
         double stat = sqrt(1.0 - p->rho * p->rho);
         for (int t = 0; t < T; t++)
             for (int c = 0; c < C; c++) {
-                double z = syn_normal(key_val, elem_ctr(c, t));
-                double x;
-                if (t == 0)
-                    x = sigma[c] * z / stat;
-                else
-                    x = p->rho * state[c] + sigma[c] * z;
+                double x = syn_ar1_next(p, key_val, c, t, sigma[c], stat, state[c]);
                 state[c] = x;
                 out[(int64_t)t * C + c] = syn_to_half(x);
             }
     } else { /* SYN_STUDENT_T, nu = 3 */
         for (int t = 0; t < T; t++)
-            for (int c = 0; c < C; c++) {
-                uint64_t i = elem_ctr(c, t) * 2;
-                double z0, z1, z2, z3;
-                syn_normal2(key_val, i, &z0, &z1);
-                syn_normal2(key_val, i + 1, &z2, &z3);
-                double chi = (z1 * z1 + z2 * z2) + z3 * z3;
-                double x = sigma[c] * z0 / sqrt(chi / 3.0);
-                out[(int64_t)t * C + c] = syn_to_half(x);
-            }
+            for (int c = 0; c < C; c++)
+                out[(int64_t)t * C + c] = syn_to_half(syn_student_value(key_val, c, t, sigma[c]));
     }
     free(sigma);
-    free(perm);
     free(state);
     return 0;
 }
@@ -307,6 +158,46 @@ int syn_generate(const syn_params *p, uint16_t *k, uint16_t *v,
     free(jobs);
     free(th);
     return err;
+}
+
+/* Tokens [t0, t1) of one (kv, layer) slice into out[(t - t0) * C + c]; the
+ * AR(1) recurrence still runs from token 0. */
+int syn_generate_slice_range(const syn_params *p, int kv, int layer, int t0, int t1,
+                             uint16_t *out)
+{
+    if (!p || kv < 0 || kv > 1 || layer < 0 || layer >= p->L || t0 < 0 || t1 < t0 || t1 > p->T || !out)
+        return -1;
+    const int C = p->C;
+    uint64_t key_val = sm64(slice_key(p, kv, layer), 3);
+    if (p->kind == SYN_UNIFORM) {
+        for (int t = t0; t < t1; t++)
+            for (int c = 0; c < C; c++)
+                out[(int64_t)(t - t0) * C + c] = syn_to_half(u01(sm64(key_val, elem_ctr(c, t))));
+        return 0;
+    }
+    double *sigma = (double *)malloc(sizeof(double) * C);
+    double *state = (double *)calloc((size_t)C, sizeof(double));
+    if (!sigma || !state || syn_slice_sigma(p, kv, layer, sigma) != 0) {
+        free(sigma); free(state);
+        return -1;
+    }
+    if (p->kind == SYN_AR1) {
+        double stat = sqrt(1.0 - p->rho * p->rho);
+        for (int t = 0; t < t1; t++)
+            for (int c = 0; c < C; c++) {
+                double x = syn_ar1_next(p, key_val, c, t, sigma[c], stat, state[c]);
+                state[c] = x;
+                if (t >= t0)
+                    out[(int64_t)(t - t0) * C + c] = syn_to_half(x);
+            }
+    } else {
+        for (int t = t0; t < t1; t++)
+            for (int c = 0; c < C; c++)
+                out[(int64_t)(t - t0) * C + c] = syn_to_half(syn_student_value(key_val, c, t, sigma[c]));
+    }
+    free(sigma);
+    free(state);
+    return 0;
 }
 
 /* One slice alone (for regenerating a sample on the host). */

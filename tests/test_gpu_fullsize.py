@@ -1,0 +1,109 @@
+"""Full-size workloads (the 34B-shaped 32K-token context and the 80K-token
+low-locality stress case) on the GPU, in the launch configuration the
+benchmark times (one cg_compress_chunk and one cg_decompress_chunk over the
+whole tensor).
+
+The oracle cannot code 6-10 GB in a test, so:
+- sampled (chunk, kv, layer) slices are coded by the oracle from inputs the
+  host generator regenerates on its own, and every output of those slices
+  (max1, CDF rows, stream lengths, packed bytes, dequantised values) must match
+  the GPU's bit for bit;
+- properties that hold at any size are checked over every element on the GPU:
+  status words clear, offsets the exclusive scan of the lengths, lengths within
+  2C + 8, and the quantisation error bound |x - x^| <= max1/(2 MAX) + ulp(max1).
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cg():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from kv_cache_compression_cg_gb300 import build, codec
+    build.build()
+    return codec
+
+
+def _samples(w, seed):
+    nch = w.n_chunks
+    rng = np.random.default_rng(seed)
+    picks = [(0, 0, 0), (nch - 1, 1, w.L - 1), (nch // 2, 0, w.L // 2), (nch // 3, 1, 1)]
+    for _ in range(2):
+        picks.append((int(rng.integers(nch)), int(rng.integers(2)), int(rng.integers(w.L))))
+    return picks
+
+
+def _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l):
+    L, T, C_, Tc = w.L, w.T, w.C, w.chunk_tokens
+    bins = (w.bins_k, w.bins_v)[kv]
+    A_k, A_v = max(w.bins_k), max(w.bins_v)
+    A = (A_k, A_v)[kv]
+    t0, t1 = kc * Tc, min(T, (kc + 1) * Tc)
+    Tk = t1 - t0
+    x = synth_mod.generate_slice_range(w, kv, l, t0, t1)
+    dev_x = (k, v)[kv][l, t0:t1].cpu().numpy()
+    assert np.array_equal(dev_x.view(np.uint16), x.view(np.uint16)), "device generator differs from host"
+    # the oracle on [2 layers][Tk][C]: layer 0 is the slice, layer 1 a zero
+    # layer with bins A, so that the oracle's alphabet is the tensor's A
+    K = np.zeros((2, Tk, C_), np.float16)
+    K[0] = x
+    V = np.zeros((2, Tk, C_), np.float16)
+    ref = oracle_mod.compress(K, V, Tc, [bins[l], A], [A, A])
+    assert ref["A_k"] == A
+    # max1
+    got_m1 = out.max1[kv, l, t0:t1].cpu().numpy().view(np.uint16)
+    assert np.array_equal(got_m1, ref["max1"][0, 0])
+    # CDF rows of the slice
+    g0 = oracle_mod.cdf_offset(L, C_, A_k, A_v, kc, kv, l, 0)
+    got_cdf = out.cdf[g0:g0 + C_ * A].cpu().numpy().view(np.uint16)
+    assert np.array_equal(got_cdf, ref["cdf"][:C_ * A])
+    # stream lengths and bytes
+    s0 = oracle_mod.stream_id(L, T, Tc, kc, kv, l, 0)
+    got_len = out.len[s0:s0 + Tk].cpu().numpy().view(np.uint32)
+    assert np.array_equal(got_len, ref["len"][:Tk])
+    b0, b1 = int(out.off[s0].item()), int(out.off[s0 + Tk].item())
+    assert b1 - b0 == int(ref["off"][Tk])
+    assert np.array_equal(out.packed[b0:b1].cpu().numpy(), ref["packed"][:b1 - b0])
+    # dequantised output of the slice
+    rk, _ = oracle_mod.decompress(ref["packed"], ref["off"], ref["len"], ref["cdf"], ref["max1"],
+                                  2, Tk, C_, Tc, [bins[l], A], [A, A])
+    got = (ok, ov)[kv][l, t0:t1].cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), rk[0].view(np.uint32))
+
+
+def _check_properties(w, k, v, codec, out, ok, ov):
+    ns = 2 * w.L * w.T
+    ln = out.len[:ns].to(torch.int64) & 0xFFFFFFFF
+    off = out.off
+    assert int(off[0].item()) == 0
+    assert torch.equal(off[1:] - off[:-1], ln)
+    assert int(ln.max().item()) <= 2 * w.C + 8
+    assert int(off[-1].item()) <= codec.capacity
+    for kv, (x, xh, bins) in enumerate(((k, ok, w.bins_k), (v, ov, w.bins_v))):
+        for l in range(w.L):
+            m1 = out.max1[kv, l].view(torch.float16)
+            ulp = (out.max1[kv, l] + 1).view(torch.float16).float() - m1.float()
+            MAX = bins[l] // 2 - 1
+            bound = m1.float() / (2 * MAX) + ulp
+            err = (xh[l] - x[l].float()).abs().amax(dim=1)
+            assert bool((err <= bound).all()), f"error bound broken at kv={kv} layer={l}"
+
+
+@pytest.mark.parametrize("name", ["ctx32k", "stress80k"])
+def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name):
+    w = synth_mod.WORKLOADS[name]
+    k, v = synth_mod.generate_device(w)
+    codec = cg.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens,
+                     capacity=w.elements // 2)
+    out = codec.compress(k, v)
+    ok, ov = codec.decompress()
+    torch.cuda.synchronize()
+    assert int(out.status.item()) == 0
+    assert int(codec.dstatus.item()) == 0
+    _check_properties(w, k, v, codec, out, ok, ov)
+    for kc, kv, l in _samples(w, seed=len(name)):
+        _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l)
