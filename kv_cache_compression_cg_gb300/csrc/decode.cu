@@ -90,27 +90,49 @@ __device__ __forceinline__ void stream_init(Stream &s, const uint8_t *packed, lo
     refill(s, packed);
 }
 
-// One symbol with the row (cum, frq) of its channel; needs nb >= 16. Entries
-// at or past A hold cum = 65535: a valid stream's code never reaches them (its
-// symbol's upper bound is at most 65535), and the clamp to A - 1 gives a
-// corrupt stream the decoder rule's answer (largest s < A with r*cum[s] <= code).
+// One binary-search step over a uint16 CDF row at shared address `addr`:
+// move addr forward by STEP entries when r * row[STEP] <= code.
+template <int STEP>
+__device__ __forceinline__ void search_step(uint32_t &addr, uint32_t r, uint32_t code) {
+    asm("{\n\t.reg .pred p;\n\t.reg .u32 v;\n\t"
+        "ld.shared.u16 v, [%0 + %3];\n\t"
+        "mul.lo.u32 v, %1, v;\n\t"
+        "setp.le.u32 p, v, %2;\n\t"
+        "@p add.u32 %0, %0, %3;\n\t}"
+        : "+r"(addr)
+        : "r"(r), "r"(code), "n"(2 * STEP));
+}
+
+template <int STEP>
+__device__ __forceinline__ void search_from(uint32_t &addr, uint32_t r, uint32_t code) {
+    search_step<STEP>(addr, r, code);
+    if constexpr (STEP > 1) search_from<STEP / 2>(addr, r, code);
+}
+
+// One symbol from the row of its channel: `cum` is the shared address of the
+// uint16 cumulative row, its frequencies sit frq_off bytes further; needs
+// nb >= 16. Entries at or past A hold cum = 65535: a valid stream's code never
+// reaches them (its symbol's upper bound is at most 65535), and the clamp to
+// A - 1 gives a corrupt stream the decoder rule's answer (largest s < A with
+// r*cum[s] <= code).
 template <int P>
-__device__ __forceinline__ uint32_t decode_symbol(Stream &s, const uint16_t *cum, const uint16_t *frq,
+__device__ __forceinline__ uint32_t decode_symbol(Stream &s, uint32_t cum, uint32_t frq_off,
                                                   uint32_t amax) {
     const uint32_t r = s.range >> 16;
-    uint32_t q = 0;
-#pragma unroll
-    for (int step = P / 2; step >= 1; step >>= 1)
-        q = (r * (uint32_t)cum[q + step] <= s.code) ? q + step : q;
-    q = min(q, amax);
-    s.code -= r * (uint32_t)cum[q];
-    s.range = r * (uint32_t)frq[q];
+    uint32_t addr = cum;
+    search_from<P / 2>(addr, r, s.code);
+    addr = min(addr, cum + 2 * amax);
+    uint32_t lo, f;
+    asm("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(addr));
+    asm("ld.shared.u16 %0, [%1];" : "=r"(f) : "r"(addr + frq_off));
+    s.code -= r * lo;
+    s.range = r * f;
     const uint32_t sh = __clz(s.range) & 24;
     s.code = __funnelshift_l((uint32_t)(s.bb >> 32), s.code, sh);
     s.bb <<= sh;
     s.nb -= (int)sh;
     s.range <<= sh;
-    return q;
+    return (addr - cum) >> 1;
 }
 
 constexpr int kHelpers = 32;  // one helper warp per CTA
@@ -272,24 +294,26 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
         const int Wc = min(W, d.C - c0);
         if (!helper) {
             if (tid < Tk) {
-                const uint16_t *cb = cum + b * W * P;
-                const uint16_t *fb = frq + b * W * P;
+                // shared addresses of this buffer's rows; frequencies follow at a fixed offset
+                const uint32_t cb = (uint32_t)__cvta_generic_to_shared(cum + b * W * P);
+                const uint32_t fo = (uint32_t)(L::frq - L::cum);
                 uint8_t *my = tile + b * kThreads * TS + tid * TS;
                 if (Wc == W) {
 #pragma unroll 4
                     for (int c = 0; c < W; c += 4) {
+                        const uint32_t rc = cb + 2 * P * c;
                         if (s.nb < 32) refill(s, packed);
-                        const uint32_t q0 = decode_symbol<P>(s, cb + c * P, fb + c * P, amax);
-                        const uint32_t q1 = decode_symbol<P>(s, cb + (c + 1) * P, fb + (c + 1) * P, amax);
+                        const uint32_t q0 = decode_symbol<P>(s, rc, fo, amax);
+                        const uint32_t q1 = decode_symbol<P>(s, rc + 2 * P, fo, amax);
                         if (s.nb < 32) refill(s, packed);
-                        const uint32_t q2 = decode_symbol<P>(s, cb + (c + 2) * P, fb + (c + 2) * P, amax);
-                        const uint32_t q3 = decode_symbol<P>(s, cb + (c + 3) * P, fb + (c + 3) * P, amax);
+                        const uint32_t q2 = decode_symbol<P>(s, rc + 4 * P, fo, amax);
+                        const uint32_t q3 = decode_symbol<P>(s, rc + 6 * P, fo, amax);
                         *reinterpret_cast<uint32_t *>(my + c) = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
                     }
                 } else {
                     for (int c = 0; c < Wc; c++) {
                         if (s.nb < 32) refill(s, packed);
-                        my[c] = (uint8_t)decode_symbol<P>(s, cb + c * P, fb + c * P, amax);
+                        my[c] = (uint8_t)decode_symbol<P>(s, cb + 2 * P * c, fo, amax);
                     }
                 }
             }
