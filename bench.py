@@ -107,6 +107,47 @@ def dist_env():
     return world, rank, local
 
 
+def alg_ops_encode() -> int:
+    """Integer/fp32 operations the specification needs per symbol to compress:
+    quantise (convert, multiply, add, round, clamp: 5), count (1), coder step
+    (r = range >> 16, split the CDF entry into lo and f, low += r*lo with the
+    carry into the pending bits, range = r*f: 6), renormalise (shift count from
+    clz: 2, shift low into the pending bits, low, range, bit count: 4), group
+    max (1) -> 19."""
+    return 19
+
+
+def alg_ops_decode(P: int) -> int:
+    """Per symbol to decompress: r (1), binary search over the P-entry row
+    (multiply, compare, select per step: 3 log2 P), clamp (1), code -= r*lo (1),
+    range = r*f (1), shift count (2), shift code, bit buffer, range, bit count
+    (4), dequantise (lookup, multiply: 2) -> 12 + 3 log2 P."""
+    return 12 + 3 * (P.bit_length() - 1)
+
+
+def kernel_traffic(kernel: str, sources):
+    """DRAM bytes per launch from the committed ncu table, only while the
+    kernel's sources still hash to the values recorded with the counters."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    csrc = os.path.join(ROOT, "kv_cache_compression_cg_gb300", "csrc")
+    try:
+        with open(path) as fh:
+            text = fh.read()
+        h = hashlib.sha256()
+        for name in sources:
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(fh.read())
+        digest = h.hexdigest()[:16]
+    except OSError:
+        return None
+    for m in re.finditer(r"^\|\s*(\w+)\s*\|\s*([0-9]+)\s*\|\s*([0-9a-f]{16})\s*\|", text, re.M):
+        if m.group(1) == kernel and m.group(3) == digest:
+            return int(m.group(2))
+    return None
+
+
 def workload_config(w, extra=None):
     cfg = {"workload": w.name, "shape_per_kv": [w.L, w.T, w.C], "chunk_tokens": w.chunk_tokens,
            "bins_k": sorted(set(w.bins_k)), "bins_layer_split": sum(1 for b in w.bins_k if b == max(w.bins_k)),
@@ -235,23 +276,51 @@ def run_ours(args):
         dist.barrier()
     hbm, peak_kind = peaks()
 
-    # dominant kernel: decode fused with dequantisation (the only kernel of
-    # cg_decompress_chunk), timed alone with events on the launching stream
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    for a, b in kev:
-        flush.zero_()
-        a.record(stream)
-        cd.decompress()
-        b.record(stream)
-    torch.cuda.synchronize()
-    dec_kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    # Per-call device time on the launching stream. cg_decompress_chunk is one
+    # kernel (k_decode_pipe); cg_compress_chunk is k_compress_init (zeroing the
+    # look-back slots, a few microseconds) followed by k_compress_fused.
+    def time_call(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    comp_kernel_ms = time_call(lambda: cd.compress(k, v))
+    dec_kernel_ms = time_call(cd.decompress)
     n_el = 2 * w.L * w.T * w.C
     cdf_bytes = 2 * cd.cdf_elems
     side = cdf_bytes + 2 * 2 * w.L * w.T + 4 * cd.nstreams + 8 * (cd.nstreams + 1)
     dec_alg_bytes = total + side + 4 * n_el
     comp_alg_bytes = fp16_bytes + total + side
-    achieved = dec_alg_bytes / (dec_kernel_ms * 1e-3) / 1e9
+    A = max(max(w.bins_k), max(w.bins_v))
+    P = 1 << (A - 1).bit_length()
+    props = torch.cuda.get_device_properties(local)
+    max_mhz = clocks.get("sm_max_mhz") or 2070.0
+    # issue peak: SMs x 4 schedulers x one 32-lane instruction per cycle
+    peak_tops = props.multi_processor_count * 4 * 32 * max_mhz * 1e6 / 1e12
+    kern = {
+        "compress": ("k_compress_fused (quantise + CDF + encode + pack)", comp_kernel_ms,
+                     alg_ops_encode(), comp_alg_bytes, ["compress.cu", "coder.cuh", "cg_internal.cuh"]),
+        "decompress": ("k_decode_pipe (decode + dequantise)", dec_kernel_ms,
+                       alg_ops_decode(P), dec_alg_bytes, ["decode.cu", "cg_internal.cuh"]),
+    }
+    dom = "compress" if comp_kernel_ms >= dec_kernel_ms else "decompress"
+    kname, kms, ops, kbytes, srcs = kern[dom]
+    achieved = n_el * ops / (kms * 1e-3) / 1e12
+    hbm_achieved = kbytes / (kms * 1e-3) / 1e9
+    roofline = {
+        "kernel": kname, "bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Tops/s",
+        "frac": achieved / peak_tops, "traffic": kernel_traffic(kname.split()[0], srcs),
+        "peak_kind": f"derived: {props.multi_processor_count} SMs x 4 schedulers x 32 lanes x {max_mhz:g} MHz",
+        "ops_per_symbol": ops, "algorithmic_bytes": kbytes, "ms": kms,
+        "hbm": {"achieved": hbm_achieved, "peak": hbm, "unit": "GB/s", "frac": hbm_achieved / hbm,
+                "peak_kind": peak_kind},
+    }
 
     comp_gbs = fp16_bytes / (statistics.mean(comp_ms) * 1e-3) / 1e9
     dec_gbs = fp16_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9
@@ -270,16 +339,14 @@ def run_ours(args):
                                    "algorithmic": dec_alg_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9 / hbm},
         "compression_ratio": {"total": fp16_bytes / (total + side), "payload": fp16_bytes / total,
                               "bits_per_symbol": 8 * total / n_el},
-        "roofline": {"kernel": "k_decode (decode + dequantise)", "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None},
+        "roofline": roofline,
         "status_word": status, "clocks": clocks, "wall_s_timed_region": wall,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
     }
 
     if not args.no_e2e:
         result["e2e"] = e2e(args, cd, k_pin, v_pin, k, v, fp16_bytes, stream)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens))
         reps = max(1, int(10.0 / max(cpu_dt, 1e-3)))
         times = [cpu_dt]
