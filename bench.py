@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KV encode & decode GB/s (fp16 in) at 1 GB300, % of HBM roofline; compression ratio"
 UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
-KERNELS_PER_STEP = 3  # compress_init, compress_fused, decode_pipe (the ctx4096 shape takes the fused paths)
+KERNELS_PER_STEP = 3  # compress_init, compress_tma, decode_pipe (the ctx4096 shape takes the fused paths)
 
 
 def parse():
@@ -278,7 +278,7 @@ def run_ours(args):
 
     # Per-call device time on the launching stream. cg_decompress_chunk is one
     # kernel (k_decode_pipe); cg_compress_chunk is k_compress_init (zeroing the
-    # look-back slots, a few microseconds) followed by k_compress_fused.
+    # look-back slots, a few microseconds) followed by k_compress_tma.
     def time_call(fn):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
@@ -304,7 +304,7 @@ def run_ours(args):
     # issue peak: SMs x 4 schedulers x one 32-lane instruction per cycle
     peak_tops = props.multi_processor_count * 4 * 32 * max_mhz * 1e6 / 1e12
     kern = {
-        "compress": ("k_compress_fused (quantise + CDF + encode + pack)", comp_kernel_ms,
+        "compress": ("k_compress_tma (quantise + CDF + encode + pack)", comp_kernel_ms,
                      alg_ops_encode(), comp_alg_bytes, ["compress.cu", "coder.cuh", "cg_internal.cuh"]),
         "decompress": ("k_decode_pipe (decode + dequantise)", dec_kernel_ms,
                        alg_ops_decode(P), dec_alg_bytes, ["decode.cu", "cg_internal.cuh"]),

@@ -2,30 +2,42 @@
 // [CG §2.3(1)], per-channel CDF [CG §2.3(2)], range encoding [CG §1.2(3)] and
 // packing of one (chunk, kv, layer) slice per CTA, straight from fp16.
 //
-// Used for chunks of up to 256 tokens, alphabets up to 64 and C % 8 == 0 with
+// Used for chunks of up to 256 tokens, alphabets up to 32, C % 8 == 0 and
 // 16-byte aligned rows (other shapes take the quantise + slice-coder + scan
-// kernels). One thread per token stream. Per CTA:
+// kernels). One thread per token stream, 256 threads, three CTAs per SM.
+//
+// The fp16 slice [Tc_k][C] arrives in [rows][64-channel] boxes by TMA
+// (cp.async.bulk.tensor, completion on an mbarrier; every wait is bounded and
+// sets CG_FLAG_TIMEOUT when it runs out). Per CTA:
 //   0. take a slice ticket (so every slice a CTA waits on below belongs to a
-//      CTA that is already running); max1 of every token row (warp per row,
-//      128-bit loads, max of the fp16 magnitude bits) and factor = MAX / max1
+//      CTA that is already running);
+//   1. max1 pass: the slice's boxes stream through two buffers; each lane
+//      keeps the running max of the fp16 magnitude bits of its rows, then a
+//      half-warp reduction gives max1 per token and factor = MAX / max1
 //      (0 for an all-zero row: every value then maps to MAX);
-//   then per window of W channels:
-//   1. load the [Tc_k x W] fp16 tile with 128-bit loads, quantise it on the
-//      way into a shared symbol tile, and count each symbol with a shared
-//      atomic add into a per-window [symbol][channel] table of 16-bit counters
-//      (padded rows: the eight channels of one vector land in distinct banks);
-//   2. four threads per channel normalise its counts into a CDF row (two
-//      passes over their quarter of the alphabet, combined with shuffles),
-//      written as packed (lo | f << 16) entries and as the uint16 CDF output;
-//   3. every thread codes its token's W symbols;
+//   then per window of 64 channels (the next window's box is in flight while
+//   this one is coded):
+//   2. quantise the box, four channels per lane, two rows per warp
+//      instruction, each warp on the rows it codes later (so only a warp-level
+//      sync separates its coding of one window from its writes of the next).
+//      y = RN(RN(x * factor) + MAX) in binary32 (the adds two at a time as
+//      f32x2); adding 1.5 * 2^23 rounds y to the nearest integer, ties to even, into
+//      the low bits. Symbols go to a shared tile as 8q (a byte offset into a
+//      CDF row), counts to a [symbol][channel] table of 16-bit counters;
+//   3. four threads per channel turn its counts into a CDF row in one pass
+//      (own eight symbols, then a four-lane scan), zeroing the counters they
+//      read, and write (lo, f) pairs to shared memory and lo to the output;
+//   4. every thread codes its token's 64 symbols;
 //   after the last window:
-//   4. a block scan of the stream lengths gives offsets inside the slice, a
+//   5. a block scan of the stream lengths gives offsets inside the slice, a
 //      decoupled look-back over the preceding slices' totals gives the slice's
-//      offset in the packed buffer (spins are bounded; on timeout the
-//      CG_FLAG_TIMEOUT bit is set and the CTA carries on), and the CTA copies
-//      its streams from the staging area (L2-resident, just written) into
-//      place, clipped at the capacity.
+//      offset in the packed buffer (spins are bounded), and the CTA copies its
+//      streams from the staging area (L2-resident, just written) into place,
+//      clipped at the capacity.
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched through the runtime
 #include <cuda_fp16.h>
+
+#include <mutex>
 
 #include "cg_internal.cuh"
 #include "coder.cuh"
@@ -35,59 +47,93 @@ namespace {
 
 constexpr int kNT = 256;  // threads = max tokens per chunk on this path
 constexpr int kNW = kNT / 32;
+constexpr int kW = 64;        // channels per window = fp16 box width (128-byte rows)
+constexpr int kAmax = 32;     // largest alphabet on this path
+constexpr int kAS = kAmax + 1;  // (lo, f) entries per CDF row in shared memory
+constexpr int kSP = 8;        // symbols per CDF thread (four threads per channel)
+constexpr int kCntRow = kW + 2;  // 16-bit counters per symbol row (one spare word)
+constexpr int kSymRow = kW + 4;  // bytes per symbol-tile row (spreads rows over banks)
 constexpr uint32_t kTotal = 65536u;
+constexpr uint32_t kMagic = 0x4B400000u;  // bits of 1.5 * 2^23
 constexpr unsigned long long kFlagAggregate = 1ull << 62;
-constexpr unsigned long long kFlagPrefix = 2ull << 62;
 constexpr unsigned long long kValueMask = (1ull << 62) - 1;
 constexpr int kSpinLimit = 1 << 22;
+constexpr int kWaitLimit = 1 << 22;
 
-struct FusedSmem {
-    size_t tile, cnt, cdfw, ftab, fac, m1, scan, bytes;
-    int cnt_stride;  // 32-bit words per counter row (one row per symbol)
-};
+// The union region: CDF rows, counters and symbol tile while coding; the
+// second fp16 box buffer during the max1 pass.
+constexpr int kCdfwBytes = kW * kAS * 8;
+constexpr int kCntBytes = kAmax * kCntRow * 2;
+constexpr int kSymBytes = kNT * kSymRow;
+constexpr int kBoxBytesMax = kNT * kW * 2;
+constexpr int kCodeBytes = kCdfwBytes + kCntBytes + kSymBytes;
+constexpr int kUnionBytes = kCodeBytes > kBoxBytesMax ? kCodeBytes : kBoxBytesMax;
 
-template <int W>
-__host__ __device__ inline FusedSmem fused_layout(int A) {
-    FusedSmem s;
-    s.cnt_stride = W / 2 + 1;
-    size_t o = 0;
-    s.tile = o;
-    o += (size_t)kNT * (W + 4);
-    o = (o + 15) & ~(size_t)15;
-    s.cnt = o;  // [symbol][channel] uint16 counters, rows padded by one word
-    o += (size_t)A * s.cnt_stride * 4;
-    s.cdfw = o;  // [channel][A + 1] uint32
-    o += (size_t)W * (A + 1) * 4;
-    s.ftab = o;  // f(n), n = 0..kNT, uint16
-    o += (size_t)(kNT + 1) * 2;
-    o = (o + 3) & ~(size_t)3;
-    s.fac = o;  // float per token
-    o += (size_t)kNT * 4;
-    s.m1 = o;  // max1 bits per token
-    o += (size_t)kNT * 2;
-    o = (o + 7) & ~(size_t)7;
-    s.scan = o;  // kNW + 4 uint64 for the block scan and the slice base
-    o += (size_t)(kNW + 4) * 8;
-    s.bytes = (o + 15) & ~(size_t)15;
-    return s;
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Quantise two halves packed in w to two symbols (specification Q); factor 0
-// encodes an all-zero row. The unsigned min keeps non-finite input in range.
-__device__ __forceinline__ uint32_t quant2(uint32_t w, float factor, float fmax, uint32_t qmax) {
-    const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&w));
-    const uint32_t q0 = min((uint32_t)__float2int_rn(__fadd_rn(__fmul_rn(x.x, factor), fmax)), qmax);
-    const uint32_t q1 = min((uint32_t)__float2int_rn(__fadd_rn(__fmul_rn(x.y, factor), fmax)), qmax);
-    return q0 | (q1 << 8);
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
 }
 
-// Count symbol q of channel c (in the window) in the [q][c] uint16 table.
-__device__ __forceinline__ void count_symbol(uint32_t *cnt, int stride, uint32_t q, int c) {
-    atomicAdd(cnt + q * stride + (c >> 1), 1u << (16 * (c & 1)));
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ uint32_t count_of(const uint32_t *cnt, int stride, int s, int c) {
-    return (cnt[s * stride + (c >> 1)] >> (16 * (c & 1))) & 0xFFFFu;
+// Bounded wait for the phase with the given parity; false if it ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < kWaitLimit; i++) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// Box (x = channel, y = token, z = layer) of the tensor map into shared memory.
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                         uint32_t bar, uint32_t bytes) {
+    mbar_expect_tx(bar, bytes);
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void red_add(uint32_t addr, uint32_t v) {
+    asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long pair(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// y + 1.5 * 2^23 for two values, y = RN(RN(x * factor) + MAX) (specification
+// Q); the low byte of each result is rint(y) for y in [-0.5, 255]. The
+// products stay scalar: ptxas fuses a packed mul.rn.f32x2 feeding a packed
+// add.rn.f32x2 into one rounding (a fused multiply-add), which moves rare
+// near-ties to the next level; the two adds are packed.
+__device__ __forceinline__ void quant_pair(uint32_t h2, float f, unsigned long long fm, unsigned long long mg,
+                                           uint32_t &b0, uint32_t &b1) {
+    const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+    const float p0 = __fmul_rn(x.x, f), p1 = __fmul_rn(x.y, f);
+    asm("{\n\t.reg .b64 t;\n\t"
+        "mov.b64 t, {%2, %3};\n\t"
+        "add.rn.f32x2 t, t, %4;\n\t"
+        "add.rn.f32x2 t, t, %5;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t}"
+        : "=r"(b0), "=r"(b1)
+        : "f"(p0), "f"(p1), "l"(fm), "l"(mg));
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
@@ -106,20 +152,71 @@ __global__ void k_compress_init(unsigned long long *state, long long nslices) {
         state[i] = 0ull;  // state[0] is the ticket counter, state[1 + s] slice s
 }
 
-template <int W>
-__global__ void __launch_bounds__(kNT, 4) k_compress_fused(
-    const uint16_t *__restrict__ kin, const uint16_t *__restrict__ vin, Dims d, MaxTab mt,
-    uint16_t *__restrict__ max1_out, uint16_t *__restrict__ cdf_out, uint8_t *__restrict__ stage,
+// Step 2 for one window: quantise this lane's quads of its rows, store 8q to
+// the symbol tile and count q. SAFE (a slice with a non-finite max1, or a box
+// whose wait ran out) clamps q to [0, 2 MAX] before using it; finite input
+// under its own max1 needs no clamp.
+template <bool SAFE>
+__device__ __forceinline__ void quantise_window(const unsigned char *box, const float *fac, uint8_t *sym,
+                                                uint32_t cnt_lane, int rbase, int kq, int Tk,
+                                                unsigned long long fm, unsigned long long mg, uint32_t qmax) {
+#pragma unroll 4
+    for (int i = 0; i < kNT / 32 * 2; i++) {
+        const int r = rbase + 2 * i;
+        if (r >= Tk) break;
+        const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
+        const float f = fac[r];
+        uint32_t b0, b1, b2, b3;
+        quant_pair(x.x, f, fm, mg, b0, b1);
+        quant_pair(x.y, f, fm, mg, b2, b3);
+        if (SAFE) {
+            b0 = min(b0 - kMagic, qmax) + kMagic;
+            b1 = min(b1 - kMagic, qmax) + kMagic;
+            b2 = min(b2 - kMagic, qmax) + kMagic;
+            b3 = min(b3 - kMagic, qmax) + kMagic;
+        }
+        const uint32_t lo2 = __byte_perm(b0, b1, 0x0040), hi2 = __byte_perm(b2, b3, 0x0040);
+        *reinterpret_cast<uint32_t *>(sym + r * kSymRow + 4 * kq) = __byte_perm(lo2, hi2, 0x5410) << 3;
+        // counter word of (q, channel pair) = cnt_lane + 132 q (+4 for the second pair)
+        red_add(b0 * (kCntRow * 2) + cnt_lane, 1u);
+        red_add(b1 * (kCntRow * 2) + cnt_lane, 1u << 16);
+        red_add(b2 * (kCntRow * 2) + cnt_lane + 4, 1u);
+        red_add(b3 * (kCntRow * 2) + cnt_lane + 4, 1u << 16);
+    }
+}
+
+__global__ void __launch_bounds__(kNT, 3) k_compress_tma(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, Dims d, MaxTab mt,
+    int box_rows, uint16_t *__restrict__ max1_out, uint16_t *__restrict__ cdf_out, uint8_t *__restrict__ stage,
     uint32_t *__restrict__ len, uint64_t *__restrict__ off, uint8_t *__restrict__ packed,
     unsigned long long capacity, unsigned long long *state, int32_t *status) {
-    constexpr int TS = W + 4;
-    constexpr int VPR = W / 8;  // 8-half vectors per tile row
-    constexpr int TPC = kNT / W;  // threads per channel in the CDF step
-    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ __align__(1024) unsigned char s_union[kUnionBytes];
+    __shared__ unsigned long long s_scan[kNW + 4];
+    __shared__ unsigned long long s_bar[2];
+    __shared__ float s_fac[kNT];
+    __shared__ uint16_t s_m1[kNT];
+    __shared__ uint16_t s_ftab[kNT + 2];
     __shared__ int s_ticket;
+    extern __shared__ __align__(128) unsigned char dsm[];
+
+    uint2 *cdfw = reinterpret_cast<uint2 *>(s_union);
+    uint16_t *cnt16 = reinterpret_cast<uint16_t *>(s_union + kCdfwBytes);
+    uint32_t *cnt32 = reinterpret_cast<uint32_t *>(s_union + kCdfwBytes);
+    uint8_t *sym = s_union + kCdfwBytes + kCntBytes;
+    const uint32_t dyn = smem_u32(dsm);
+    const uint32_t buf0 = (dyn + 127u) & ~127u;  // box buffer 0 (dynamic, 128-byte aligned)
+    const uint32_t buf1 = smem_u32(s_union);     // box buffer 1 (max1 pass only)
+    const unsigned char *box0 = dsm + (buf0 - dyn);
+    const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) s_ticket = (int)atomicAdd(state, 1ull);
+    if (tid == 0) {
+        s_ticket = (int)atomicAdd(state, 1ull);
+        mbar_init(bar0);
+        mbar_init(bar1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     __syncthreads();
     const int ticket = s_ticket;
     int k, kv, l;
@@ -127,162 +224,188 @@ __global__ void __launch_bounds__(kNT, 4) k_compress_fused(
     const int A = d.A[kv];
     const int Tk = chunk_tokens(d, k);
     const int MAX = mt.v[kv][l];
-    const float fmax = (float)MAX;
-    const uint32_t qmax = 2u * (uint32_t)MAX;
-    const FusedSmem lay = fused_layout<W>(A);
-    const int cs = lay.cnt_stride;
-    uint8_t *tile = smem + lay.tile;
-    uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + lay.cnt);
-    uint32_t *cdfw = reinterpret_cast<uint32_t *>(smem + lay.cdfw);
-    uint16_t *ftab = reinterpret_cast<uint16_t *>(smem + lay.ftab);
-    float *fac = reinterpret_cast<float *>(smem + lay.fac);
-    uint16_t *m1 = reinterpret_cast<uint16_t *>(smem + lay.m1);
-    unsigned long long *scan = reinterpret_cast<unsigned long long *>(smem + lay.scan);
-
-    const long long t0 = (long long)k * d.Tc;
-    const uint16_t *x = (kv ? vin : kin) + (long long)l * d.layer_stride + t0 * d.C;
+    const CUtensorMap *tm = kv ? &tmv : &tmk;
+    const int t0 = k * d.Tc;
+    const int nwin = (d.C + kW - 1) / kW;
+    const uint32_t box_bytes = (uint32_t)box_rows * (kW * 2);
     const long long cdf_base = cdf_slice_offset(d, k, kv, l);
     const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk;
     const long long sid = sid0 + tid;
     uint8_t *stream = stage_stream(stage, tid < Tk ? sid : sid0, d);
+    // this lane's rows (rbase + 2i) and quad (channels 4 kq .. 4 kq + 3 of a window)
+    const int kq = lane & 15;
+    const int rbase = 32 * warp + (lane >> 4);
+    bool timed_out = false;
 
-    // 0. max1 per token row, the per-row factor and the f(n) table
-    const int nvec = d.C >> 3;
-    bool nonfinite = false;
-    for (int r = warp; r < Tk; r += kNW) {
-        const uint4 *row = reinterpret_cast<const uint4 *>(x + (long long)r * d.C);
-        unsigned m = 0;
-        for (int v0 = lane; v0 < nvec; v0 += 128) {
-            uint4 q[4];
+    if (tid == 0) {
+        tma_load(buf0, tm, 0, t0, l, bar0, box_bytes);
+        if (nwin > 1) tma_load(buf1, tm, kW, t0, l, bar1, box_bytes);
+    }
+
+    // 1. max1 pass over the slice's boxes (buffers alternate)
+    uint32_t ph0 = 0, ph1 = 0;
+    uint32_t mx[16];
 #pragma unroll
-            for (int u = 0; u < 4; u++)
-                q[u] = (v0 + 32 * u < nvec) ? __ldg(row + v0 + 32 * u) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 16; i++) mx[i] = 0;
+    for (int m = 0; m < nwin; m++) {
+        const bool odd = (m & 1) != 0;
+        if (!mbar_wait(odd ? bar1 : bar0, odd ? ph1 : ph0)) timed_out = true;
+        if (odd)
+            ph1 ^= 1u;
+        else
+            ph0 ^= 1u;
+        const unsigned char *box = odd ? s_union : box0;
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
-                m = __vmaxu2(m, q[u].x & 0x7FFF7FFFu);
-                m = __vmaxu2(m, q[u].y & 0x7FFF7FFFu);
-                m = __vmaxu2(m, q[u].z & 0x7FFF7FFFu);
-                m = __vmaxu2(m, q[u].w & 0x7FFF7FFFu);
+        for (int i = 0; i < 16; i++) {
+            const int r = rbase + 2 * i;
+            if (r < Tk) {
+                const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
+                mx[i] = __vmaxu2(mx[i], x.x & 0x7FFF7FFFu);
+                mx[i] = __vmaxu2(mx[i], x.y & 0x7FFF7FFFu);
             }
         }
-        m = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
-        if (lane == 0) {
-            m1[r] = (uint16_t)m;
-            max1_out[group_index(d, kv, l, t0 + r)] = (uint16_t)m;
-            nonfinite |= (m >= 0x7C00u);
+        __syncthreads();  // the buffer is free again
+        if (tid == 0) {
+            if (m + 2 < nwin)
+                tma_load(odd ? buf1 : buf0, tm, (m + 2) * kW, t0, l, odd ? bar1 : bar0, box_bytes);
+            else if (!odd)
+                tma_load(buf0, tm, 0, t0, l, bar0, box_bytes);  // first window of the coding loop
+        }
+    }
+    bool nonfinite = false;
+    {
+        uint32_t mine = 0;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            uint32_t v = max(mx[i] & 0xFFFFu, mx[i] >> 16);
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 8));
+            if (kq == i) mine = v;
+        }
+        const int r = rbase + 2 * kq;
+        if (r < Tk) {
+            s_m1[r] = (uint16_t)mine;
+            max1_out[group_index(d, kv, l, t0 + r)] = (uint16_t)mine;
+            nonfinite = mine >= 0x7C00u;
         }
     }
     for (int n = tid; n <= Tk; n += kNT)
-        ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kTotal - (uint32_t)A)) / (uint32_t)Tk);
-    for (int i = tid; i < A * cs; i += kNT) cnt[i] = 0;
-    __syncthreads();
+        s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kTotal - (uint32_t)A)) / (uint32_t)Tk);
+    for (int i = tid; i < kCntBytes / 4; i += kNT) cnt32[i] = 0;
+    nonfinite = __syncthreads_or(nonfinite) != 0;
+    const float fmax = (float)MAX;
     if (tid < Tk) {
-        const unsigned mb = m1[tid];
-        fac[tid] = mb ? __fdiv_rn(fmax, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
+        const unsigned mb = s_m1[tid];
+        s_fac[tid] = mb ? __fdiv_rn(fmax, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
     }
     __syncthreads();
 
+    const unsigned long long fm = pair(fmax, fmax);
+    const unsigned long long mg = pair(12582912.0f, 12582912.0f);
+    const uint32_t qmax = 2u * (uint32_t)MAX;
+    // counter byte address of (q, channel 4 kq) is cnt_lane + 132 * (kMagic + q)
+    const uint32_t cnt_lane = smem_u32(cnt32) + 8u * (uint32_t)kq - (uint32_t)(kCntRow * 2) * kMagic;
     Enc e;
     enc_init(e);
-    for (int c0 = 0; c0 < d.C; c0 += W) {
-        const int Wc = min(W, d.C - c0);  // a multiple of 8
-        // 1. fp16 tile -> symbol tile, counting every symbol
-        for (int i = tid; i < Tk * VPR; i += kNT) {
-            const int r = i / VPR, j = i % VPR;
-            if (8 * j < Wc) {
-                const uint4 h = __ldg(reinterpret_cast<const uint4 *>(x + (long long)r * d.C + c0) + j);
-                const float f = fac[r];
-                const uint32_t s01 = quant2(h.x, f, fmax, qmax), s23 = quant2(h.y, f, fmax, qmax);
-                const uint32_t s45 = quant2(h.z, f, fmax, qmax), s67 = quant2(h.w, f, fmax, qmax);
-                uint32_t *dst = reinterpret_cast<uint32_t *>(tile + r * TS + 8 * j);
-                dst[0] = s01 | (s23 << 16);
-                dst[1] = s45 | (s67 << 16);
-                const int cb = 8 * j;
-                count_symbol(cnt, cs, s01 & 0xFF, cb);
-                count_symbol(cnt, cs, s01 >> 8, cb + 1);
-                count_symbol(cnt, cs, s23 & 0xFF, cb + 2);
-                count_symbol(cnt, cs, s23 >> 8, cb + 3);
-                count_symbol(cnt, cs, s45 & 0xFF, cb + 4);
-                count_symbol(cnt, cs, s45 >> 8, cb + 5);
-                count_symbol(cnt, cs, s67 & 0xFF, cb + 6);
-                count_symbol(cnt, cs, s67 >> 8, cb + 7);
-            }
+    for (int w = 0; w < nwin; w++) {
+        const int c0 = w * kW;
+        const int Wc = min(kW, d.C - c0);  // a multiple of 8
+        if (!mbar_wait(bar0, ph0)) timed_out = true;
+        ph0 ^= 1u;
+        __syncwarp();  // this warp's coding of the previous window has read its symbol rows
+        // 2. quantise + count
+        if (4 * kq < Wc) {
+            // a box that did not arrive in time holds stale values: clamp those too
+            if (nonfinite || timed_out)
+                quantise_window<true>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+            else
+                quantise_window<false>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
         }
         __syncthreads();
-        // 2. CDF rows: thread (channel c, part p) owns symbols p, p + TPC, ...
+        if (tid == 0 && w + 1 < nwin) tma_load(buf0, tm, c0 + kW, t0, l, bar0, box_bytes);
+        // 3. CDF rows: thread (channel c, part p) owns symbols 8p .. 8p + 7
         {
-            const int c = tid / TPC, p = tid % TPC;
-            // a warp covers 32 / TPC channels and Wc is a multiple of 8, so a
-            // warp is entirely inside or entirely outside the window
+            const int c = tid >> 2, p = tid & 3;
+            // a warp covers eight channels and Wc is a multiple of 8, so a warp
+            // is entirely inside or entirely outside the window
             if (c < Wc) {
+                uint32_t fj[kSP], pre[kSP];
                 uint32_t sum = 0, key = 0;
-                for (int s = p; s < A; s += TPC) {
-                    const uint32_t n = count_of(cnt, cs, s, c);
-                    sum += ftab[n];
-                    key = max(key, (n << 8) | (255u - (uint32_t)s));  // largest n, then smallest s
-                }
 #pragma unroll
-                for (int o = 1; o < TPC; o <<= 1) {
-                    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+                for (int j = 0; j < kSP; j++) {
+                    const int s = kSP * p + j;
+                    uint32_t fv = 0;
+                    if (s < A) {
+                        uint16_t *cp = cnt16 + s * kCntRow + c;
+                        const uint32_t n = *cp;
+                        *cp = 0;
+                        fv = s_ftab[n];
+                        key = max(key, (n << 8) | (255u - (uint32_t)s));  // largest n, then smallest s
+                    }
+                    pre[j] = sum;
+                    sum += fv;
+                    fj[j] = fv;
+                }
+                uint32_t incl = sum;
+#pragma unroll
+                for (int o = 1; o < 4; o <<= 1) {
+                    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o, 4);
+                    if (p >= o) incl += v;
                     key = max(key, __shfl_xor_sync(0xFFFFFFFFu, key, o));
                 }
+                const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
+                const uint32_t base = incl - sum;
                 const uint32_t best = 255u - (key & 255u);
-                const uint32_t extra = kTotal - sum;
-                // cumulative walk over the symbols in order: each part walks the
-                // whole row's prefix of its own symbols through shuffles
-                uint32_t *row = cdfw + c * (A + 1);
+                const uint32_t extra = kTotal - total;
+                uint2 *row = cdfw + c * kAS;
                 uint16_t *g = cdf_out + cdf_base + (long long)(c0 + c) * A;
-                uint32_t lo = 0;
-                for (int s0 = 0; s0 < A; s0 += TPC) {
-                    const int s = s0 + p;
-                    uint32_t f = 0;
-                    if (s < A) f = (uint32_t)ftab[count_of(cnt, cs, s, c)] + ((uint32_t)s == best ? extra : 0u);
-                    uint32_t incl = f;
 #pragma unroll
-                    for (int o = 1; o < TPC; o <<= 1) {
-                        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o, TPC);
-                        if (p >= o) incl += v;
+                for (int j = 0; j < kSP; j++) {
+                    const uint32_t s = (uint32_t)(kSP * p + j);
+                    if ((int)s < A) {
+                        const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
+                        const uint32_t f = fj[j] + (s == best ? extra : 0u);
+                        row[s] = make_uint2(lo, f);
+                        g[s] = (uint16_t)lo;
                     }
-                    if (s < A) {
-                        const uint32_t mylo = lo + incl - f;
-                        row[s] = mylo | (f << 16);
-                        g[s] = (uint16_t)mylo;
-                    }
-                    lo += __shfl_sync(0xFFFFFFFFu, incl, TPC - 1, TPC);
                 }
             }
         }
         __syncthreads();
-        // the counters are free again: clear them for the next window
-        for (int i = tid; i < A * cs; i += kNT) cnt[i] = 0;
-        // 3. code my token's symbols of this window
+        // 4. code my token's symbols of this window
         if (tid < Tk) {
-            const uint8_t *my = tile + tid * TS;
-            const uint32_t *row = cdfw;
-            const int rs = A + 1;
-            if (Wc == W) {
-#pragma unroll 4
-                for (int c = 0; c < W; c += 4) {
-                    const uint32_t q4 = *reinterpret_cast<const uint32_t *>(my + c);
+            const uint32_t *my = reinterpret_cast<const uint32_t *>(sym + tid * kSymRow);
+            const unsigned char *rows = reinterpret_cast<const unsigned char *>(cdfw);
+            if (Wc == kW) {
+#pragma unroll
+                for (int g = 0; g < kW / 4; g++) {
+                    const uint32_t w4 = my[g];
+                    const unsigned char *r0 = rows + (4 * g) * kAS * 8;
+                    const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + (w4 & 0xFFu));
+                    const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + ((w4 >> 8) & 0xFFu));
+                    const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + ((w4 >> 16) & 0xFFu));
+                    const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + (w4 >> 24));
                     if (e.nbits >= 32) enc_flush_word(e, stream);
-                    enc_symbol(e, row[q4 & 0xFF]);
-                    enc_symbol(e, row[rs + ((q4 >> 8) & 0xFF)]);
+                    enc_symbol_lf(e, e0.x, e0.y);
+                    enc_symbol_lf(e, e1.x, e1.y);
                     if (e.nbits >= 32) enc_flush_word(e, stream);
-                    enc_symbol(e, row[2 * rs + ((q4 >> 16) & 0xFF)]);
-                    enc_symbol(e, row[3 * rs + (q4 >> 24)]);
-                    row += 4 * rs;
+                    enc_symbol_lf(e, e2.x, e2.y);
+                    enc_symbol_lf(e, e3.x, e3.y);
                 }
             } else {
+                const uint8_t *mb = sym + tid * kSymRow;
                 for (int c = 0; c < Wc; c++) {
+                    const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + mb[c]);
                     if (e.nbits >= 32) enc_flush_word(e, stream);
-                    enc_symbol(e, row[c * rs + my[c]]);
+                    enc_symbol_lf(e, en.x, en.y);
                 }
             }
         }
-        __syncthreads();
     }
 
-    // 4. lengths, offsets inside the slice, the slice's place, the copy
+    // 5. lengths, offsets inside the slice, the slice's place, the copy
     const uint32_t mylen = tid < Tk ? enc_finish(e, stream) : 0u;
     unsigned long long incl = mylen;
 #pragma unroll
@@ -290,21 +413,20 @@ __global__ void __launch_bounds__(kNT, 4) k_compress_fused(
         const unsigned long long v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += v;
     }
-    if (lane == 31) scan[warp] = incl;
+    if (lane == 31) s_scan[warp] = incl;
     __syncthreads();
     if (tid == 0) {
         unsigned long long run = 0;
         for (int w = 0; w < kNW; w++) {
-            const unsigned long long t = scan[w];
-            scan[w] = run;
+            const unsigned long long t = s_scan[w];
+            s_scan[w] = run;
             run += t;
         }
         // decoupled look-back over the previous slices (ticket order = stream order)
         unsigned long long *mine = state + 1 + ticket;
         unsigned long long base = 0;
-        bool timed_out = false;
         if (ticket == 0) {
-            st_release(mine, kFlagPrefix | run);
+            st_release(mine, (2ull << 62) | run);
         } else {
             st_release(mine, kFlagAggregate | run);
             long long j = ticket - 1;
@@ -324,26 +446,23 @@ __global__ void __launch_bounds__(kNT, 4) k_compress_fused(
                 if ((v >> 62) == 2) break;
                 j--;
             }
-            st_release(mine, kFlagPrefix | ((base + run) & kValueMask));
+            st_release(mine, (2ull << 62) | ((base + run) & kValueMask));
         }
-        scan[kNW] = base;
-        scan[kNW + 1] = run;
-        if (timed_out && status) atomicOr(status, CG_FLAG_TIMEOUT);
+        s_scan[kNW] = base;
         if (ticket == 2LL * d.L * d.nch - 1) {
             off[d.nstreams] = base + run;
             if (base + run > capacity && status) atomicOr(status, CG_FLAG_CAPACITY);
         }
     }
     __syncthreads();
-    const unsigned long long base = scan[kNW];
-    const unsigned long long myoff = base + scan[warp] + incl - mylen;
+    const unsigned long long myoff = s_scan[kNW] + s_scan[warp] + incl - mylen;
     if (tid < Tk) {
         len[sid] = mylen;
         off[sid] = myoff;
     }
     // copy: every stream's (offset, length) goes through shared memory, then a
     // warp at a time copies one stream in consecutive 4-byte words
-    unsigned long long *info = reinterpret_cast<unsigned long long *>(tile);  // reuse: 2 x kNT uint64
+    unsigned long long *info = reinterpret_cast<unsigned long long *>(sym);  // 2 x kNT uint64
     if (tid < Tk) {
         info[2 * tid] = myoff;
         info[2 * tid + 1] = mylen;
@@ -363,24 +482,40 @@ __global__ void __launch_bounds__(kNT, 4) k_compress_fused(
             }
         }
     }
-    if (nonfinite && status) atomicOr(status, CG_FLAG_NONFINITE);
+    if (status && (nonfinite || timed_out) && (tid == 0 || timed_out))
+        atomicOr(status, (nonfinite ? CG_FLAG_NONFINITE : 0) | (timed_out ? CG_FLAG_TIMEOUT : 0));
 }
 
-template <int W>
-cudaError_t launch_w(const uint16_t *k, const uint16_t *v, const Dims &d, const MaxTab &mt,
-                     uint16_t *max1, uint16_t *cdf, uint8_t *stage, uint32_t *len, uint64_t *off,
-                     uint8_t *packed, uint64_t capacity, unsigned long long *state, int32_t *status,
-                     cudaStream_t s) {
-    const size_t s0 = fused_layout<W>(d.A[0]).bytes, s1 = fused_layout<W>(d.A[1]).bytes;
-    const size_t smem = s0 > s1 ? s0 : s1;
-    cudaError_t err = cudaFuncSetAttribute(k_compress_fused<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-    if (err != cudaSuccess) return err;
-    const long long nslices = 2LL * d.L * d.nch;
-    k_compress_init<<<(unsigned)((nslices + 1 + 255) / 256), 256, 0, s>>>(state, nslices);
-    k_compress_fused<W><<<(unsigned)nslices, kNT, smem, s>>>(k, v, d, mt, max1, cdf, stage, len, off, packed,
-                                                              capacity, state, status);
-    return cudaGetLastError();
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// [L][T][C] fp16 with the given layer stride, boxes of [box_rows][kW].
+bool make_map(CUtensorMap *map, const uint16_t *base, const Dims &d, int box_rows) {
+    EncodeTiled fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d.C, (cuuint64_t)d.T, (cuuint64_t)d.L};
+    const cuuint64_t strides[2] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.layer_stride * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kW, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -390,17 +525,27 @@ bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v)
     const int A = d.A[0] > d.A[1] ? d.A[0] : d.A[1];
     const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0 &&
                          d.layer_stride % 8 == 0;
-    return tmax <= kNT && A <= 64 && d.C % 8 == 0 && aligned;
+    return d.T > 0 && tmax <= kNT && A <= kAmax && d.C % 8 == 0 && aligned;
 }
 
 cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d, const MaxTab &mt,
                                   uint16_t *max1, uint16_t *cdf, uint8_t *stage, uint32_t *len,
                                   uint64_t *off, uint8_t *packed, uint64_t capacity,
                                   unsigned long long *state, int32_t *status, cudaStream_t s) {
-    const int A = d.A[0] > d.A[1] ? d.A[0] : d.A[1];
-    if (A <= 32)
-        return launch_w<64>(k, v, d, mt, max1, cdf, stage, len, off, packed, capacity, state, status, s);
-    return launch_w<32>(k, v, d, mt, max1, cdf, stage, len, off, packed, capacity, state, status, s);
+    const int box_rows = d.Tc < d.T ? d.Tc : d.T;
+    CUtensorMap tmk, tmv;
+    if (!make_map(&tmk, k, d, box_rows) || !make_map(&tmv, v, d, box_rows)) return cudaErrorNotSupported;
+    const int dyn = 128 + box_rows * kW * 2;
+    cudaError_t err = cudaFuncSetAttribute(k_compress_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(k_compress_tma, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    const long long nslices = 2LL * d.L * d.nch;
+    k_compress_init<<<(unsigned)((nslices + 1 + 255) / 256), 256, 0, s>>>(state, nslices);
+    k_compress_tma<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, cdf, stage, len, off,
+                                                       packed, capacity, state, status);
+    return cudaGetLastError();
 }
 
 }  // namespace cg
