@@ -2,13 +2,19 @@
 // [CG §2.4(2)] for chunks of up to 256 tokens, specialised at compile time on
 // the CDF width P (the alphabet rounded up to a power of two).
 //
-// CTA per (chunk, kv, layer) slice, thread per token stream. For each window of
-// W channels the CTA stages the window's cumulative counts and frequencies in
-// shared memory (entries at or past A hold 65536 / 0, so an unrolled binary
-// search of log2(P) steps never leaves a valid stream's row); every thread
-// decodes its W symbols into a shared symbol tile, four per 32-bit store; the
-// tile then leaves as coalesced rows: dequantised binary32 through a per-layer
-// table of (q - MAX) / MAX, or raw symbols.
+// CTA per (chunk, kv, layer) slice: 256 decoder threads (one per token stream)
+// and one helper warp. For each window of W channels the helper stages the
+// window's cumulative counts and frequencies in shared memory (entries at or
+// past A hold 65535 / 0, so an unrolled binary search of log2(P) steps never
+// leaves a row); every decoder thread decodes its W symbols into a shared tile,
+// four per 32-bit store, while the helper writes the previous window's tile out
+// as coalesced rows: dequantised binary32 through a per-layer table of
+// (q - MAX) / MAX, or raw symbols. One barrier per window.
+//
+// Stream state is 32-bit: code, range, a 64-bit bit buffer held as two words,
+// and a prefetched word whose load has the next ~32 coded bits to land. Bytes
+// past a stream's end read as zero; the masked load runs only for a stream's
+// last words.
 #include <cuda_fp16.h>
 
 #include "cg_internal.cuh"
@@ -18,76 +24,95 @@ namespace {
 
 constexpr uint32_t kM = 65536u;
 constexpr int kThreads = 256;
+constexpr int kHelpers = 32;  // one helper warp per CTA
 
 template <int P>
 struct DecodeCfg {
     static constexpr int W = P <= 32 ? 64 : (P == 64 ? 32 : 16);  // channels per window
     static constexpr int TS = W + 4;                                 // symbol tile row stride
+    // tile bytes hold 4s (a byte offset into the dequantisation table) while
+    // that fits a byte, else s
+    static constexpr int SYM_SHIFT = P <= 64 ? 2 : 0;
 };
 
 struct Stream {
     uint32_t code, range;
-    uint64_t bb;     // bit buffer, next bits at the top
-    int nb;          // valid bits in bb
-    uint32_t next;   // prefetched big-endian word at byte offset wa
-    long long wa;    // offset of `next`; bytes [start, wa) are in bb or consumed
-    long long start; // first byte of the stream
-    long long end;   // one past the last readable byte of the stream
+    uint32_t bhi, blo;    // bit buffer, next bits at the top of bhi
+    int nb;               // valid bits in (bhi, blo)
+    uint32_t raw;         // the loaded next word, as in memory (not yet byte-swapped or masked)
+    int rem;              // stream bytes from raw's word onwards (<= 0 once past the end)
+    const uint32_t *wp;   // raw's word; stays on the stream's last word once rem <= 4
 };
 
-// Big-endian word at aligned byte offset wa, bytes outside [start, end) read
-// as 0; taken only for a stream's first and last words.
-__device__ __noinline__ uint32_t word_at_edge(const uint8_t *packed, long long wa, long long start,
-                                              long long end) {
+// Bytes [0, n) of the 4 at p in memory order (the others read as zero); for a
+// stream's first word and, in warps holding a stream that ends in the
+// buffer's last partial word, for every word.
+__device__ __noinline__ uint32_t bytes_masked(const uint8_t *p, int n) {
     uint32_t w = 0;
-    for (int i = 0; i < 4; i++) {
-        const long long p = wa + i;
-        w = (w << 8) | ((p >= start && p < end) ? (uint32_t)__ldg(packed + p) : 0u);
-    }
+    for (int i = 0; i < 4; i++)
+        if (i < n) w |= (uint32_t)__ldg(p + i) << (8 * i);
     return w;
 }
 
-__device__ __forceinline__ uint32_t word_at(const uint8_t *packed, long long wa, long long start,
-                                            long long end) {
-    if (wa >= start && wa + 4 <= end)
-        return __byte_perm(__ldg(reinterpret_cast<const uint32_t *>(packed + wa)), 0, 0x0123);
-    return word_at_edge(packed, wa, start, end);
+// Append the prefetched word below the nb valid bits when nb < 32, then load
+// the following word (TAIL: byte by byte, within the stream only). The
+// appended word is raw byte-swapped with the bytes past the stream's end
+// cleared; the loaded word is first used by the next refill, so its latency
+// hides behind about 32 decoded bits. Past the end the load repeats the
+// stream's last word, so it never leaves the stream's words.
+template <bool TAIL>
+__device__ __forceinline__ void refill(Stream &s) {
+    if (!TAIL) {
+        if (s.nb < 32) {
+            uint32_t v = __byte_perm(s.raw, 0, 0x0123);
+            const int t = max(32 - 8 * s.rem, 0);  // bits past the stream's end
+            v &= t >= 32 ? 0u : (0xFFFFFFFFu << t);
+            s.bhi |= v >> s.nb;
+            s.blo |= s.nb ? v << (32 - s.nb) : 0u;
+            s.nb += 32;
+            if (s.rem > 4) s.wp++;
+            s.rem -= 4;
+            s.raw = __ldg(s.wp);
+        }
+    } else if (s.nb < 32) {
+        uint32_t v = __byte_perm(s.raw, 0, 0x0123);
+        v = s.rem >= 4 ? v : (s.rem <= 0 ? 0u : v & (0xFFFFFFFFu << (32 - 8 * s.rem)));
+        s.bhi |= v >> s.nb;
+        s.blo |= s.nb ? v << (32 - s.nb) : 0u;
+        s.nb += 32;
+        if (s.rem > 4) s.wp++;
+        s.rem -= 4;
+        s.raw = s.rem > 0 ? bytes_masked(reinterpret_cast<const uint8_t *>(s.wp), s.rem) : 0u;
+    }
 }
 
-// Next word of the stream (wa >= start always holds once initialised).
-__device__ __forceinline__ uint32_t load_word(const uint8_t *packed, long long wa, long long start,
-                                              long long end) {
-    if (wa + 4 <= end)
-        return __byte_perm(__ldg(reinterpret_cast<const uint32_t *>(packed + wa)), 0, 0x0123);
-    return word_at_edge(packed, wa, start, end);
-}
-
-// Move the prefetched word into the bit buffer (needs nb <= 32) and start the
-// load of the following one, which has the next ~32 bits of decoding to land.
-__device__ __forceinline__ void refill(Stream &s, const uint8_t *packed) {
-    s.bb |= (uint64_t)s.next << (32 - s.nb);
-    s.nb += 32;
-    s.wa += 4;
-    s.next = load_word(packed, s.wa, s.start, s.end);
-}
-
-__device__ __forceinline__ void stream_init(Stream &s, const uint8_t *packed, long long start,
-                                            long long end) {
-    s.start = start;
-    s.end = end;
+// Stream over bytes [start, end) of the packed buffer (4-byte aligned); the
+// first words come byte by byte.
+__device__ __forceinline__ void stream_init(Stream &s, const uint8_t *packed, long long start, long long end) {
     const int a = (int)(start & 3);
     const long long w0 = start - a;
-    const uint32_t w = word_at(packed, w0, start, end);
-    s.bb = ((uint64_t)w << 32) << (8 * a);
+    // first word: bytes [a, min(4, end - w0)) belong to the stream; the bytes
+    // before `a` leave with the shift
+    const int n0 = (int)min(4LL, end - w0);
+    s.bhi = __byte_perm(bytes_masked(packed + w0, n0), 0, 0x0123) << (8 * a);
+    s.blo = 0;
     s.nb = 32 - 8 * a;
-    s.wa = w0 + 4;
-    s.next = load_word(packed, s.wa, start, end);
-    refill(s, packed);
-    s.code = (uint32_t)(s.bb >> 32);
-    s.bb <<= 32;
-    s.nb -= 32;
+    s.rem = (int)(end - (w0 + 4));
+    s.wp = reinterpret_cast<const uint32_t *>(packed + w0) + (s.rem > 0 ? 1 : 0);
+    s.raw = s.rem > 0 ? bytes_masked(packed + w0 + 4, s.rem) : 0u;
+    if (a == 0) {  // the first word alone fills code
+        s.code = s.bhi;
+        s.bhi = 0;
+        s.nb = 0;
+    } else {
+        refill<true>(s);
+        s.code = s.bhi;
+        s.bhi = s.blo;
+        s.blo = 0;
+        s.nb -= 32;
+    }
     s.range = 0xFFFFFFFFu;
-    refill(s, packed);
+    refill<true>(s);
 }
 
 // One binary-search step over a uint16 CDF row at shared address `addr`:
@@ -111,41 +136,40 @@ __device__ __forceinline__ void search_from(uint32_t &addr, uint32_t r, uint32_t
 
 // One symbol from the row of its channel: `cum` is the shared address of the
 // uint16 cumulative row, its frequencies sit frq_off bytes further; needs
-// nb >= 16. Entries at or past A hold cum = 65535: a valid stream's code never
-// reaches them (its symbol's upper bound is at most 65535), and the clamp to
-// A - 1 gives a corrupt stream the decoder rule's answer (largest s < A with
-// r*cum[s] <= code).
-template <int P>
-__device__ __forceinline__ uint32_t decode_symbol(Stream &s, uint32_t cum, uint32_t frq_off,
-                                                  uint32_t amax) {
+// nb >= 16. Returns the entry's byte offset in the row (2s). Entries at or
+// past A hold cum = 65535: a valid stream's code never passes symbol A - 1's
+// upper bound, and with CLAMP (A < P) the clamp to A - 1 gives both a valid
+// stream whose code reaches r * 65535 and a corrupt stream the decoder rule's
+// answer (largest s < A with r*cum[s] <= code). With A == P no entry is
+// padding and the search cannot pass A - 1.
+template <int P, bool CLAMP>
+__device__ __forceinline__ uint32_t decode_symbol(Stream &s, uint32_t cum, uint32_t frq_off, uint32_t amax2) {
     const uint32_t r = s.range >> 16;
     uint32_t addr = cum;
     search_from<P / 2>(addr, r, s.code);
-    addr = min(addr, cum + 2 * amax);
+    if (CLAMP) addr = min(addr, cum + amax2);
     uint32_t lo, f;
     asm("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(addr));
     asm("ld.shared.u16 %0, [%1];" : "=r"(f) : "r"(addr + frq_off));
     s.code -= r * lo;
     s.range = r * f;
     const uint32_t sh = __clz(s.range) & 24;
-    s.code = __funnelshift_l((uint32_t)(s.bb >> 32), s.code, sh);
-    s.bb <<= sh;
+    s.code = __funnelshift_l(s.bhi, s.code, sh);
+    s.bhi = __funnelshift_l(s.blo, s.bhi, sh);
+    s.blo <<= sh;
     s.nb -= (int)sh;
     s.range <<= sh;
-    return (addr - cum) >> 1;
+    return addr - cum;
 }
-
-constexpr int kHelpers = 32;  // one helper warp per CTA
 
 template <int P>
 struct PipeSmem {
     static constexpr int W = DecodeCfg<P>::W;
     static constexpr int TS = DecodeCfg<P>::TS;
-    static constexpr size_t cum = 0;                                   // [2][W][P] uint16
-    static constexpr size_t frq = cum + 2ull * W * P * 2;              // [2][W][P] uint16
+    static constexpr size_t cum = 0;                                        // [2][W][P] uint16
+    static constexpr size_t frq = cum + 2ull * W * P * 2;                   // [2][W][P] uint16
     static constexpr size_t tile = (frq + 2ull * W * P * 2 + 15) & ~15ull;  // [2][kThreads*TS]
-    static constexpr size_t unit = tile + 2ull * kThreads * TS;        // float[256]
-    static constexpr size_t m1 = unit + 256 * 4;                       // float[kThreads]
+    static constexpr size_t m1 = tile + 2ull * kThreads * TS;               // float[kThreads]
     static constexpr size_t bytes = m1 + kThreads * 4;
 };
 
@@ -192,41 +216,94 @@ __device__ __forceinline__ void stage_rows(uint16_t *cum, uint16_t *frq, const u
     }
 }
 
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+
 // Write the decoded window in `tile` out as rows: dequantised binary32
-// (MODE 1) or symbols (MODE 0). Executed by `nthr` threads with index `id`.
-template <int P, int MODE>
+// (MODE 1: unit[s] * max1, with unit[s] = (s - MAX) / MAX) or symbols (MODE
+// 0). NTHR threads with index `id` share the work. With 4s in the tile bytes
+// and the table 256-byte aligned, one byte permute makes each entry's shared
+// address (table base with the low byte replaced).
+template <int P, int MODE, int NTHR>
 __device__ __forceinline__ void write_window(const uint8_t *tile, const float *unit, const float *m1s,
                                              const Dims &d, int kv, int l, long long t0, int Tk, int c0,
-                                             int Wc, uint8_t *sym, float *out_k, float *out_v, int id,
-                                             int nthr) {
+                                             int Wc, uint8_t *sym, float *out_k, float *out_v, int id) {
     constexpr int W = DecodeCfg<P>::W;
     constexpr int TS = DecodeCfg<P>::TS;
+    constexpr int SH = DecodeCfg<P>::SYM_SHIFT;
     if (MODE == 0) {
         uint8_t *dst = sym + group_index(d, kv, l, t0) * d.C + c0;
-        for (int i = id; i < Tk * W; i += nthr) {
+        for (int i = id; i < Tk * W; i += NTHR) {
             const int r = i / W, j = i % W;
-            if (j < Wc) dst[(long long)r * d.C + j] = tile[r * TS + j];
+            if (j < Wc) dst[(long long)r * d.C + j] = (uint8_t)(tile[r * TS + j] >> SH);
         }
         return;
     }
     float *out = (kv ? out_v : out_k) + ((long long)l * d.T + t0) * d.C + c0;
-    if (Wc == W && (d.C & 3) == 0) {
-        constexpr int PR = W / 4;  // float4 per row
-        for (int i = id; i < Tk * PR; i += nthr) {
-            const int r = i / PR, j = i % PR;
-            const uint32_t q4 = *reinterpret_cast<const uint32_t *>(tile + r * TS + 4 * j);
-            const float m = m1s[r];
-            float4 o;
-            o.x = __fmul_rn(unit[q4 & 0xFF], m);
-            o.y = __fmul_rn(unit[(q4 >> 8) & 0xFF], m);
-            o.z = __fmul_rn(unit[(q4 >> 16) & 0xFF], m);
-            o.w = __fmul_rn(unit[q4 >> 24], m);
-            reinterpret_cast<float4 *>(out + (long long)r * d.C)[j] = o;
+    if (SH == 2 && Wc == W && (d.C & 3) == 0 && NTHR % (W / 4) == 0) {
+        constexpr int PR = W / 4;        // float4 per row
+        constexpr int RPI = NTHR / PR;   // rows per pass
+        const int j = id % PR;
+        int r = id / PR;
+        const uint32_t us = (uint32_t)__cvta_generic_to_shared(unit);
+        uint32_t ts = (uint32_t)__cvta_generic_to_shared(tile) + r * TS + 4 * j;
+        uint32_t ms = (uint32_t)__cvta_generic_to_shared(m1s) + 4 * r;
+        float4 *o = reinterpret_cast<float4 *>(out + (long long)r * d.C) + j;
+        const long long ostep = (long long)RPI * d.C / 4;
+#pragma unroll 1
+        for (; r < Tk; r += RPI, ts += RPI * TS, ms += 4 * RPI, o += ostep) {
+            const uint32_t q4 = lds_u32(ts);
+            const float m = lds_f32(ms);
+            const float u0 = lds_f32(__byte_perm(q4, us, 0x7650));
+            const float u1 = lds_f32(__byte_perm(q4, us, 0x7651));
+            const float u2 = lds_f32(__byte_perm(q4, us, 0x7652));
+            const float u3 = lds_f32(__byte_perm(q4, us, 0x7653));
+            *o = make_float4(__fmul_rn(u0, m), __fmul_rn(u1, m), __fmul_rn(u2, m), __fmul_rn(u3, m));
         }
     } else {
-        for (int i = id; i < Tk * W; i += nthr) {
+        for (int i = id; i < Tk * W; i += NTHR) {
             const int r = i / W, j = i % W;
-            if (j < Wc) out[(long long)r * d.C + j] = __fmul_rn(unit[tile[r * TS + j]], m1s[r]);
+            if (j < Wc) out[(long long)r * d.C + j] = __fmul_rn(unit[tile[r * TS + j] >> SH], m1s[r]);
+        }
+    }
+}
+
+// Decode this thread's Wc symbols of one window into its tile row.
+template <int P, bool CLAMP, bool TAIL>
+__device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t fo, uint32_t amax2, uint8_t *my,
+                                              int Wc) {
+    constexpr int W = DecodeCfg<P>::W;
+    constexpr int SH = DecodeCfg<P>::SYM_SHIFT;
+    if (Wc == W && !TAIL) {
+#pragma unroll 4
+        for (int c = 0; c < W; c += 4) {
+            const uint32_t rc = cb + 2 * P * c;
+            refill<TAIL>(s);
+            const uint32_t e0 = decode_symbol<P, CLAMP>(s, rc, fo, amax2);
+            const uint32_t e1 = decode_symbol<P, CLAMP>(s, rc + 2 * P, fo, amax2);
+            refill<TAIL>(s);
+            const uint32_t e2 = decode_symbol<P, CLAMP>(s, rc + 4 * P, fo, amax2);
+            const uint32_t e3 = decode_symbol<P, CLAMP>(s, rc + 6 * P, fo, amax2);
+            // e = 2s: store 4s (SH == 2) or s
+            const uint32_t w = SH == 2 ? 2u * (e0 | (e1 << 8) | (e2 << 16) | (e3 << 24))
+                                       : (e0 >> 1) | ((e1 >> 1) << 8) | ((e2 >> 1) << 16) | ((e3 >> 1) << 24);
+            *reinterpret_cast<uint32_t *>(my + c) = w;
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < Wc; c++) {
+            refill<TAIL>(s);
+            const uint32_t e = decode_symbol<P, CLAMP>(s, cb + 2 * P * c, fo, amax2);
+            my[c] = (uint8_t)(SH == 2 ? 2u * e : e >> 1);
         }
     }
 }
@@ -244,17 +321,17 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     using L = PipeSmem<P>;
     constexpr int W = L::W;
     constexpr int TS = L::TS;
+    __shared__ __align__(256) float s_unit[256];  // (s - MAX) / MAX
     extern __shared__ __align__(16) unsigned char smem[];
     uint16_t *cum = reinterpret_cast<uint16_t *>(smem + L::cum);
     uint16_t *frq = reinterpret_cast<uint16_t *>(smem + L::frq);
     uint8_t *tile = smem + L::tile;
-    float *unit = reinterpret_cast<float *>(smem + L::unit);
     float *m1s = reinterpret_cast<float *>(smem + L::m1);
 
     int k, kv, l;
     slice_coords(d, blockIdx.x, k, kv, l);
     const int A = d.A[kv];
-    const uint32_t amax = (uint32_t)A - 1;
+    const uint32_t amax2 = 2u * ((uint32_t)A - 1);
     const int Tk = chunk_tokens(d, k);
     const int tid = threadIdx.x;
     const bool helper = tid >= kThreads;
@@ -266,11 +343,11 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
 
     if (MODE == 1 && !helper) {
         const int MAX = mt.v[kv][l];
-        unit[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
+        s_unit[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
         if (tid < Tk) m1s[tid] = __half2float(__ushort_as_half(max1[group_index(d, kv, l, t0 + tid)]));
     }
     Stream s;
-    bool corrupt = false;
+    bool corrupt = false, tail = false;
     if (!helper && tid < Tk) {
         long long start = (long long)off[sid];
         long long end = start + (long long)len[sid];
@@ -280,7 +357,12 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
             end = min(end, packed_bytes);
         }
         stream_init(s, packed, start, end);
+        // whole-word loads stay inside the stream's first and last words; in
+        // the buffer's last, partial word they would cross its end
+        const long long p4 = packed_bytes & ~3LL;
+        tail = end > p4 || (start & ~3LL) >= p4;
     }
+    if (!helper) tail = __any_sync(0xFFFFFFFFu, tail);  // warp-uniform refill path
     // 128-bit row loads need 16-byte aligned windows: cdf itself, and every
     // slice offset a multiple of 8 entries (both alphabets multiples of 8)
     const bool vec = ((reinterpret_cast<uintptr_t>(cdf) & 15) == 0) && (d.A[0] % 8 == 0) &&
@@ -288,33 +370,26 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     if (helper) stage_rows<P>(cum, frq, cdf + cdf_base, A, min(W, d.C), hl, vec);
     __syncthreads();
 
+    const uint32_t fo = (uint32_t)(L::frq - L::cum);
     for (int i = 0; i < nwin; i++) {
         const int b = i & 1;
         const int c0 = i * W;
         const int Wc = min(W, d.C - c0);
         if (!helper) {
             if (tid < Tk) {
-                // shared addresses of this buffer's rows; frequencies follow at a fixed offset
+                // shared address of this buffer's rows; frequencies follow at a fixed offset
                 const uint32_t cb = (uint32_t)__cvta_generic_to_shared(cum + b * W * P);
-                const uint32_t fo = (uint32_t)(L::frq - L::cum);
                 uint8_t *my = tile + b * kThreads * TS + tid * TS;
-                if (Wc == W) {
-#pragma unroll 4
-                    for (int c = 0; c < W; c += 4) {
-                        const uint32_t rc = cb + 2 * P * c;
-                        if (s.nb < 32) refill(s, packed);
-                        const uint32_t q0 = decode_symbol<P>(s, rc, fo, amax);
-                        const uint32_t q1 = decode_symbol<P>(s, rc + 2 * P, fo, amax);
-                        if (s.nb < 32) refill(s, packed);
-                        const uint32_t q2 = decode_symbol<P>(s, rc + 4 * P, fo, amax);
-                        const uint32_t q3 = decode_symbol<P>(s, rc + 6 * P, fo, amax);
-                        *reinterpret_cast<uint32_t *>(my + c) = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
-                    }
+                if (A == P) {
+                    if (tail)
+                        decode_window<P, false, true>(s, cb, fo, amax2, my, Wc);
+                    else
+                        decode_window<P, false, false>(s, cb, fo, amax2, my, Wc);
                 } else {
-                    for (int c = 0; c < Wc; c++) {
-                        if (s.nb < 32) refill(s, packed);
-                        my[c] = (uint8_t)decode_symbol<P>(s, cb + 2 * P * c, fo, amax);
-                    }
+                    if (tail)
+                        decode_window<P, true, true>(s, cb, fo, amax2, my, Wc);
+                    else
+                        decode_window<P, true, false>(s, cb, fo, amax2, my, Wc);
                 }
             }
         } else {
@@ -322,19 +397,21 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
                 stage_rows<P>(cum + (b ^ 1) * W * P, frq + (b ^ 1) * W * P,
                               cdf + cdf_base + (long long)(c0 + W) * A, A, min(W, d.C - c0 - W), hl, vec);
             if (i >= 1)
-                write_window<P, MODE>(tile + (b ^ 1) * kThreads * TS, unit, m1s, d, kv, l, t0, Tk, c0 - W, W,
-                                      sym, out_k, out_v, hl, kHelpers);
+                write_window<P, MODE, kHelpers>(tile + (b ^ 1) * kThreads * TS, s_unit, m1s, d, kv, l, t0, Tk,
+                                                c0 - W, W, sym, out_k, out_v, hl);
         }
         __syncthreads();
     }
     // the last window, written by the whole CTA
     {
         const int i = nwin - 1;
-        write_window<P, MODE>(tile + (i & 1) * kThreads * TS, unit, m1s, d, kv, l, t0, Tk, i * W,
-                              min(W, d.C - i * W), sym, out_k, out_v, tid, kThreads + kHelpers);
+        write_window<P, MODE, kThreads + kHelpers>(tile + (i & 1) * kThreads * TS, s_unit, m1s, d, kv, l, t0, Tk,
+                                                   i * W, min(W, d.C - i * W), sym, out_k, out_v, tid);
     }
     if (!helper && tid < Tk) {
-        const long long consumed = (s.wa - s.start) - s.nb / 8;
+        // bytes taken from the stream: up to the loaded word (which starts rem
+        // bytes before the end), less the whole bytes still in the bit buffer
+        const long long consumed = (long long)len[sid] - s.rem - s.nb / 8;
         if ((corrupt || consumed != (long long)len[sid] + 3) && status) atomicOr(status, CG_FLAG_CORRUPT);
     }
 }
