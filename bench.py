@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KV encode & decode GB/s (fp16 in) at 1 GB300, % of HBM roofline; compression ratio"
 UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
-KERNELS_PER_STEP = 3  # compress_init, compress_tma, decode_pipe (the ctx4096 shape takes the fused paths)
+KERNELS_PER_STEP = 4  # compress_init, compress_tma, pack, decode_pipe (the ctx4096 shape takes the fused paths)
 
 
 def parse():

@@ -72,7 +72,7 @@ struct Workspace {
     uint8_t *stage;
     unsigned long long *partials;
     uint8_t *sym;
-    unsigned long long *state;  // fused compress: ticket + one look-back slot per slice
+    unsigned long long *state;  // fused compress: two tickets, a look-back slot and a total per slice
 };
 
 uint64_t encode_ws_bytes(const Dims &d) {
@@ -83,7 +83,7 @@ uint64_t encode_ws_bytes(const Dims &d) {
 
 uint64_t sym_bytes(const Dims &d) { return round_up(2ull * d.L * (uint64_t)d.T * d.C, kAlign); }
 
-uint64_t state_bytes(const Dims &d) { return round_up(8ull * (2ull * d.L * d.nch + 1), kAlign); }
+uint64_t state_bytes(const Dims &d) { return round_up(8ull * (2ull + 4ull * d.L * d.nch), kAlign); }
 
 Workspace carve(void *ws, const Dims &d, bool with_sym) {
     Workspace w;

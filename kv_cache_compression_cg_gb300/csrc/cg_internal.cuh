@@ -95,7 +95,8 @@ cudaError_t launch_scan_and_pack(const uint32_t *len, uint64_t *off,
 // A <= 64, C % 8 == 0, 16-byte aligned rows); compress_fused_applies says when.
 bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v);
 // Writes max1, cdf, len, off (incl. off[nstreams]) and packed; `state` holds
-// 1 + nslices zeroed-per-call uint64 words (ticket counter, look-back slots).
+// 2 + 2 * nslices uint64 words (two tickets, a look-back slot and a byte total
+// per slice), set up by the launch itself.
 cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d,
                                   const MaxTab &mt, uint16_t *max1, uint16_t *cdf,
                                   uint8_t *stage, uint32_t *len, uint64_t *off,

@@ -29,11 +29,13 @@
 //      read, and write (lo, f) pairs to shared memory and lo to the output;
 //   4. every thread codes its token's 64 symbols;
 //   after the last window:
-//   5. a block scan of the stream lengths gives offsets inside the slice, a
-//      decoupled look-back over the preceding slices' totals gives the slice's
-//      offset in the packed buffer (spins are bounded), and the CTA copies its
-//      streams from the staging area (L2-resident, just written) into place,
-//      clipped at the capacity.
+//   5. each stream's length and the slice's byte total go out; no CTA of this
+//      kernel waits on another.
+// k_pack then places the slices: it publishes every slice total at once, so
+// its decoupled look-back over the preceding slices only waits for CTAs that
+// have just started (spins are bounded), and copies the streams from the
+// staging area (just written, mostly L2-resident) into the packed buffer,
+// clipped at the capacity.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched through the runtime
 #include <cuda_fp16.h>
 
@@ -108,6 +110,14 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// Pull a box into L2 ahead of its TMA load.
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 __device__ __forceinline__ void red_add(uint32_t addr, uint32_t v) {
     asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -146,10 +156,13 @@ __device__ __forceinline__ void st_release(unsigned long long *p, unsigned long 
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// state: [0] compress ticket, [1] pack ticket, [2 + s] look-back slot of
+// slice s, [2 + nslices + s] byte total of slice s (written by the compress
+// kernel). The tickets and slots start at zero.
 __global__ void k_compress_init(unsigned long long *state, long long nslices) {
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i <= nslices;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 + nslices;
          i += (long long)gridDim.x * blockDim.x)
-        state[i] = 0ull;  // state[0] is the ticket counter, state[1 + s] slice s
+        state[i] = 0ull;
 }
 
 // Step 2 for one window: quantise this lane's quads of its rows, store 8q to
@@ -188,8 +201,7 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
 __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, Dims d, MaxTab mt,
     int box_rows, uint16_t *__restrict__ max1_out, uint16_t *__restrict__ cdf_out, uint8_t *__restrict__ stage,
-    uint32_t *__restrict__ len, uint64_t *__restrict__ off, uint8_t *__restrict__ packed,
-    unsigned long long capacity, unsigned long long *state, int32_t *status) {
+    uint32_t *__restrict__ len, unsigned long long *state, int32_t *status) {
     __shared__ __align__(1024) unsigned char s_union[kUnionBytes];
     __shared__ unsigned long long s_scan[kNW + 4];
     __shared__ unsigned long long s_bar[2];
@@ -240,6 +252,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     if (tid == 0) {
         tma_load(buf0, tm, 0, t0, l, bar0, box_bytes);
         if (nwin > 1) tma_load(buf1, tm, kW, t0, l, bar1, box_bytes);
+        for (int m = 2; m < 4 && m < nwin; m++) tma_prefetch_l2(tm, m * kW, t0, l);
     }
 
     // 1. max1 pass over the slice's boxes (buffers alternate)
@@ -266,6 +279,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         }
         __syncthreads();  // the buffer is free again
         if (tid == 0) {
+            if (m + 4 < nwin) tma_prefetch_l2(tm, (m + 4) * kW, t0, l);
             if (m + 2 < nwin)
                 tma_load(odd ? buf1 : buf0, tm, (m + 2) * kW, t0, l, odd ? bar1 : bar0, box_bytes);
             else if (!odd)
@@ -381,7 +395,8 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
             if (Wc == kW) {
 #pragma unroll
                 for (int g = 0; g < kW / 4; g++) {
-                    const uint32_t w4 = my[g];
+                    // every byte is 8q; the mask keeps any tile content 8-byte aligned
+                    const uint32_t w4 = my[g] & 0xF8F8F8F8u;
                     const unsigned char *r0 = rows + (4 * g) * kAS * 8;
                     const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + (w4 & 0xFFu));
                     const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + ((w4 >> 8) & 0xFFu));
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
             } else {
                 const uint8_t *mb = sym + tid * kSymRow;
                 for (int c = 0; c < Wc; c++) {
-                    const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + mb[c]);
+                    const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + (mb[c] & 0xF8u));
                     if (e.nbits >= 32) enc_flush_word(e, stream);
                     enc_symbol_lf(e, en.x, en.y);
                 }
@@ -405,85 +420,142 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         }
     }
 
-    // 5. lengths, offsets inside the slice, the slice's place, the copy
+    // 5. stream lengths and the slice's total (offsets and packing follow in
+    // k_pack, so no slice here waits on another)
     const uint32_t mylen = tid < Tk ? enc_finish(e, stream) : 0u;
-    unsigned long long incl = mylen;
+    if (tid < Tk) len[sid] = mylen;
+    uint32_t tot = mylen;  // a slice holds at most 256 * (2C + 8) bytes
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_scan[warp] = incl;
+    for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+    if (lane == 0) s_scan[warp] = tot;
     __syncthreads();
     if (tid == 0) {
         unsigned long long run = 0;
-        for (int w = 0; w < kNW; w++) {
-            const unsigned long long t = s_scan[w];
-            s_scan[w] = run;
-            run += t;
-        }
-        // decoupled look-back over the previous slices (ticket order = stream order)
-        unsigned long long *mine = state + 1 + ticket;
-        unsigned long long base = 0;
-        if (ticket == 0) {
-            st_release(mine, (2ull << 62) | run);
-        } else {
-            st_release(mine, kFlagAggregate | run);
-            long long j = ticket - 1;
-            while (j >= 0) {
-                unsigned long long v = ld_acquire(state + 1 + j);
-                int spins = 0;
-                while ((v >> 62) == 0 && spins < kSpinLimit) {
-                    __nanosleep(64);
-                    v = ld_acquire(state + 1 + j);
-                    spins++;
-                }
-                if ((v >> 62) == 0) {
-                    timed_out = true;
-                    break;
-                }
-                base += v & kValueMask;
-                if ((v >> 62) == 2) break;
-                j--;
-            }
-            st_release(mine, (2ull << 62) | ((base + run) & kValueMask));
-        }
-        s_scan[kNW] = base;
-        if (ticket == 2LL * d.L * d.nch - 1) {
-            off[d.nstreams] = base + run;
-            if (base + run > capacity && status) atomicOr(status, CG_FLAG_CAPACITY);
-        }
-    }
-    __syncthreads();
-    const unsigned long long myoff = s_scan[kNW] + s_scan[warp] + incl - mylen;
-    if (tid < Tk) {
-        len[sid] = mylen;
-        off[sid] = myoff;
-    }
-    // copy: every stream's (offset, length) goes through shared memory, then a
-    // warp at a time copies one stream in consecutive 4-byte words
-    unsigned long long *info = reinterpret_cast<unsigned long long *>(sym);  // 2 x kNT uint64
-    if (tid < Tk) {
-        info[2 * tid] = myoff;
-        info[2 * tid + 1] = mylen;
-    }
-    __syncthreads();
-    for (int t = warp; t < Tk; t += kNW) {
-        const unsigned long long dst = info[2 * t];
-        const uint32_t n = (uint32_t)info[2 * t + 1];
-        const uint8_t *src = stage_stream(stage, sid0 + t, d);
-        for (uint32_t b = 4u * lane; b < n; b += 128u) {
-            const uint32_t wv = *reinterpret_cast<const uint32_t *>(src + b);
-            const uint32_t nb = min(4u, n - b);
 #pragma unroll
-            for (uint32_t q = 0; q < 4; q++) {
-                const unsigned long long pos = dst + b + q;
-                if (q < nb && pos < capacity) packed[pos] = (uint8_t)(wv >> (8 * q));
-            }
-        }
+        for (int w = 0; w < kNW; w++) run += s_scan[w];
+        state[2 + 2LL * d.L * d.nch + ticket] = run;
     }
     if (status && (nonfinite || timed_out) && (tid == 0 || timed_out))
         atomicOr(status, (nonfinite ? CG_FLAG_NONFINITE : 0) | (timed_out ? CG_FLAG_TIMEOUT : 0));
+}
+
+// Offsets and packing: CTA per slice in stream order (by ticket). Every
+// slice's byte total is known when this kernel starts, so each CTA publishes
+// its aggregate at once and its decoupled look-back (32 predecessors per step,
+// bounded spins) never waits on slow work. Then a block scan of the lengths
+// gives each stream's offset, and warps copy the streams from the staging
+// area into place, clipped at the capacity; lane i takes word i of a stream,
+// eight streams per batch of loads.
+__global__ void __launch_bounds__(kNT) k_pack(Dims d, const uint8_t *__restrict__ stage,
+                                              const uint32_t *__restrict__ len, uint64_t *__restrict__ off,
+                                              uint8_t *__restrict__ packed, unsigned long long capacity,
+                                              unsigned long long *state, int32_t *status) {
+    __shared__ unsigned long long s_scan[kNW + 1];
+    __shared__ uint32_t s_len[kNT], s_loc[kNT];
+    __shared__ int s_ticket;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long nslices = 2LL * d.L * d.nch;
+    if (tid == 0) {
+        // take the next slice and publish its total at once
+        const long long t = (long long)atomicAdd(state + 1, 1ull);
+        s_ticket = (int)t;
+        st_release(state + 2 + t, (t == 0 ? (2ull << 62) : kFlagAggregate) | state[2 + nslices + t]);
+    }
+    __syncthreads();
+    const int ticket = s_ticket;
+    int k, kv, l;
+    slice_coords(d, ticket, k, kv, l);
+    const int Tk = chunk_tokens(d, k);
+    const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk;
+    bool timed_out = false;
+    // offsets inside the slice
+    const uint32_t mylen = tid < Tk ? len[sid0 + tid] : 0u;
+    uint32_t incl = mylen;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+    s_len[tid] = mylen;
+    __syncthreads();
+    uint32_t wbase = 0;
+#pragma unroll
+    for (int w = 0; w < kNW; w++) wbase += w < warp ? (uint32_t)s_scan[w] : 0u;
+    s_loc[tid] = wbase + incl - mylen;
+    if (warp == 0) {
+        const unsigned long long run = state[2 + nslices + ticket];
+        unsigned long long *mine = state + 2 + ticket;
+        unsigned long long base = 0;
+        for (long long j = ticket - 1; j >= 0; j -= 32) {
+            const long long idx = j - lane;
+            unsigned long long v = idx >= 0 ? ld_acquire(state + 2 + idx) : (2ull << 62);
+            for (int spins = 0; __any_sync(0xFFFFFFFFu, (v >> 62) == 0) && spins < kSpinLimit; spins++) {
+                if ((v >> 62) == 0) {
+                    __nanosleep(32);
+                    v = ld_acquire(state + 2 + idx);
+                }
+            }
+            if (__any_sync(0xFFFFFFFFu, (v >> 62) == 0)) {
+                timed_out = true;
+                break;
+            }
+            const unsigned pm = __ballot_sync(0xFFFFFFFFu, (v >> 62) == 2);
+            const int first = pm ? __ffs(pm) - 1 : 31;
+            unsigned long long x = lane <= first ? (v & kValueMask) : 0ull;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+            base += x;
+            if (pm) break;
+        }
+        if (lane == 0) {
+            if (ticket > 0) st_release(mine, (2ull << 62) | ((base + run) & kValueMask));
+            s_scan[kNW] = base;
+            if (ticket == nslices - 1) {
+                off[d.nstreams] = base + run;
+                if (base + run > capacity && status) atomicOr(status, CG_FLAG_CAPACITY);
+            }
+        }
+    }
+    // the first batch of stage words is read while warp 0 looks back
+    constexpr int kBatch = 8;
+    uint32_t held[kBatch];
+    auto load_batch = [&](int b0) {
+#pragma unroll
+        for (int u = 0; u < kBatch; u++) {
+            const int t = warp + kNW * (b0 + u);
+            held[u] = 0;
+            if (t < Tk && 4u * lane < s_len[t])
+                held[u] = *reinterpret_cast<const uint32_t *>(stage_stream(const_cast<uint8_t *>(stage), sid0 + t, d) +
+                                                              4 * lane);
+        }
+    };
+    load_batch(0);
+    __syncthreads();
+    const unsigned long long sbase = s_scan[kNW];
+    if (tid < Tk) off[sid0 + tid] = sbase + s_loc[tid];
+    const int nper = (Tk + kNW - 1) / kNW;  // streams per warp
+    for (int b0 = 0; b0 < nper; b0 += kBatch) {
+        if (b0 > 0) load_batch(b0);
+#pragma unroll
+        for (int u = 0; u < kBatch; u++) {
+            const int t = warp + kNW * (b0 + u);
+            if (t >= Tk) continue;
+            const uint32_t n = s_len[t];
+            const unsigned long long dst = sbase + s_loc[t];
+            const uint8_t *src = stage_stream(const_cast<uint8_t *>(stage), sid0 + t, d);
+            for (uint32_t b = 4u * lane; b < n; b += 128u) {
+                const uint32_t wv = b < 128u ? held[u] : *reinterpret_cast<const uint32_t *>(src + b);
+                const uint32_t nb = min(4u, n - b);
+#pragma unroll
+                for (uint32_t q = 0; q < 4; q++) {
+                    const unsigned long long pos = dst + b + q;
+                    if (q < nb && pos < capacity) packed[pos] = (uint8_t)(wv >> (8 * q));
+                }
+            }
+        }
+    }
+    if (timed_out && status && lane == 0) atomicOr(status, CG_FLAG_TIMEOUT);
 }
 
 // cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
@@ -542,9 +614,10 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
                                cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     const long long nslices = 2LL * d.L * d.nch;
-    k_compress_init<<<(unsigned)((nslices + 1 + 255) / 256), 256, 0, s>>>(state, nslices);
-    k_compress_tma<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, cdf, stage, len, off,
-                                                       packed, capacity, state, status);
+    k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
+    k_compress_tma<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, cdf, stage, len, state,
+                                                       status);
+    k_pack<<<(unsigned)nslices, kNT, 0, s>>>(d, stage, len, off, packed, capacity, state, status);
     return cudaGetLastError();
 }
 

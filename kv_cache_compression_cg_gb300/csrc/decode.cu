@@ -261,7 +261,7 @@ __device__ __forceinline__ void write_window(const uint8_t *tile, const float *u
         const long long ostep = (long long)RPI * d.C / 4;
 #pragma unroll 1
         for (; r < Tk; r += RPI, ts += RPI * TS, ms += 4 * RPI, o += ostep) {
-            const uint32_t q4 = lds_u32(ts);
+            const uint32_t q4 = lds_u32(ts) & 0xFCFCFCFCu;  // 4s: keeps every table load aligned
             const float m = lds_f32(ms);
             const float u0 = lds_f32(__byte_perm(q4, us, 0x7650));
             const float u1 = lds_f32(__byte_perm(q4, us, 0x7651));
