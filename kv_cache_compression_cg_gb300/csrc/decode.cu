@@ -3,13 +3,14 @@
 // the CDF width P (the alphabet rounded up to a power of two).
 //
 // CTA per (chunk, kv, layer) slice: 256 decoder threads (one per token stream)
-// and one helper warp. For each window of W channels the helper stages the
-// window's cumulative counts and frequencies in shared memory (entries at or
-// past A hold 65535 / 0, so an unrolled binary search of log2(P) steps never
-// leaves a row); every decoder thread decodes its W symbols into a shared tile,
-// four per 32-bit store, while the helper writes the previous window's tile out
-// as coalesced rows: dequantised binary32 through a per-layer table of
-// (q - MAX) / MAX, or raw symbols. One barrier per window.
+// and one helper warp. While the decoders work on window i the helper stages
+// window i + 1's cumulative counts and frequencies in shared memory (entries at
+// or past A hold 65535 / 0, so an unrolled binary search of log2(P) steps never
+// leaves a row). Every decoder thread decodes its W symbols into its row of a
+// shared tile, four per 32-bit store; then each warp writes its own 32 rows out
+// as coalesced row segments: dequantised binary32 through a per-layer table of
+// (q - MAX) / MAX, or raw symbols. One barrier per window (for the row
+// buffers); the tile rows are warp-private.
 //
 // Stream state is 32-bit: code, range, a 64-bit bit buffer held as two words,
 // and a prefetched word whose load has the next ~32 coded bits to land. Bytes
@@ -168,8 +169,8 @@ struct PipeSmem {
     static constexpr int TS = DecodeCfg<P>::TS;
     static constexpr size_t cum = 0;                                        // [2][W][P] uint16
     static constexpr size_t frq = cum + 2ull * W * P * 2;                   // [2][W][P] uint16
-    static constexpr size_t tile = (frq + 2ull * W * P * 2 + 15) & ~15ull;  // [2][kThreads*TS]
-    static constexpr size_t m1 = tile + 2ull * kThreads * TS;               // float[kThreads]
+    static constexpr size_t tile = (frq + 2ull * W * P * 2 + 15) & ~15ull;  // [kThreads*TS]
+    static constexpr size_t m1 = tile + 1ull * kThreads * TS;               // float[kThreads]
     static constexpr size_t bytes = m1 + kThreads * 4;
 };
 
@@ -309,9 +310,8 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
 }
 
 // CTA = kThreads decoder threads (one per token stream) + one helper warp.
-// Iteration i: decoders decode window i with rows[i & 1] into tile[i & 1]
-// while the helper stages rows[(i + 1) & 1] and writes out tile[(i + 1) & 1]
-// (window i - 1); one barrier per window.
+// Iteration i: decoders decode window i with rows[i & 1] and write it out
+// while the helper stages rows[(i + 1) & 1]; one barrier per window.
 template <int P, int MODE>
 __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     const uint8_t *__restrict__ packed, long long packed_bytes, const uint64_t *__restrict__ off,
@@ -371,6 +371,9 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     __syncthreads();
 
     const uint32_t fo = (uint32_t)(L::frq - L::cum);
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wrows = min(32, Tk - 32 * warp);  // rows of this decoder warp
+    uint8_t *wtile = tile + warp * 32 * TS;
     for (int i = 0; i < nwin; i++) {
         const int b = i & 1;
         const int c0 = i * W;
@@ -379,7 +382,7 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
             if (tid < Tk) {
                 // shared address of this buffer's rows; frequencies follow at a fixed offset
                 const uint32_t cb = (uint32_t)__cvta_generic_to_shared(cum + b * W * P);
-                uint8_t *my = tile + b * kThreads * TS + tid * TS;
+                uint8_t *my = tile + tid * TS;
                 if (A == P) {
                     if (tail)
                         decode_window<P, false, true>(s, cb, fo, amax2, my, Wc);
@@ -392,21 +395,16 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
                         decode_window<P, true, false>(s, cb, fo, amax2, my, Wc);
                 }
             }
-        } else {
-            if (i + 1 < nwin)
-                stage_rows<P>(cum + (b ^ 1) * W * P, frq + (b ^ 1) * W * P,
-                              cdf + cdf_base + (long long)(c0 + W) * A, A, min(W, d.C - c0 - W), hl, vec);
-            if (i >= 1)
-                write_window<P, MODE, kHelpers>(tile + (b ^ 1) * kThreads * TS, s_unit, m1s, d, kv, l, t0, Tk,
-                                                c0 - W, W, sym, out_k, out_v, hl);
+            __syncwarp();
+            if (wrows > 0)
+                write_window<P, MODE, 32>(wtile, s_unit, m1s + 32 * warp, d, kv, l, t0 + 32 * warp, wrows, c0, Wc,
+                                          sym, out_k, out_v, lane);
+            __syncwarp();  // the rows are read before the next window overwrites them
+        } else if (i + 1 < nwin) {
+            stage_rows<P>(cum + (b ^ 1) * W * P, frq + (b ^ 1) * W * P, cdf + cdf_base + (long long)(c0 + W) * A, A,
+                          min(W, d.C - c0 - W), hl, vec);
         }
         __syncthreads();
-    }
-    // the last window, written by the whole CTA
-    {
-        const int i = nwin - 1;
-        write_window<P, MODE, kThreads + kHelpers>(tile + (i & 1) * kThreads * TS, s_unit, m1s, d, kv, l, t0, Tk,
-                                                   i * W, min(W, d.C - i * W), sym, out_k, out_v, tid);
     }
     if (!helper && tid < Tk) {
         // bytes taken from the stream: up to the loaded word (which starts rem
