@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ctx4096")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--piece-chunks", type=int, default=2,
+                    help="chunks per piece of the streamed end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -345,7 +347,7 @@ def run_ours(args):
     }
 
     if not args.no_e2e:
-        result["e2e"] = e2e(args, cd, k_pin, v_pin, k, v, fp16_bytes, stream)
+        result["e2e"] = e2e(args, w, cd, k_pin, v_pin, fp16_bytes)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens))
         reps = max(1, int(10.0 / max(cpu_dt, 1e-3)))
@@ -364,54 +366,41 @@ def run_ours(args):
         print(json.dumps(result))
 
 
-def e2e(args, cd, k_pin, v_pin, k, v, fp16_bytes, stream):
-    """Through the public API with host buffers: the sender copies fp16 K/V in,
-    compresses and copies the compressed chunk out; the receiver copies it in,
-    decompresses, and reads the status word back."""
+def e2e(args, w, cd, k_pin, v_pin, fp16_bytes):
+    """Through the public streaming API with host buffers: pinned fp16 K, V go
+    in piece by piece (runs of whole chunks) while earlier pieces compress;
+    each compressed piece comes back to pinned host memory as it is done; the
+    receiver copies each piece back in and decompresses it, and the status
+    words come back to the host. One step = all of that for the whole tensor;
+    the decompressed output is checked once against the single-call result."""
     import torch
-    o = cd.out
-    total = o.total_bytes()
-    host_packed = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-    host_len = torch.empty_like(o.len, device="cpu").pin_memory()
-    host_off = torch.empty_like(o.off, device="cpu").pin_memory()
-    host_cdf = torch.empty_like(o.cdf, device="cpu").pin_memory()
-    host_max1 = torch.empty_like(o.max1, device="cpu").pin_memory()
-    host_status = torch.empty(1, dtype=torch.int32, pin_memory=True)
-    from kv_cache_compression_cg_gb300 import codec as codec_mod
-    rx = codec_mod.Compressed(o.L, o.T, o.C, o.chunk_tokens, o.bins_k, o.bins_v,
-                              max1=torch.empty_like(o.max1), cdf=torch.empty_like(o.cdf),
-                              packed=torch.empty(max(total, 16), dtype=torch.uint8, device="cuda"),
-                              len=torch.empty_like(o.len), off=torch.empty_like(o.off),
-                              status=torch.zeros_like(o.status))
-    h2d = d2h = 0
+    from kv_cache_compression_cg_gb300.stream import StreamingCodec
+    sc = StreamingCodec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens,
+                        piece_chunks=args.piece_chunks)
     times = []
-    for i in range(args.warmup + args.steps):
+    pieces = outs = None
+    for i in range(max(args.warmup, 3) + args.steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        k.copy_(k_pin, non_blocking=True)
-        v.copy_(v_pin, non_blocking=True)
-        cd.compress(k, v)
-        n = cd.out.total_bytes()  # 8-byte read, needed to size the copy
-        host_packed[:n].copy_(o.packed[:n], non_blocking=True)
-        for h, dsrc in ((host_len, o.len), (host_off, o.off), (host_cdf, o.cdf), (host_max1, o.max1)):
-            h.copy_(dsrc, non_blocking=True)
-        rx.packed[:n].copy_(host_packed[:n], non_blocking=True)
-        for dd, h in ((rx.len, host_len), (rx.off, host_off), (rx.cdf, host_cdf), (rx.max1, host_max1)):
-            dd.copy_(h, non_blocking=True)
-        cd.decompress(rx)
-        host_status.copy_(cd.dstatus, non_blocking=True)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
+        pieces, outs, done = sc.roundtrip(k_pin, v_pin)
+        done.synchronize()
+        if i >= max(args.warmup, 3):
             times.append(time.perf_counter() - t0)
-        side = (host_len.numel() * 4 + host_off.numel() * 8 + host_cdf.numel() * 2 +
-                host_max1.numel() * 2)
-        h2d = fp16_bytes + n + side
-        d2h = 8 + n + side + 4
+    status = sc.status()
+    # the streamed output equals the single-call one, piece by piece
+    ref_k, ref_v = cd.decompress()
+    torch.cuda.synchronize()
+    exact = all(torch.equal(ok.view(torch.int32), ref_k[:, hp.t0:hp.t1].view(torch.int32)) and
+                torch.equal(ov.view(torch.int32), ref_v[:, hp.t0:hp.t1].view(torch.int32))
+                for (ok, ov), hp in zip(outs, pieces))
+    h2d, d2h = sc.bytes_moved(pieces)
     sec = statistics.mean(times)
     return {"value": fp16_bytes / sec / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": sec * 1e3,
-            "path": "pinned host fp16 K,V -> compress -> compressed chunk to host -> back to "
-                    "device -> decompress -> status word to host"}
+            "d2h_bytes_per_step": d2h, "ms_per_step": sec * 1e3, "pieces": len(pieces),
+            "status_word": status, "matches_single_call": exact,
+            "path": "pinned host fp16 K,V -> per piece of %d chunks: copy in, compress, compressed piece "
+                    "to pinned host -> copy back in, decompress -> status words to host (5 CUDA streams)"
+                    % args.piece_chunks}
 
 
 def main():

@@ -1,0 +1,253 @@
+"""Chunk-pipelined streaming between pinned host memory and the GPU.
+
+The page streams a context's KV cache chunk by chunk: chunks are coded
+independently, so a chunk can be sent while the next one is still being
+encoded ([CG §1.2(4)], chunk-wise processing; [CG §2.3(2)], one CDF set per
+chunk). `StreamingCodec` does that on one GPU with six CUDA streams:
+
+- sender: the fp16 K, V rows of piece p (a run of whole chunks) go host to
+  device on the copy-in stream while piece p - 1 is compressed on the coding
+  stream; each compressed piece goes back to pinned host buffers on the
+  copy-out stream as soon as it is done;
+- receiver: each host piece is copied in and decompressed as soon as its bytes
+  are on the host, while later pieces are still moving.
+
+A piece's compressed bytes are exactly the bytes of those chunks in a
+whole-tensor call (streams are chunk-major), so `shard.assemble` of the pieces'
+host arrays gives the whole tensor's compressed form. Every coding step runs in
+the CUDA library through `codec.Codec`; this module only orders copies and
+launches.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import ctypes.util
+import dataclasses
+import os
+
+import numpy as np
+import torch
+
+from . import codec as _codec
+
+__all__ = ["StreamingCodec", "HostPiece"]
+
+_MEMCPY_H2D = 1
+_rt = None
+
+
+def _cudart():
+    """The CUDA runtime, for strided (2D) asynchronous copies."""
+    global _rt
+    if _rt is None:
+        cands = [ctypes.util.find_library("cudart"), "/usr/local/cuda/lib64/libcudart.so"]
+        for c in cands:
+            if c and (os.path.exists(c) or not os.path.isabs(c)):
+                try:
+                    lib = C.CDLL(c)
+                    break
+                except OSError:
+                    continue
+        else:
+            raise RuntimeError("CUDA runtime library not found")
+        lib.cudaMemcpy2DAsync.restype = C.c_int
+        lib.cudaMemcpy2DAsync.argtypes = [C.c_void_p, C.c_size_t, C.c_void_p, C.c_size_t, C.c_size_t,
+                                          C.c_size_t, C.c_int, C.c_void_p]
+        lib.cudaMemcpyAsync.restype = C.c_int
+        lib.cudaMemcpyAsync.argtypes = [C.c_void_p, C.c_void_p, C.c_size_t, C.c_int, C.c_void_p]
+        _rt = lib
+    return _rt
+
+
+_MEMCPY_DEFAULT = 4  # direction from the pointers (unified addressing)
+
+
+def _copy(dst: torch.Tensor, src: torch.Tensor, nbytes: int, stream: torch.cuda.Stream):
+    """Asynchronous copy of the first nbytes of src to dst on `stream` (one
+    runtime call; torch's copy_ between pinned host and device memory spends
+    a few hundred microseconds on the host, which would stall the pipeline)."""
+    if nbytes <= 0:
+        return
+    if nbytes > dst.numel() * dst.element_size() or nbytes > src.numel() * src.element_size():
+        raise ValueError("copy larger than a buffer")
+    err = _cudart().cudaMemcpyAsync(C.c_void_p(dst.data_ptr()), C.c_void_p(src.data_ptr()), nbytes,
+                                    _MEMCPY_DEFAULT, C.c_void_p(stream.cuda_stream))
+    if err != 0:
+        raise RuntimeError(f"cudaMemcpyAsync failed ({err})")
+
+
+def _nb(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+@dataclasses.dataclass
+class HostPiece:
+    """Compressed tokens [t0, t1) in pinned host memory (one codec call)."""
+    t0: int
+    t1: int
+    nbytes: int
+    packed: torch.Tensor   # uint8 [capacity]; bytes [0, nbytes) are the streams
+    len: torch.Tensor      # int32 [2 L (t1 - t0)] (uint32)
+    off: torch.Tensor      # int64 [2 L (t1 - t0) + 1]
+    cdf: torch.Tensor      # int16 (uint16 entries)
+    max1: torch.Tensor     # int16 [2, L, t1 - t0] (fp16 bits)
+    ready: torch.cuda.Event
+
+    def arrays(self) -> dict:
+        """numpy views in the layout `shard.assemble` joins."""
+        return {"max1": self.max1.numpy().view(np.uint16), "cdf": self.cdf.numpy().view(np.uint16),
+                "packed": self.packed[:self.nbytes].numpy(), "len": self.len.numpy().view(np.uint32),
+                "off": self.off.numpy().view(np.uint64)}
+
+
+class StreamingCodec:
+    """Pipelined compress from pinned host K, V and decompress of host pieces.
+
+    All buffers (device staging of the fp16 input, one sender and one receiver
+    codec per piece, pinned host pieces) are allocated once here.
+    """
+
+    def __init__(self, L: int, T: int, C_: int, bins_k, bins_v=None, chunk_tokens: int = 256,
+                 piece_chunks: int = 2, device: str | torch.device = "cuda"):
+        if piece_chunks < 1:
+            raise ValueError("piece_chunks must be >= 1")
+        self.L, self.T, self.C = L, T, C_
+        self.bins_k = bins_k
+        self.bins_v = bins_k if bins_v is None else bins_v
+        step = piece_chunks * chunk_tokens
+        self.ranges = [(t0, min(T, t0 + step)) for t0 in range(0, T, step)]
+        dev = torch.device(device)
+        self.k = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
+        self.v = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
+        mk = lambda t0, t1: _codec.Codec(L, t1 - t0, C_, self.bins_k, self.bins_v, chunk_tokens=chunk_tokens,
+                                         device=dev)
+        self.enc = [mk(t0, t1) for t0, t1 in self.ranges]
+        self.dec = [mk(t0, t1) for t0, t1 in self.ranges]
+        self.host = []
+        for cd in self.enc:
+            o = cd.out
+            pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            self.host.append(dict(packed=torch.empty(cd.capacity, dtype=torch.uint8, pin_memory=True),
+                                  len=pin(o.len), off=pin(o.off), cdf=pin(o.cdf), max1=pin(o.max1)))
+        self.n_host = torch.zeros(len(self.ranges), dtype=torch.int64, pin_memory=True)
+        self.status_host = torch.zeros(2 * len(self.ranges), dtype=torch.int32, pin_memory=True)
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_code = torch.cuda.Stream(device=dev)
+        self.s_n = torch.cuda.Stream(device=dev)    # byte counts (kept off s_out: each waits on its piece)
+        self.s_out = torch.cuda.Stream(device=dev)
+        self.s_rx = torch.cuda.Stream(device=dev)
+        self.s_dec = torch.cuda.Stream(device=dev)
+        ev = lambda: [torch.cuda.Event() for _ in self.ranges]
+        self.ev_in, self.ev_enc, self.ev_n, self.ev_out, self.ev_rx = ev(), ev(), ev(), ev(), ev()
+        self.ev_done = torch.cuda.Event()
+
+    # -- sender ---------------------------------------------------------------
+    def _copy_in(self, dst: torch.Tensor, src: torch.Tensor, t0: int, t1: int):
+        rt = _cudart()
+        row = self.C * 2
+        pitch = self.T * row
+        err = rt.cudaMemcpy2DAsync(C.c_void_p(dst.data_ptr() + t0 * row), pitch,
+                                   C.c_void_p(src.data_ptr() + t0 * row), pitch, (t1 - t0) * row, self.L,
+                                   _MEMCPY_H2D, C.c_void_p(self.s_in.cuda_stream))
+        if err != 0:
+            raise RuntimeError(f"cudaMemcpy2DAsync failed ({err})")
+
+    def _send(self, p: int, k_host: torch.Tensor, v_host: torch.Tensor):
+        t0, t1 = self.ranges[p]
+        self._copy_in(self.k, k_host, t0, t1)
+        self._copy_in(self.v, v_host, t0, t1)
+        self.ev_in[p].record(self.s_in)
+        self.s_code.wait_event(self.ev_in[p])
+        self.enc[p].compress(self.k[:, t0:t1], self.v[:, t0:t1], stream=self.s_code)
+        self.ev_enc[p].record(self.s_code)
+        self.s_n.wait_event(self.ev_enc[p])
+        _copy(self.n_host[p:p + 1], self.enc[p].out.off[-1:], 8, self.s_n)
+        self.ev_n[p].record(self.s_n)
+
+    def stream_pieces(self, k_host: torch.Tensor, v_host: torch.Tensor, ahead: int = 2):
+        """fp16 [L, T, C] pinned host K, V -> compressed pieces in pinned host
+        memory, yielded in order as soon as each piece's copy-out is enqueued
+        (its `ready` event marks the bytes on the host). Input copies run
+        `ahead` pieces in front of the piece being yielded, so copies a
+        consumer enqueues for piece p (the receiver's) take their place in the
+        host-to-device queue behind piece p + ahead's input rather than behind
+        every input."""
+        for t in (k_host, v_host):
+            if t.device.type != "cpu" or not t.is_pinned() or t.dtype != torch.float16 or not t.is_contiguous():
+                raise ValueError("K and V must be contiguous pinned host fp16 tensors")
+            if tuple(t.shape) != (self.L, self.T, self.C):
+                raise ValueError("K/V shape differs from the streamer's")
+        npc = len(self.ranges)
+        ahead = max(1, ahead)
+        for p in range(min(ahead, npc)):
+            self._send(p, k_host, v_host)
+        for p, (t0, t1) in enumerate(self.ranges):
+            self.ev_n[p].synchronize()  # the piece's byte count, needed to size its copy
+            n = int(self.n_host[p])
+            o, h = self.enc[p].out, self.host[p]
+            self.s_out.wait_event(self.ev_enc[p])
+            _copy(h["packed"], o.packed, n, self.s_out)
+            for key in ("len", "off", "cdf", "max1"):
+                _copy(h[key], getattr(o, key), _nb(h[key]), self.s_out)
+            _copy(self.status_host[2 * p:2 * p + 1], o.status, 4, self.s_out)
+            self.ev_out[p].record(self.s_out)
+            yield HostPiece(t0, t1, n, h["packed"], h["len"], h["off"], h["cdf"], h["max1"], self.ev_out[p])
+            if p + ahead < npc:
+                self._send(p + ahead, k_host, v_host)
+
+    def compress_from_host(self, k_host: torch.Tensor, v_host: torch.Tensor) -> list[HostPiece]:
+        """All pieces of `stream_pieces` (returns once every copy-out is enqueued)."""
+        return list(self.stream_pieces(k_host, v_host))
+
+    # -- receiver -------------------------------------------------------------
+    def receive(self, p: int, hp: HostPiece, upload: torch.cuda.Stream | None = None):
+        """Piece p (host) -> fp32 [L, t1 - t0, C] K, V on the device: copy in on
+        `upload` (default: the receiver's own stream) once the piece is on the
+        host, decompress on the decoding stream, status word back to the host."""
+        rx, cd = self.dec[p].out, self.dec[p]
+        up = self.s_rx if upload is None else upload
+        up.wait_event(hp.ready)
+        _copy(rx.packed, hp.packed, hp.nbytes, up)
+        for key in ("len", "off", "cdf", "max1"):
+            _copy(getattr(rx, key), getattr(hp, key), _nb(getattr(hp, key)), up)
+        self.ev_rx[p].record(up)
+        self.s_dec.wait_event(self.ev_rx[p])
+        out = cd.decompress(rx, stream=self.s_dec)
+        _copy(self.status_host[2 * p + 1:2 * p + 2], cd.dstatus, 4, self.s_dec)
+        return out
+
+    def decompress_from_host(self, pieces, upload: torch.cuda.Stream | None = None):
+        """Every piece through `receive`; `pieces` may be the `stream_pieces`
+        generator, so each piece's receive is enqueued as soon as it exists.
+        Returns the list of (out_k, out_v) and the event that marks the last
+        decompression (and the status words in `status_host`) done."""
+        outs = [self.receive(p, hp, upload) for p, hp in enumerate(pieces)]
+        self.ev_done.record(self.s_dec)
+        return outs, self.ev_done
+
+    def roundtrip(self, k_host: torch.Tensor, v_host: torch.Tensor):
+        """Compress from host, ship each piece to the host and back, decompress:
+        returns (pieces, outs, done event), receiver work enqueued piece by piece
+        as the sender produces them. The uploads share the input-copy stream, so
+        the host-to-device queue alternates: input p + 2 waits behind upload p."""
+        pieces = []
+
+        def gen():
+            for hp in self.stream_pieces(k_host, v_host):
+                pieces.append(hp)
+                yield hp
+        outs, done = self.decompress_from_host(gen(), upload=self.s_in)
+        return pieces, outs, done
+
+    def status(self) -> int:
+        """OR of every piece's compress and decompress status words (call
+        after the returned event has completed)."""
+        return int(np.bitwise_or.reduce(self.status_host.numpy()))
+
+    def bytes_moved(self, pieces: list[HostPiece]) -> tuple[int, int]:
+        """(host-to-device, device-to-host) bytes of one compress + decompress."""
+        fp16 = 2 * 2 * self.L * self.T * self.C
+        side = sum(hp.len.numel() * 4 + hp.off.numel() * 8 + hp.cdf.numel() * 2 + hp.max1.numel() * 2
+                   for hp in pieces)
+        comp = sum(hp.nbytes for hp in pieces)
+        return fp16 + comp + side, 8 * len(pieces) + comp + side + 8 * len(pieces)

@@ -1,0 +1,55 @@
+"""The chunk-pipelined streaming path: pinned host K, V in, compressed pieces
+out to pinned host memory, pieces back in and decompressed. The pieces,
+joined, are byte-identical to the oracle's whole-tensor output (and to one
+call over the whole tensor), and the decompressed pieces equal the
+single-call output row for row."""
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_compression_cg_gb300 import shard
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,T,Tc,piece_chunks", [("tiny", 64, 64, 1), ("mistral_chunk", 200, 32, 2),
+                                                   ("mistral_chunk", 256, 64, 3)])
+def test_stream_pieces_match_oracle_and_single_call(synth_mod, oracle_mod, name, T, Tc, piece_chunks):
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required")
+    from kv_cache_compression_cg_gb300 import build, codec
+    from kv_cache_compression_cg_gb300.stream import StreamingCodec
+    build.build()
+    w = synth_mod.WORKLOADS[name]
+    k, v = synth_mod.generate(w, T=T)
+    k_pin = torch.from_numpy(k).pin_memory()
+    v_pin = torch.from_numpy(v).pin_memory()
+    sc = StreamingCodec(w.L, T, w.C, w.bins_k, w.bins_v, chunk_tokens=Tc, piece_chunks=piece_chunks)
+    pieces = sc.compress_from_host(k_pin, v_pin)  # list form, then the interleaved form
+    outs, done = sc.decompress_from_host(pieces)
+    done.synchronize()
+    pieces, outs, done = sc.roundtrip(k_pin, v_pin)  # reuse of every buffer
+    done.synchronize()
+    assert sc.status() == 0
+    joined = shard.assemble([hp.arrays() for hp in pieces])
+    ref = oracle_mod.compress(k, v, Tc, w.bins_k, w.bins_v)
+    for key in ("max1", "cdf", "packed", "len", "off"):
+        assert np.array_equal(joined[key], ref[key]), key
+    whole = codec.Codec(w.L, T, w.C, w.bins_k, w.bins_v, chunk_tokens=Tc)
+    whole.compress(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    rk, rv = whole.decompress()
+    torch.cuda.synchronize()
+    for (ok, ov), hp in zip(outs, pieces):
+        assert torch.equal(ok.view(torch.int32), rk[:, hp.t0:hp.t1].view(torch.int32))
+        assert torch.equal(ov.view(torch.int32), rv[:, hp.t0:hp.t1].view(torch.int32))
+
+
+def test_stream_rejects_pageable_input(synth_mod):
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required")
+    from kv_cache_compression_cg_gb300.stream import StreamingCodec
+    w = synth_mod.WORKLOADS["tiny"]
+    k, v = synth_mod.generate(w)
+    sc = StreamingCodec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens)
+    with pytest.raises(ValueError):
+        sc.compress_from_host(torch.from_numpy(k), torch.from_numpy(v))
