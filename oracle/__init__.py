@@ -70,6 +70,15 @@ def lib() -> C.CDLL:
                 "orc_compress": (C.c_int, [p, p, C.c_int, C.c_int, C.c_int, C.c_int, i64,
                                            p, p, p, p, p, u64, p, p]),
                 "orc_decompress": (C.c_int, [p, p, p, p, p] + [C.c_int] * 4 + [p, p, p, p]),
+                "orc_alphabet_v2": (C.c_int, [C.c_int]),
+                "orc_rec_bytes": (i64, [C.c_int] * 4 + [p, p]),
+                "orc_rec_offset": (i64, [C.c_int, C.c_int, p, p] + [C.c_int] * 4),
+                "orc_record_from_counts": (C.c_int, [p, C.c_int, p]),
+                "orc_counts_from_record": (C.c_int, [p, C.c_int, C.c_uint32, p]),
+                "orc_cdf_from_counts_mode": (C.c_int, [p, C.c_int, C.c_uint32, C.c_int, p]),
+                "orc_compress_v2": (C.c_int, [p, p, C.c_int, C.c_int, C.c_int, C.c_int, i64,
+                                              p, p, p, p, p, u64, p, p]),
+                "orc_decompress_v2": (C.c_int, [p, p, p, p, p] + [C.c_int] * 4 + [p, p, p, p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -301,4 +310,87 @@ def decompress(packed, off, ln, cdf, max1, L, T, C_, Tc, bins_k, bins_v=None):
                                 _ptr(np.ascontiguousarray(max1, np.uint16)),
                                 L, T, C_, Tc, _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)),
            "decompress")
+    return out_k, out_v
+
+
+# ----------------------------------------------------------------------------
+# format 2: side information as symbol counts
+# ----------------------------------------------------------------------------
+def alphabet_v2(bins: int) -> int:
+    """A = 2*MAX + 1 symbols for a layer with `bins` bins."""
+    return lib().orc_alphabet_v2(int(bins))
+
+
+def rec_bytes(L, T, C_, Tc, bins_k, bins_v=None) -> int:
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    return int(lib().orc_rec_bytes(L, T, C_, Tc, _ptr(bk), _ptr(bv)))
+
+
+def rec_offset(L, C_, bins_k, bins_v, k, kv, l, c) -> int:
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    return int(lib().orc_rec_offset(L, C_, _ptr(bk), _ptr(bv), k, kv, l, c))
+
+
+def record_from_counts(counts) -> np.ndarray:
+    n = np.ascontiguousarray(np.asarray(counts, dtype=np.uint32))
+    rec = np.zeros(n.size, np.uint8)
+    _check(lib().orc_record_from_counts(_ptr(n), n.size, _ptr(rec)), "record_from_counts")
+    return rec
+
+
+def counts_from_record(rec, Tk: int) -> np.ndarray:
+    r = np.ascontiguousarray(np.asarray(rec, dtype=np.uint8))
+    n = np.zeros(r.size, np.uint32)
+    _check(lib().orc_counts_from_record(_ptr(r), r.size, int(Tk), _ptr(n)), "counts_from_record")
+    return n
+
+
+def cdf_from_counts_mode(counts, Tk: int, mode: int) -> np.ndarray:
+    n = np.ascontiguousarray(np.asarray(counts, dtype=np.uint32))
+    cdf = np.zeros(n.size, np.uint16)
+    _check(lib().orc_cdf_from_counts_mode(_ptr(n), n.size, int(Tk), int(mode), _ptr(cdf)),
+           "cdf_from_counts_mode")
+    return cdf
+
+
+def compress_v2(k, v, Tc: int, bins_k, bins_v=None):
+    """Format 2: quantise -> counts -> records -> encode. Returns max1, rec,
+    packed, len, off."""
+    k, v = _bits(k), _bits(v)
+    L, T, C_ = k.shape
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    ns = num_streams(L, T)
+    cap = max_compressed_bytes(L, T, C_)
+    max1 = np.empty((2, L, T), np.uint16)
+    rec = np.zeros(max(rec_bytes(L, T, C_, Tc, bk, bv), 1), np.uint8)
+    packed = np.zeros(max(cap, 1), np.uint8)
+    ln = np.empty(max(ns, 1), np.uint32)
+    off = np.empty(ns + 1, np.uint64)
+    _check(lib().orc_compress_v2(_ptr(k), _ptr(v), L, T, C_, Tc, T * C_, _ptr(bk), _ptr(bv),
+                                 _ptr(max1), _ptr(rec), _ptr(packed), cap, _ptr(ln), _ptr(off)),
+           "compress_v2")
+    nrec = rec_bytes(L, T, C_, Tc, bk, bv)
+    return {"max1": max1, "rec": rec[:nrec].copy(), "packed": packed[:int(off[-1])].copy(),
+            "len": ln[:ns], "off": off}
+
+
+def decompress_v2(packed, off, ln, rec, max1, L, T, C_, Tc, bins_k, bins_v=None):
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    if packed.size == 0:
+        packed = np.zeros(1, np.uint8)
+    rec = np.ascontiguousarray(rec, dtype=np.uint8)
+    if rec.size == 0:
+        rec = np.zeros(1, np.uint8)
+    out_k = np.empty((L, T, C_), np.float32)
+    out_v = np.empty((L, T, C_), np.float32)
+    _check(lib().orc_decompress_v2(_ptr(packed), _ptr(np.ascontiguousarray(off, np.uint64)),
+                                   _ptr(np.ascontiguousarray(ln, np.uint32)), _ptr(rec),
+                                   _ptr(np.ascontiguousarray(max1, np.uint16)),
+                                   L, T, C_, Tc, _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)),
+           "decompress_v2")
     return out_k, out_v

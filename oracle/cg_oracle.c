@@ -461,3 +461,250 @@ int orc_decompress(const uint8_t *packed, const uint64_t *off,
     free(sym);
     return st;
 }
+
+/* ---- format 2: side information as symbol counts (specification S, F2) ---- */
+
+int orc_alphabet_v2(int bins)
+{
+    return 2 * (bins / 2 - 1) + 1;
+}
+
+/* Bytes of one chunk's records of one tensor: C records per layer. */
+static int64_t orc_rec_tensor_bytes(int L, int C, const int32_t *bins)
+{
+    int64_t b = 0;
+    for (int l = 0; l < L; l++)
+        b += (int64_t)C * orc_alphabet_v2(bins[l]);
+    return b;
+}
+
+int64_t orc_rec_bytes(int L, int T, int C, int Tc, const int32_t *bins_k,
+                      const int32_t *bins_v)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1)
+        return -1;
+    if (!bins_v)
+        bins_v = bins_k;
+    int64_t nch = (T + Tc - 1) / Tc;
+    return nch * (orc_rec_tensor_bytes(L, C, bins_k) +
+                  orc_rec_tensor_bytes(L, C, bins_v));
+}
+
+int64_t orc_rec_offset(int L, int C, const int32_t *bins_k,
+                       const int32_t *bins_v, int k, int kv, int l, int c)
+{
+    if (!bins_v)
+        bins_v = bins_k;
+    int64_t per_k = orc_rec_tensor_bytes(L, C, bins_k);
+    int64_t o = (int64_t)k * (per_k + orc_rec_tensor_bytes(L, C, bins_v));
+    if (kv)
+        o += per_k;
+    const int32_t *bins = kv ? bins_v : bins_k;
+    for (int j = 0; j < l; j++)
+        o += (int64_t)C * orc_alphabet_v2(bins[j]);
+    return o + (int64_t)c * orc_alphabet_v2(bins[l]);
+}
+
+/* The mode: the largest count, the smallest symbol on ties. */
+static int orc_mode(const uint32_t *n, int A)
+{
+    int best = 0;
+    for (int s = 1; s < A; s++)
+        if (n[s] > n[best])
+            best = s;
+    return best;
+}
+
+int orc_record_from_counts(const uint32_t *n, int A, uint8_t *rec)
+{
+    if (A < 2 || A > 256)
+        return ORC_ERR_ARG;
+    int m = orc_mode(n, A);
+    rec[0] = (uint8_t)m;
+    int i = 1;
+    for (int s = 0; s < A; s++) {
+        if (s == m)
+            continue;
+        if (n[s] > 255)
+            return ORC_ERR_ARG;
+        rec[i++] = (uint8_t)n[s];
+    }
+    return ORC_OK;
+}
+
+int orc_counts_from_record(const uint8_t *rec, int A, uint32_t Tk, uint32_t *n)
+{
+    if (A < 2 || A > 256 || Tk < 1)
+        return ORC_ERR_ARG;
+    int m = rec[0];
+    if (m >= A)
+        return ORC_ERR_CORRUPT;
+    uint32_t others = 0;
+    int i = 1;
+    for (int s = 0; s < A; s++) {
+        if (s == m)
+            continue;
+        n[s] = rec[i++];
+        others += n[s];
+    }
+    if (others > Tk)
+        return ORC_ERR_CORRUPT;
+    n[m] = Tk - others;
+    return ORC_OK;
+}
+
+/* F with the remainder given to `mode` rather than to the argmax. */
+int orc_cdf_from_counts_mode(const uint32_t *n, int A, uint32_t Tk, int mode,
+                             uint16_t *cdf)
+{
+    if (A < 2 || A > 256 || Tk < 1 || mode < 0 || mode >= A)
+        return ORC_ERR_ARG;
+    uint32_t f[256];
+    uint64_t sum = 0;
+    for (int s = 0; s < A; s++) {
+        f[s] = 1u + (uint32_t)(((uint64_t)n[s] * (ORC_M - (uint32_t)A)) / Tk);
+        sum += f[s];
+    }
+    if (sum > ORC_M)
+        return ORC_ERR_ARG;
+    f[mode] += (uint32_t)(ORC_M - sum);
+    uint32_t acc = 0;
+    for (int s = 0; s < A; s++) {
+        cdf[s] = (uint16_t)acc;
+        acc += f[s];
+    }
+    return acc == ORC_M ? ORC_OK : ORC_ERR_ARG;
+}
+
+/* [CG §2.3(1)-(3), §1.2(3)] format 2: quantise, count per (chunk, kv, layer,
+ * channel), store the counts as records, build each CDF over the layer's own
+ * alphabet and code the streams as in format 1. */
+int orc_compress_v2(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                    int Tc, int64_t layer_stride, const int32_t *bins_k,
+                    const int32_t *bins_v, uint16_t *max1, uint8_t *rec,
+                    uint8_t *packed, uint64_t capacity, uint32_t *len,
+                    uint64_t *off)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1 || Tc > 256)
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
+    uint16_t *rows = (uint16_t *)malloc((size_t)C * 256 * sizeof(uint16_t));
+    int64_t cap1 = 2 * (int64_t)C + 8;
+    uint8_t *buf = (uint8_t *)malloc((size_t)cap1);
+    if (!sym || !rows || !buf) {
+        free(sym), free(rows), free(buf);
+        return ORC_ERR_NOMEM;
+    }
+    int status = orc_quantize(k, v, L, T, C, layer_stride, bins_k, bins_v, sym,
+                              max1);
+    int nch = (T + Tc - 1) / Tc;
+    uint64_t total = 0;
+    for (int kc = 0; kc < nch && status != ORC_ERR_NONFINITE && status != ORC_ERR_ARG; kc++) {
+        int Tk = orc_chunk_tokens(T, Tc, kc);
+        for (int kv = 0; kv < 2; kv++) {
+            const int32_t *bins = kv ? bins_v : bins_k;
+            for (int l = 0; l < L; l++) {
+                int A = orc_alphabet_v2(bins[l]);
+                /* counts -> record and CDF row per channel */
+                for (int c = 0; c < C; c++) {
+                    uint32_t n[256] = {0};
+                    for (int tl = 0; tl < Tk; tl++) {
+                        int64_t t = (int64_t)kc * Tc + tl;
+                        n[sym[(((int64_t)kv * L + l) * T + t) * C + c]]++;
+                    }
+                    uint8_t *r = rec + orc_rec_offset(L, C, bins_k, bins_v, kc, kv, l, c);
+                    int st = orc_record_from_counts(n, A, r);
+                    if (st == ORC_OK)
+                        st = orc_cdf_from_counts_mode(n, A, (uint32_t)Tk, r[0],
+                                                      rows + (int64_t)c * A);
+                    if (st != ORC_OK) {
+                        free(sym), free(rows), free(buf);
+                        return st;
+                    }
+                }
+                /* one stream per token of the chunk */
+                for (int tl = 0; tl < Tk; tl++) {
+                    int64_t t = (int64_t)kc * Tc + tl;
+                    int64_t sid = orc_stream_id(L, T, Tc, kc, kv, l, tl);
+                    const uint8_t *s = sym + (((int64_t)kv * L + l) * T + t) * C;
+                    int64_t n = orc_encode_stream(s, C, rows, A, A, buf, cap1);
+                    if (n < 0) {
+                        free(sym), free(rows), free(buf);
+                        return ORC_ERR_ARG;
+                    }
+                    off[sid] = total;
+                    len[sid] = (uint32_t)n;
+                    if (total + (uint64_t)n <= capacity) {
+                        memcpy(packed + total, buf, (size_t)n);
+                    } else {
+                        if (total < capacity)
+                            memcpy(packed + total, buf, (size_t)(capacity - total));
+                        status = ORC_ERR_CAPACITY;
+                    }
+                    total += (uint64_t)n;
+                }
+            }
+        }
+    }
+    if (status == ORC_OK || status == ORC_ERR_CAPACITY)
+        off[orc_num_streams(L, T)] = total;
+    free(sym), free(rows), free(buf);
+    return status;
+}
+
+int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
+                      const uint32_t *len, const uint8_t *rec,
+                      const uint16_t *max1, int L, int T, int C, int Tc,
+                      const int32_t *bins_k, const int32_t *bins_v,
+                      float *out_k, float *out_v)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1 || Tc > 256)
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
+    uint16_t *rows = (uint16_t *)malloc((size_t)C * 256 * sizeof(uint16_t));
+    if (!sym || !rows) {
+        free(sym), free(rows);
+        return ORC_ERR_NOMEM;
+    }
+    int status = ORC_OK;
+    int nch = (T + Tc - 1) / Tc;
+    for (int kc = 0; kc < nch; kc++) {
+        int Tk = orc_chunk_tokens(T, Tc, kc);
+        for (int kv = 0; kv < 2; kv++) {
+            const int32_t *bins = kv ? bins_v : bins_k;
+            for (int l = 0; l < L; l++) {
+                int A = orc_alphabet_v2(bins[l]);
+                for (int c = 0; c < C; c++) {
+                    const uint8_t *r = rec + orc_rec_offset(L, C, bins_k, bins_v, kc, kv, l, c);
+                    uint32_t n[256];
+                    int st = orc_counts_from_record(r, A, (uint32_t)Tk, n);
+                    if (st == ORC_OK)
+                        st = orc_cdf_from_counts_mode(n, A, (uint32_t)Tk, r[0],
+                                                      rows + (int64_t)c * A);
+                    if (st != ORC_OK) {
+                        free(sym), free(rows);
+                        return st;
+                    }
+                }
+                for (int tl = 0; tl < Tk; tl++) {
+                    int64_t t = (int64_t)kc * Tc + tl;
+                    int64_t sid = orc_stream_id(L, T, Tc, kc, kv, l, tl);
+                    int64_t used = 0;
+                    int st = orc_decode_stream(
+                        packed + off[sid], len[sid], C, rows, A, A,
+                        sym + (((int64_t)kv * L + l) * T + t) * C, &used);
+                    if (st != ORC_OK)
+                        status = st;
+                }
+            }
+        }
+    }
+    if (status == ORC_OK)
+        status = orc_dequantize(sym, max1, L, T, C, bins_k, bins_v, out_k, out_v);
+    free(sym), free(rows);
+    return status;
+}

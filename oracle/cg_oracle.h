@@ -65,6 +65,24 @@
  *
  * D  (dequantise, binary32, no FMA): x^ = ((float)(q - MAX) / (float)MAX)
  *    * (float)max1.
+ *
+ * ---------------------------------------------------------------------------
+ * Format version 2: side information as symbol counts
+ * ---------------------------------------------------------------------------
+ * The page sends, with each chunk, what the decoder needs to rebuild the
+ * chunk's CDFs [CG §2.3(2), §2.4(1)]; format 2 sends the symbol counts the
+ * CDFs are built from instead of the CDF entries. Q, R, P and D are as in
+ * format 1; requires Tc <= 256.
+ *
+ * A2 (alphabet per (kv, l)): A = 2*MAX_l + 1, the symbols Q can produce.
+ * S  (count record per (chunk k, kv, l, channel c), A bytes): byte 0 is the
+ *    mode s* (largest n_s, smallest s on ties); bytes 1..A-1 are n_s for
+ *    every s != s* in increasing s, one byte each (a count other than the
+ *    mode's is at most Tc_k / 2 <= 128). The mode's count is Tc_k minus the
+ *    others. Layout: rec[k] = { K: layer 0 [C][A_0], layer 1 [C][A_1], ...,
+ *    then V likewise }.
+ * F2 (CDF) F over the layer's A symbols, the remainder going to the record's
+ *    mode byte.
  */
 #ifndef CG_ORACLE_H
 #define CG_ORACLE_H
@@ -153,6 +171,36 @@ int orc_decompress(const uint8_t *packed, const uint64_t *off,
                    const uint16_t *max1, int L, int T, int C, int Tc,
                    const int32_t *bins_k, const int32_t *bins_v, float *out_k,
                    float *out_v);
+
+/* ---- format 2 ---------------------------------------------------------- */
+/* A = 2*MAX + 1 for a layer with `bins` bins (specification A2). */
+int orc_alphabet_v2(int bins);
+/* Bytes of all count records / offset of record (k, kv, l, c). */
+int64_t orc_rec_bytes(int L, int T, int C, int Tc, const int32_t *bins_k,
+                      const int32_t *bins_v);
+int64_t orc_rec_offset(int L, int C, const int32_t *bins_k,
+                       const int32_t *bins_v, int k, int kv, int l, int c);
+/* [CG §2.3(2)] counts of A symbols -> the A-byte record (S); error if a
+ * non-mode count exceeds 255. */
+int orc_record_from_counts(const uint32_t *n, int A, uint8_t *rec);
+/* The record -> counts over Tk tokens; error if the mode byte is >= A or the
+ * stored counts exceed Tk. */
+int orc_counts_from_record(const uint8_t *rec, int A, uint32_t Tk, uint32_t *n);
+/* F2: counts and the mode -> A uint16 CDF entries. */
+int orc_cdf_from_counts_mode(const uint32_t *n, int A, uint32_t Tk, int mode,
+                             uint16_t *cdf);
+/* Quantise -> counts -> records and CDFs -> encode (format 2). */
+int orc_compress_v2(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                    int Tc, int64_t layer_stride, const int32_t *bins_k,
+                    const int32_t *bins_v, uint16_t *max1, uint8_t *rec,
+                    uint8_t *packed, uint64_t capacity, uint32_t *len,
+                    uint64_t *off);
+/* Records -> CDFs -> decode -> dequantise (format 2). */
+int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
+                      const uint32_t *len, const uint8_t *rec,
+                      const uint16_t *max1, int L, int T, int C, int Tc,
+                      const int32_t *bins_k, const int32_t *bins_v,
+                      float *out_k, float *out_v);
 
 #ifdef __cplusplus
 }
