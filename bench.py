@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ctx4096")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--format", type=int, choices=[1, 2], default=2,
+                    help="side information: 1 = CDF entries, 2 = symbol-count records")
     ap.add_argument("--piece-chunks", type=int, default=2,
                     help="chunks per piece of the streamed end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -162,14 +164,19 @@ def workload_config(w, extra=None):
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, single thread, on a bounded sample
 # ---------------------------------------------------------------------------
-def oracle_step_time(k, v, w, tokens):
+def oracle_step_time(k, v, w, tokens, fmt=2):
     import oracle
     ks = k[:, :tokens].copy()
     vs = v[:, :tokens].copy()
     t0 = time.perf_counter()
-    r = oracle.compress(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v)
-    oracle.decompress(r["packed"], r["off"], r["len"], r["cdf"], r["max1"], w.L, tokens, w.C,
-                      w.chunk_tokens, w.bins_k, w.bins_v)
+    if fmt == 2:
+        r = oracle.compress_v2(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v)
+        oracle.decompress_v2(r["packed"], r["off"], r["len"], r["rec"], r["max1"], w.L, tokens, w.C,
+                             w.chunk_tokens, w.bins_k, w.bins_v)
+    else:
+        r = oracle.compress(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v)
+        oracle.decompress(r["packed"], r["off"], r["len"], r["cdf"], r["max1"], w.L, tokens, w.C,
+                          w.chunk_tokens, w.bins_k, w.bins_v)
     dt = time.perf_counter() - t0
     return dt, ks.nbytes + vs.nbytes
 
@@ -185,11 +192,11 @@ def run_reference(args):
     tokens = min(w.T, w.chunk_tokens)
     k, v = synth.generate(w, T=tokens)
     for _ in range(args.warmup):
-        oracle_step_time(k, v, w, tokens)
+        oracle_step_time(k, v, w, tokens, args.format)
     times = []
     nbytes = 0
     for _ in range(args.steps):
-        dt, nbytes = oracle_step_time(k, v, w, tokens)
+        dt, nbytes = oracle_step_time(k, v, w, tokens, args.format)
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = nbytes / (ms * 1e-3) / 1e9
@@ -198,7 +205,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w, {"sample": sample}),
+        "config": workload_config(w, {"sample": sample, "format": args.format}),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -235,7 +242,7 @@ def run_ours(args):
     v_pin.copy_(v)
     k_h, v_h = k_pin.numpy(), v_pin.numpy()
     stream = torch.cuda.current_stream()
-    cd = codec.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens)
+    cd = codec.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens, fmt=args.format)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
 
     def step():
@@ -295,11 +302,13 @@ def run_ours(args):
     comp_kernel_ms = time_call(lambda: cd.compress(k, v))
     dec_kernel_ms = time_call(cd.decompress)
     n_el = 2 * w.L * w.T * w.C
-    cdf_bytes = 2 * cd.cdf_elems
+    cdf_bytes = 2 * cd.cdf_elems if args.format == 1 else cd.rec_bytes  # side information
     side = cdf_bytes + 2 * 2 * w.L * w.T + 4 * cd.nstreams + 8 * (cd.nstreams + 1)
     dec_alg_bytes = total + side + 4 * n_el
     comp_alg_bytes = fp16_bytes + total + side
     A = max(max(w.bins_k), max(w.bins_v))
+    if args.format == 2:  # the largest layer alphabet, 2 * MAX + 1
+        A = max(2 * (b // 2 - 1) + 1 for b in list(w.bins_k) + list(w.bins_v))
     P = 1 << (A - 1).bit_length()
     props = torch.cuda.get_device_properties(local)
     max_mhz = clocks.get("sm_max_mhz") or 2070.0
@@ -332,7 +341,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": workload_config(w, {"parallelism": f"chunk-sharded x{world}" if world > 1 else "1 GPU"}),
+        "config": workload_config(w, {"parallelism": f"chunk-sharded x{world}" if world > 1 else "1 GPU",
+                                      "format": args.format}),
         "compress_gbs": comp_gbs, "decompress_gbs": dec_gbs,
         "compress_ms": statistics.mean(comp_ms), "decompress_ms": statistics.mean(dec_ms),
         "compress_frac_of_hbm": {"fp16_in": comp_gbs / hbm,
@@ -349,11 +359,11 @@ def run_ours(args):
     if not args.no_e2e:
         result["e2e"] = e2e(args, w, cd, k_pin, v_pin, fp16_bytes)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens))
+        cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens), args.format)
         reps = max(1, int(10.0 / max(cpu_dt, 1e-3)))
         times = [cpu_dt]
         for _ in range(min(reps, 20) - 1):
-            times.append(oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens))[0])
+            times.append(oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens), args.format)[0])
         cpu_gbs = cpu_bytes / statistics.mean(times) / 1e9
         result["cpu_baseline"] = {
             "value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -375,7 +385,7 @@ def e2e(args, w, cd, k_pin, v_pin, fp16_bytes):
     the decompressed output is checked once against the single-call result."""
     import torch
     from kv_cache_compression_cg_gb300.stream import StreamingCodec
-    sc = StreamingCodec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens,
+    sc = StreamingCodec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens, fmt=args.format,
                         piece_chunks=args.piece_chunks)
     times = []
     pieces = outs = None

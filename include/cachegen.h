@@ -222,6 +222,51 @@ cg_status cg_compress_chunk_noalloc(const uint16_t *k, const uint16_t *v,
                                     uint64_t *off, int32_t *status,
                                     cudaStream_t stream);
 
+/* ---- format 2: side information as symbol counts ------------------------
+ * The page sends, with each chunk, what the decoder needs to rebuild the
+ * chunk's CDFs [CG §2.3(2), §2.4(1)]. Format 2 sends the symbol counts the
+ * CDFs are built from instead of CDF entries, over each layer's own alphabet:
+ *
+ * A2 A = 2*MAX_l + 1 per (kv, layer): the symbols Q can produce.
+ * S  count record per (chunk k, kv, l, channel c), A bytes: byte 0 is the
+ *    mode s* (largest count, smallest s on ties), bytes 1..A-1 the counts of
+ *    the other symbols in increasing s, one byte each (at most Tc_k / 2).
+ *    Layout: rec[k] = { K: layer 0 [C][A_0], layer 1 [C][A_1], ..., then V }.
+ * F2 CDF = F over the layer's A symbols, the remainder on the record's mode.
+ * Q, R, P and D are format 1's. Requires chunk_tokens <= 256.
+ */
+
+/* Bytes of all count records, or 0 for an invalid shape, invalid bins or
+ * chunk_tokens > 256. */
+uint64_t cg_record_bytes(const cg_shape *shape, const int32_t *bins_k,
+                         const int32_t *bins_v);
+
+/* cg_compress_chunk in format 2: max1 as in format 1, rec gets the count
+ * records (cg_record_bytes bytes), packed/len/off the streams coded with the
+ * per-layer CDFs. Workspace: cg_compress_workspace_bytes. Runs on the fused
+ * path only: every bins <= 33, C % 8 == 0, k and v 16-byte aligned with
+ * layer_stride % 8 == 0; other arguments give CG_ERR_INVALID_ARG. */
+cg_status cg_compress_chunk_v2(const uint16_t *k, const uint16_t *v,
+                               const cg_shape *shape, const int32_t *bins_k,
+                               const int32_t *bins_v, uint16_t *max1,
+                               uint8_t *rec, uint8_t *packed,
+                               uint64_t capacity, uint32_t *len,
+                               uint64_t *off, void *workspace,
+                               uint64_t workspace_bytes, int32_t *status,
+                               cudaStream_t stream);
+
+/* cg_decompress_chunk in format 2: the CDFs come from the count records; a
+ * record whose mode byte lies outside the alphabet or whose counts exceed the
+ * chunk's tokens sets CG_FLAG_CORRUPT (its channel then decodes with an
+ * all-ones count). */
+cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes,
+                                 const uint64_t *off, const uint32_t *len,
+                                 const uint8_t *rec, const uint16_t *max1,
+                                 const cg_shape *shape, const int32_t *bins_k,
+                                 const int32_t *bins_v, float *out_k,
+                                 float *out_v, int32_t *status,
+                                 cudaStream_t stream);
+
 /* Library version string ("cachegen-gb300 <format> <build>"). */
 const char *cg_version(void);
 

@@ -50,6 +50,10 @@ SIGNATURES = {
                                  _p, _p]),
     "cg_decompress_chunk": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, _p, _p, _p, _p]),
     "cg_compress_chunk_noalloc": (_i32, [_p, _p, _SHAPE, _p, _p, _p, _p, _p, _u64, _p, _p, _p, _p]),
+    "cg_record_bytes": (_u64, [_SHAPE, _p, _p]),
+    "cg_compress_chunk_v2": (_i32, [_p, _p, _SHAPE, _p, _p, _p, _p, _p, _u64, _p, _p, _p, _u64,
+                                    _p, _p]),
+    "cg_decompress_chunk_v2": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, _p, _p, _p, _p]),
     "cg_version": (C.c_char_p, []),
 }
 

@@ -72,6 +72,8 @@ class Compressed:
     len: torch.Tensor       # int32 [nstreams] (uint32)
     off: torch.Tensor       # int64 [nstreams + 1]
     status: torch.Tensor    # int32 [1]
+    fmt: int = 1            # 1: CDF entries in `cdf`; 2: count records in `rec`
+    rec: torch.Tensor | None = None  # uint8 [record bytes] (format 2)
 
     @property
     def shape(self) -> capi.cg_shape:
@@ -89,7 +91,10 @@ class Codec:
     """
 
     def __init__(self, L: int, T: int, C_: int, bins_k, bins_v=None, chunk_tokens: int = 256,
-                 capacity: int | None = None, device: str | torch.device = "cuda"):
+                 capacity: int | None = None, device: str | torch.device = "cuda", fmt: int = 1):
+        if fmt not in (1, 2):
+            raise ValueError("fmt must be 1 (CDF entries) or 2 (count records)")
+        self.fmt = fmt
         self.L, self.T, self.C, self.chunk_tokens = L, T, C_, chunk_tokens
         self.bins_k = _bins(bins_k, L)
         self.bins_v = _bins(bins_k if bins_v is None else bins_v, L)
@@ -97,6 +102,9 @@ class Codec:
         shp = make_shape(L, T, C_, chunk_tokens)
         self.nstreams = int(lib.cg_num_streams(C.byref(shp)))
         self.cdf_elems = int(lib.cg_cdf_elems(C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v)))
+        self.rec_bytes = int(lib.cg_record_bytes(C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v)))
+        if fmt == 2 and self.rec_bytes == 0 and T > 0:
+            raise ValueError("format 2 needs chunk_tokens <= 256")
         self.max_bytes = int(lib.cg_max_compressed_bytes(C.byref(shp)))
         if self.nstreams == 0 and T > 0 or self.cdf_elems == 0 and T > 0:
             raise ValueError("invalid shape or bins for the codec")
@@ -107,11 +115,12 @@ class Codec:
         self.out = Compressed(
             L, T, C_, chunk_tokens, self.bins_k, self.bins_v,
             max1=torch.empty((2, L, T), dtype=torch.int16, device=dev),
-            cdf=torch.empty(max(self.cdf_elems, 1), dtype=torch.int16, device=dev),
+            cdf=torch.empty(max(self.cdf_elems if fmt == 1 else 1, 1), dtype=torch.int16, device=dev),
             packed=torch.empty(max(self.capacity, 16), dtype=torch.uint8, device=dev),
             len=torch.empty(max(self.nstreams, 1), dtype=torch.int32, device=dev),
             off=torch.empty(self.nstreams + 1, dtype=torch.int64, device=dev),
-            status=torch.zeros(1, dtype=torch.int32, device=dev))
+            status=torch.zeros(1, dtype=torch.int32, device=dev), fmt=fmt,
+            rec=torch.empty(max(self.rec_bytes, 1), dtype=torch.uint8, device=dev) if fmt == 2 else None)
         self.out_k = torch.empty((L, T, C_), dtype=torch.float32, device=dev)
         self.out_v = torch.empty((L, T, C_), dtype=torch.float32, device=dev)
         self.dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -121,6 +130,13 @@ class Codec:
         if (shp.L, shp.T, shp.C) != (self.L, self.T, self.C):
             raise ValueError("K/V shape differs from the codec's")
         o = self.out
+        if self.fmt == 2:
+            capi.check(capi.load().cg_compress_chunk_v2(
+                _ptr(k), _ptr(v), C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v),
+                _ptr(o.max1), _ptr(o.rec), _ptr(o.packed), self.capacity, _ptr(o.len), _ptr(o.off),
+                _ptr(self.workspace), self.ws_bytes, _ptr(o.status), _stream(stream)),
+                "cg_compress_chunk_v2")
+            return o
         capi.check(capi.load().cg_compress_chunk(
             _ptr(k), _ptr(v), C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v),
             _ptr(o.max1), _ptr(o.cdf), _ptr(o.packed), self.capacity, _ptr(o.len), _ptr(o.off),
@@ -131,6 +147,12 @@ class Codec:
     def decompress(self, c: Compressed | None = None, stream=None):
         c = self.out if c is None else c
         shp = make_shape(c.L, c.T, c.C, c.chunk_tokens)
+        if c.fmt == 2:
+            capi.check(capi.load().cg_decompress_chunk_v2(
+                _ptr(c.packed), c.packed.numel(), _ptr(c.off), _ptr(c.len), _ptr(c.rec), _ptr(c.max1),
+                C.byref(shp), _np_ptr(c.bins_k), _np_ptr(c.bins_v), _ptr(self.out_k), _ptr(self.out_v),
+                _ptr(self.dstatus), _stream(stream)), "cg_decompress_chunk_v2")
+            return self.out_k, self.out_v
         capi.check(capi.load().cg_decompress_chunk(
             _ptr(c.packed), c.packed.numel(), _ptr(c.off), _ptr(c.len), _ptr(c.cdf), _ptr(c.max1),
             C.byref(shp), _np_ptr(c.bins_k), _np_ptr(c.bins_v), _ptr(self.out_k), _ptr(self.out_v),

@@ -100,6 +100,21 @@ Workspace carve(void *ws, const Dims &d, bool with_sym) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Format 2: layer alphabet 2*MAX + 1, records C * sum_l A_l per tensor and chunk.
+uint64_t record_bytes(const Dims &d, const MaxTab &mt) {
+    uint64_t per = 0;
+    for (int kv = 0; kv < 2; kv++)
+        for (int l = 0; l < d.L; l++) per += 2ull * mt.v[kv][l] + 1;
+    return (uint64_t)d.nch * (uint64_t)d.C * per;
+}
+
+int max_alphabet_v2(const Dims &d, const MaxTab &mt) {
+    int a = 0;
+    for (int kv = 0; kv < 2; kv++)
+        for (int l = 0; l < d.L; l++) a = 2 * mt.v[kv][l] + 1 > a ? 2 * mt.v[kv][l] + 1 : a;
+    return a;
+}
+
 cg_status launched(cudaError_t e) { return e == cudaSuccess ? CG_OK : CG_ERR_CUDA; }
 
 // Empty token range: only off[0] = 0 has to be written.
@@ -145,7 +160,7 @@ uint64_t cg_compress_workspace_bytes(const cg_shape *shape) {
     return encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d);
 }
 
-const char *cg_version(void) { return "cachegen-gb300 format-1 sm_103a"; }
+const char *cg_version(void) { return "cachegen-gb300 formats-1,2 sm_103a"; }
 
 cg_status cg_quantize(const uint16_t *k, const uint16_t *v, const cg_shape *shape,
                       const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym, uint16_t *max1,
@@ -235,7 +250,7 @@ cg_status cg_compress_chunk(const uint16_t *k, const uint16_t *v, const cg_shape
     if (workspace_bytes < encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d)) return CG_ERR_WORKSPACE;
     Workspace w = carve(workspace, d, true);
     if (cg::compress_fused_applies(d, k, v))
-        return launched(cg::launch_compress_fused(k, v, d, mt, max1, cdf, w.stage, len, off, packed,
+        return launched(cg::launch_compress_fused(k, v, d, mt, max1, cdf, nullptr, w.stage, len, off, packed,
                                                   capacity, w.state, status, stream));
     if (cg::launch_quantize(k, v, d, mt, w.sym, max1, status, stream) != cudaSuccess) return CG_ERR_CUDA;
     if (cg::launch_code_slices(w.sym, nullptr, cdf, w.stage, len, d, 2, status, stream) != cudaSuccess)
@@ -258,6 +273,53 @@ cg_status cg_decompress_chunk(const uint8_t *packed, uint64_t packed_bytes, cons
         return CG_ERR_INVALID_ARG;
     return launched(cg::launch_decode(packed, packed_bytes, off, len, cdf, max1, d, mt, 1, nullptr,
                                       out_k, out_v, status, stream));
+}
+
+uint64_t cg_record_bytes(const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return 0;
+    return record_bytes(d, mt);
+}
+
+cg_status cg_compress_chunk_v2(const uint16_t *k, const uint16_t *v, const cg_shape *shape,
+                               const int32_t *bins_k, const int32_t *bins_v, uint16_t *max1, uint8_t *rec,
+                               uint8_t *packed, uint64_t capacity, uint32_t *len, uint64_t *off,
+                               void *workspace, uint64_t workspace_bytes, int32_t *status,
+                               cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return CG_ERR_INVALID_ARG;
+    if (!off) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return empty_offsets(off, stream);
+    if (!k || !v || !max1 || !rec || !len || !workspace || (!packed && capacity > 0)) return CG_ERR_INVALID_ARG;
+    if (!aligned(k, 2) || !aligned(v, 2) || !aligned(max1, 2) || !aligned(len, 4) || !aligned(off, 8) ||
+        !aligned(workspace, kAlign))
+        return CG_ERR_INVALID_ARG;
+    if (workspace_bytes < encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d)) return CG_ERR_WORKSPACE;
+    // the fused kernel's limits, with format 2's alphabet
+    Dims d2 = d;
+    d2.A[0] = d2.A[1] = max_alphabet_v2(d, mt);
+    if (!cg::compress_fused_applies(d2, k, v)) return CG_ERR_INVALID_ARG;
+    Workspace w = carve(workspace, d, true);
+    return launched(cg::launch_compress_fused(k, v, d, mt, max1, nullptr, rec, w.stage, len, off, packed, capacity,
+                                              w.state, status, stream));
+}
+
+cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
+                                 const uint32_t *len, const uint8_t *rec, const uint16_t *max1,
+                                 const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v,
+                                 float *out_k, float *out_v, int32_t *status, cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    if (!packed || !off || !len || !rec || !max1 || !out_k || !out_v) return CG_ERR_INVALID_ARG;
+    if (!aligned(packed, 4) || !aligned(off, 8) || !aligned(len, 4) || !aligned(max1, 2) ||
+        !aligned(out_k, 16) || !aligned(out_v, 16))
+        return CG_ERR_INVALID_ARG;
+    return launched(cg::launch_decode_pipe(packed, packed_bytes, off, len, nullptr, rec, max1, d, mt, 1, nullptr,
+                                           out_k, out_v, status, stream));
 }
 
 }  // extern "C"

@@ -43,6 +43,42 @@ __host__ __device__ inline long long cdf_slice_offset(const Dims &d, int k, int 
     return per_chunk * k + tensor + (long long)l * d.C * d.A[kv];
 }
 
+// Format 2: byte offset of the count records of slice (k, kv, l). Records of
+// a chunk are K layer 0 [C][A_0], layer 1 [C][A_1], ..., then V, with
+// A_j = 2 * MAX_j + 1. Every thread of the CTA calls this (block reduction
+// over the layers; two barriers); every thread gets the offset.
+__device__ __forceinline__ long long record_slice_offset(const Dims &d, const MaxTab &mt, int k, int kv, int l) {
+    __shared__ unsigned long long red[3 * 32];
+    unsigned long long tk = 0, tv = 0, pre = 0;
+    for (int j = threadIdx.x; j < d.L; j += blockDim.x) {
+        const unsigned long long ak = 2ull * mt.v[0][j] + 1, av = 2ull * mt.v[1][j] + 1;
+        tk += ak;
+        tv += av;
+        if (j < l) pre += kv ? av : ak;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        tk += __shfl_xor_sync(0xFFFFFFFFu, tk, o);
+        tv += __shfl_xor_sync(0xFFFFFFFFu, tv, o);
+        pre += __shfl_xor_sync(0xFFFFFFFFu, pre, o);
+    }
+    const int warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        red[3 * warp] = tk;
+        red[3 * warp + 1] = tv;
+        red[3 * warp + 2] = pre;
+    }
+    __syncthreads();
+    tk = tv = pre = 0;
+    for (int w = 0; w < nw; w++) {
+        tk += red[3 * w];
+        tv += red[3 * w + 1];
+        pre += red[3 * w + 2];
+    }
+    __syncthreads();
+    return (long long)d.C * ((long long)k * (long long)(tk + tv) + (kv ? (long long)tk : 0LL) + (long long)pre);
+}
+
 // Symbols [2][L][T][C] and max1 [2][L][T].
 __host__ __device__ inline long long group_index(const Dims &d, int kv, int l, long long t) {
     return ((long long)kv * d.L + l) * d.T + t;
@@ -97,8 +133,10 @@ bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v)
 // Writes max1, cdf, len, off (incl. off[nstreams]) and packed; `state` holds
 // 2 + 2 * nslices uint64 words (two tickets, a look-back slot and a byte total
 // per slice), set up by the launch itself.
+// cdf != nullptr: format 1 (CDF entries out); otherwise rec gets format 2's
+// count records.
 cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d,
-                                  const MaxTab &mt, uint16_t *max1, uint16_t *cdf,
+                                  const MaxTab &mt, uint16_t *max1, uint16_t *cdf, uint8_t *rec,
                                   uint8_t *stage, uint32_t *len, uint64_t *off,
                                   uint8_t *packed, uint64_t capacity,
                                   unsigned long long *state, int32_t *status,
@@ -111,6 +149,15 @@ cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes,
                           const Dims &d, const MaxTab &mt, int mode, uint8_t *sym,
                           float *out_k, float *out_v, int32_t *status,
                           cudaStream_t s);
+
+// Chunks of up to 256 tokens; rec != nullptr selects format 2 (CDF rows from
+// the count records, cdf unused).
+cudaError_t launch_decode_pipe(const uint8_t *packed, uint64_t packed_bytes,
+                               const uint64_t *off, const uint32_t *len,
+                               const uint16_t *cdf, const uint8_t *rec,
+                               const uint16_t *max1, const Dims &d, const MaxTab &mt,
+                               int mode, uint8_t *sym, float *out_k, float *out_v,
+                               int32_t *status, cudaStream_t s);
 
 // Any chunk size up to CG_MAX_CHUNK_TOKENS (used by launch_decode beyond 256).
 cudaError_t launch_decode_generic(const uint8_t *packed, uint64_t packed_bytes,

@@ -198,9 +198,12 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
     }
 }
 
+// V2 (format 2): the alphabet is the layer's 2*MAX + 1 symbols and the side
+// output is the count records (uint8) instead of the CDF entries (uint16).
+template <bool V2>
 __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, Dims d, MaxTab mt,
-    int box_rows, uint16_t *__restrict__ max1_out, uint16_t *__restrict__ cdf_out, uint8_t *__restrict__ stage,
+    int box_rows, uint16_t *__restrict__ max1_out, void *__restrict__ side_out, uint8_t *__restrict__ stage,
     uint32_t *__restrict__ len, unsigned long long *state, int32_t *status) {
     __shared__ __align__(1024) unsigned char s_union[kUnionBytes];
     __shared__ unsigned long long s_scan[kNW + 4];
@@ -233,14 +236,14 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     const int ticket = s_ticket;
     int k, kv, l;
     slice_coords(d, ticket, k, kv, l);
-    const int A = d.A[kv];
     const int Tk = chunk_tokens(d, k);
     const int MAX = mt.v[kv][l];
+    const int A = V2 ? 2 * MAX + 1 : d.A[kv];
     const CUtensorMap *tm = kv ? &tmv : &tmk;
     const int t0 = k * d.Tc;
     const int nwin = (d.C + kW - 1) / kW;
     const uint32_t box_bytes = (uint32_t)box_rows * (kW * 2);
-    const long long cdf_base = cdf_slice_offset(d, k, kv, l);
+    const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
     const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk;
     const long long sid = sid0 + tid;
     uint8_t *stream = stage_stream(stage, tid < Tk ? sid : sid0, d);
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
             // is entirely inside or entirely outside the window
             if (c < Wc) {
                 uint32_t fj[kSP], pre[kSP];
-                uint32_t sum = 0, key = 0;
+                uint32_t sum = 0, key = 0, nlo = 0, nhi = 0;  // counts, one byte each (capped)
 #pragma unroll
                 for (int j = 0; j < kSP; j++) {
                     const int s = kSP * p + j;
@@ -357,6 +360,12 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
                         *cp = 0;
                         fv = s_ftab[n];
                         key = max(key, (n << 8) | (255u - (uint32_t)s));  // largest n, then smallest s
+                        if (V2) {
+                            if (j < 4)
+                                nlo |= min(n, 255u) << (8 * j);
+                            else
+                                nhi |= min(n, 255u) << (8 * (j - 4));
+                        }
                     }
                     pre[j] = sum;
                     sum += fv;
@@ -374,15 +383,31 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
                 const uint32_t best = 255u - (key & 255u);
                 const uint32_t extra = kTotal - total;
                 uint2 *row = cdfw + c * kAS;
-                uint16_t *g = cdf_out + cdf_base + (long long)(c0 + c) * A;
+                if (V2) {
+                    // count record: the mode, then the other symbols' counts
+                    uint8_t *g = static_cast<uint8_t *>(side_out) + side_base + (long long)(c0 + c) * A;
+                    if (p == 0) g[0] = (uint8_t)best;
 #pragma unroll
-                for (int j = 0; j < kSP; j++) {
-                    const uint32_t s = (uint32_t)(kSP * p + j);
-                    if ((int)s < A) {
-                        const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
-                        const uint32_t f = fj[j] + (s == best ? extra : 0u);
-                        row[s] = make_uint2(lo, f);
-                        g[s] = (uint16_t)lo;
+                    for (int j = 0; j < kSP; j++) {
+                        const uint32_t s = (uint32_t)(kSP * p + j);
+                        if ((int)s < A) {
+                            const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
+                            const uint32_t f = fj[j] + (s == best ? extra : 0u);
+                            row[s] = make_uint2(lo, f);
+                            if (s != best) g[s + (s < best ? 1u : 0u)] = (uint8_t)((j < 4 ? nlo >> (8 * j) : nhi >> (8 * (j - 4))) & 0xFFu);
+                        }
+                    }
+                } else {
+                    uint16_t *g = static_cast<uint16_t *>(side_out) + side_base + (long long)(c0 + c) * A;
+#pragma unroll
+                    for (int j = 0; j < kSP; j++) {
+                        const uint32_t s = (uint32_t)(kSP * p + j);
+                        if ((int)s < A) {
+                            const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
+                            const uint32_t f = fj[j] + (s == best ? extra : 0u);
+                            row[s] = make_uint2(lo, f);
+                            g[s] = (uint16_t)lo;
+                        }
                     }
                 }
             }
@@ -601,22 +626,24 @@ bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v)
 }
 
 cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d, const MaxTab &mt,
-                                  uint16_t *max1, uint16_t *cdf, uint8_t *stage, uint32_t *len,
+                                  uint16_t *max1, uint16_t *cdf, uint8_t *rec, uint8_t *stage, uint32_t *len,
                                   uint64_t *off, uint8_t *packed, uint64_t capacity,
                                   unsigned long long *state, int32_t *status, cudaStream_t s) {
     const int box_rows = d.Tc < d.T ? d.Tc : d.T;
     CUtensorMap tmk, tmv;
     if (!make_map(&tmk, k, d, box_rows) || !make_map(&tmv, v, d, box_rows)) return cudaErrorNotSupported;
     const int dyn = 128 + box_rows * kW * 2;
-    cudaError_t err = cudaFuncSetAttribute(k_compress_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    const bool v2 = cdf == nullptr;
+    auto kern = v2 ? k_compress_tma<true> : k_compress_tma<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(k_compress_tma, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     const long long nslices = 2LL * d.L * d.nch;
     k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
-    k_compress_tma<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, cdf, stage, len, state,
-                                                       status);
+    kern<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1,
+                                              v2 ? static_cast<void *>(rec) : static_cast<void *>(cdf), stage, len,
+                                              state, status);
     k_pack<<<(unsigned)nslices, kNT, 0, s>>>(d, stage, len, off, packed, capacity, state, status);
     return cudaGetLastError();
 }

@@ -137,17 +137,18 @@ __device__ __forceinline__ void search_from(uint32_t &addr, uint32_t r, uint32_t
 
 // One symbol from the row of its channel: `cum` is the shared address of the
 // uint16 cumulative row, its frequencies sit frq_off bytes further; needs
-// nb >= 16. Returns the entry's byte offset in the row (2s). Entries at or
+// nb >= 16. Searches the first PS entries of the row (PS >= A). Returns the
+// entry's byte offset in the row (2s). Entries at or
 // past A hold cum = 65535: a valid stream's code never passes symbol A - 1's
 // upper bound, and with CLAMP (A < P) the clamp to A - 1 gives both a valid
 // stream whose code reaches r * 65535 and a corrupt stream the decoder rule's
 // answer (largest s < A with r*cum[s] <= code). With A == P no entry is
 // padding and the search cannot pass A - 1.
-template <int P, bool CLAMP>
+template <int PS, bool CLAMP>
 __device__ __forceinline__ uint32_t decode_symbol(Stream &s, uint32_t cum, uint32_t frq_off, uint32_t amax2) {
     const uint32_t r = s.range >> 16;
     uint32_t addr = cum;
-    search_from<P / 2>(addr, r, s.code);
+    search_from<PS / 2>(addr, r, s.code);
     if (CLAMP) addr = min(addr, cum + amax2);
     uint32_t lo, f;
     asm("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(addr));
@@ -171,7 +172,8 @@ struct PipeSmem {
     static constexpr size_t frq = cum + 2ull * W * P * 2;                   // [2][W][P] uint16
     static constexpr size_t tile = (frq + 2ull * W * P * 2 + 15) & ~15ull;  // [kThreads*TS]
     static constexpr size_t m1 = tile + 1ull * kThreads * TS;               // float[kThreads]
-    static constexpr size_t bytes = m1 + kThreads * 4;
+    static constexpr size_t recs = m1 + kThreads * 4;                       // format 2: [2][W*P] records
+    static constexpr size_t bytes = recs + 2ull * W * P;
 };
 
 // Stage the CDF rows of window [c0, c0 + Wc) (helper warp): cum[c][j] =
@@ -215,6 +217,90 @@ __device__ __forceinline__ void stage_rows(uint16_t *cum, uint16_t *frq, const u
         cum[i] = (uint16_t)lo;
         frq[i] = (uint16_t)f;
     }
+}
+
+// Format 2, step 1 (helper warp): the count records of one window (nb
+// contiguous bytes) into shared memory with coalesced loads.
+__device__ __forceinline__ void copy_records(uint8_t *srec, const uint8_t *recw, int nb, int lane) {
+    if ((reinterpret_cast<uintptr_t>(recw) & 3) == 0) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(recw);
+        uint32_t *sw = reinterpret_cast<uint32_t *>(srec);
+        for (int i = lane; i < nb / 4; i += 32) sw[i] = __ldg(w + i);
+        for (int i = (nb & ~3) + lane; i < nb; i += 32) srec[i] = __ldg(recw + i);
+    } else {
+        for (int i = lane; i < nb; i += 32) srec[i] = __ldg(recw + i);
+    }
+}
+
+// Format 2, step 2 (the 256 decoder threads): the window's CDF rows rebuilt
+// from its records in shared memory. Four threads share a channel (t >> 2),
+// each owning P / 4 consecutive symbols: counts -> f(n) through the slice's
+// table, four-lane sums of the counts, a four-lane scan of f, the remainder
+// to the record's mode (which shifts the running sum of the symbols after
+// it); entries at or past A hold 65535 / 0. A record whose mode byte is
+// outside the alphabet or whose counts exceed Tk is corrupt: its channel gets
+// every token on the mode (symbol 0 when the mode byte is invalid) and the
+// function returns true. Channels at or past Wc (a partial last window) are
+// built from unused bytes into rows no window reads, and not checked.
+template <int P>
+__device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, const uint8_t *srec, int A, uint32_t Tk,
+                                              int W, int Wc, int t, const uint16_t *ftab) {
+    constexpr int SP = P / 4;              // symbols per thread
+    constexpr int NR = SP <= 8 ? SP : 1;   // counts held in registers (one read pass) up to 8
+    constexpr int UNR = SP <= 8 ? SP : 1;  // wider rows: plain loops (registers, code size)
+    const int c = t >> 2, p = t & 3;
+    if (c >= W) return false;  // whole four-lane groups
+    const int j0 = p * SP;
+    const uint8_t *r = srec + c * A;
+    int mode = r[0];
+    auto count_at = [&](int j) -> uint32_t {  // stored count of symbol j != mode
+        return (j < A && j != mode) ? (uint32_t)r[j < mode ? j + 1 : j] : 0u;
+    };
+    uint32_t n[NR];
+    uint32_t others = 0;
+#pragma unroll UNR
+    for (int jj = 0; jj < SP; jj++) {
+        const uint32_t x = count_at(j0 + jj);
+        if (SP <= 8) n[jj < NR ? jj : 0] = x;
+        others += x;
+    }
+    others += __shfl_xor_sync(0xFFFFFFFFu, others, 1);
+    others += __shfl_xor_sync(0xFFFFFFFFu, others, 2);
+    const bool ok = mode < A && others <= Tk;
+    if (!ok) mode = mode < A ? mode : 0;
+    const uint32_t nmode = ok ? Tk - others : Tk;
+    auto f_at = [&](int jj) -> uint32_t {
+        const int j = j0 + jj;
+        if (j >= A) return 0u;
+        const uint32_t stored = SP <= 8 ? n[jj < NR ? jj : 0] : count_at(j);
+        return ftab[j == mode ? nmode : (ok ? stored : 0u)];
+    };
+    uint32_t fl = 0;  // this thread's sum of f (without the remainder)
+#pragma unroll UNR
+    for (int jj = 0; jj < SP; jj++) fl += f_at(jj);
+    uint32_t incl = fl;
+    uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
+    if (p >= 1) incl += v;
+    v = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
+    if (p >= 2) incl += v;
+    const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
+    uint32_t acc = incl - fl;
+    uint16_t *cr = cum + c * P;
+    uint16_t *fr = frq + c * P;
+#pragma unroll UNR
+    for (int jj = 0; jj < SP; jj++) {
+        const int j = j0 + jj;
+        const uint32_t f = f_at(jj);
+        if (j < A) {
+            cr[j] = (uint16_t)(acc + (j > mode ? rem : 0u));
+            fr[j] = (uint16_t)(f + (j == mode ? rem : 0u));
+        } else {
+            cr[j] = 65535u;
+            fr[j] = 0;
+        }
+        acc += f;
+    }
+    return !ok && c < Wc;
 }
 
 __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
@@ -278,8 +364,9 @@ __device__ __forceinline__ void write_window(const uint8_t *tile, const float *u
     }
 }
 
-// Decode this thread's Wc symbols of one window into its tile row.
-template <int P, bool CLAMP, bool TAIL>
+// Decode this thread's Wc symbols of one window into its tile row: rows are P
+// entries apart, the search covers the first PS (the alphabet fits in PS).
+template <int P, int PS, bool CLAMP, bool TAIL>
 __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t fo, uint32_t amax2, uint8_t *my,
                                               int Wc) {
     constexpr int W = DecodeCfg<P>::W;
@@ -289,11 +376,11 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
         for (int c = 0; c < W; c += 4) {
             const uint32_t rc = cb + 2 * P * c;
             refill<TAIL>(s);
-            const uint32_t e0 = decode_symbol<P, CLAMP>(s, rc, fo, amax2);
-            const uint32_t e1 = decode_symbol<P, CLAMP>(s, rc + 2 * P, fo, amax2);
+            const uint32_t e0 = decode_symbol<PS, CLAMP>(s, rc, fo, amax2);
+            const uint32_t e1 = decode_symbol<PS, CLAMP>(s, rc + 2 * P, fo, amax2);
             refill<TAIL>(s);
-            const uint32_t e2 = decode_symbol<P, CLAMP>(s, rc + 4 * P, fo, amax2);
-            const uint32_t e3 = decode_symbol<P, CLAMP>(s, rc + 6 * P, fo, amax2);
+            const uint32_t e2 = decode_symbol<PS, CLAMP>(s, rc + 4 * P, fo, amax2);
+            const uint32_t e3 = decode_symbol<PS, CLAMP>(s, rc + 6 * P, fo, amax2);
             // e = 2s: store 4s (SH == 2) or s
             const uint32_t w = SH == 2 ? 2u * (e0 | (e1 << 8) | (e2 << 16) | (e3 << 24))
                                        : (e0 >> 1) | ((e1 >> 1) << 8) | ((e2 >> 1) << 16) | ((e3 >> 1) << 24);
@@ -303,7 +390,7 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
 #pragma unroll 1
         for (int c = 0; c < Wc; c++) {
             refill<TAIL>(s);
-            const uint32_t e = decode_symbol<P, CLAMP>(s, cb + 2 * P * c, fo, amax2);
+            const uint32_t e = decode_symbol<PS, CLAMP>(s, cb + 2 * P * c, fo, amax2);
             my[c] = (uint8_t)(SH == 2 ? 2u * e : e >> 1);
         }
     }
@@ -312,10 +399,10 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
 // CTA = kThreads decoder threads (one per token stream) + one helper warp.
 // Iteration i: decoders decode window i with rows[i & 1] and write it out
 // while the helper stages rows[(i + 1) & 1]; one barrier per window.
-template <int P, int MODE>
+template <int P, int MODE, bool V2>
 __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     const uint8_t *__restrict__ packed, long long packed_bytes, const uint64_t *__restrict__ off,
-    const uint32_t *__restrict__ len, const uint16_t *__restrict__ cdf,
+    const uint32_t *__restrict__ len, const uint16_t *__restrict__ cdf, const uint8_t *__restrict__ rec,
     const uint16_t *__restrict__ max1, Dims d, MaxTab mt, uint8_t *__restrict__ sym,
     float *__restrict__ out_k, float *__restrict__ out_v, int32_t *status) {
     using L = PipeSmem<P>;
@@ -327,20 +414,26 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     uint16_t *frq = reinterpret_cast<uint16_t *>(smem + L::frq);
     uint8_t *tile = smem + L::tile;
     float *m1s = reinterpret_cast<float *>(smem + L::m1);
+    uint8_t *srec = smem + L::recs;
 
     int k, kv, l;
     slice_coords(d, blockIdx.x, k, kv, l);
-    const int A = d.A[kv];
+    constexpr bool v2 = V2;  // format 2: CDF rows from count records
+    const int A = v2 ? 2 * mt.v[kv][l] + 1 : d.A[kv];
     const uint32_t amax2 = 2u * ((uint32_t)A - 1);
     const int Tk = chunk_tokens(d, k);
     const int tid = threadIdx.x;
     const bool helper = tid >= kThreads;
     const int hl = tid - kThreads;  // helper lane
     const long long t0 = (long long)k * d.Tc;
-    const long long cdf_base = cdf_slice_offset(d, k, kv, l);
+    const long long side_base = v2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
     const long long sid = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk + tid;
     const int nwin = (d.C + W - 1) / W;
 
+    __shared__ uint16_t s_ftab[kThreads + 2];  // format 2: f(n) = 1 + n (65536 - A) / Tk
+    if (v2)
+        for (int n = tid; n <= Tk; n += kThreads + kHelpers)
+            s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kM - (uint32_t)A)) / (uint32_t)Tk);
     if (MODE == 1 && !helper) {
         const int MAX = mt.v[kv][l];
         s_unit[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
@@ -367,7 +460,20 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     // slice offset a multiple of 8 entries (both alphabets multiples of 8)
     const bool vec = ((reinterpret_cast<uintptr_t>(cdf) & 15) == 0) && (d.A[0] % 8 == 0) &&
                      (d.A[1] % 8 == 0);
-    if (helper) stage_rows<P>(cum, frq, cdf + cdf_base, A, min(W, d.C), hl, vec);
+    bool bad_rec = false;
+    if (v2) {
+        // records of windows 0 and 1 in, rows of window 0 built; later windows:
+        // the helper copies window i + 2's records while the decoder threads
+        // build window i + 1's rows and decode window i
+        if (helper) {
+            copy_records(srec, rec + side_base, min(W, d.C) * A, hl);
+            if (nwin > 1) copy_records(srec + W * P, rec + side_base + (long long)W * A, min(W, d.C - W) * A, hl);
+        }
+        __syncthreads();  // s_ftab and the records
+        if (!helper) bad_rec |= build_rows_v2<P>(cum, frq, srec, A, (uint32_t)Tk, W, min(W, d.C), tid, s_ftab);
+    } else if (helper) {
+        stage_rows<P>(cum, frq, cdf + side_base, A, min(W, d.C), hl, vec);
+    }
     __syncthreads();
 
     const uint32_t fo = (uint32_t)(L::frq - L::cum);
@@ -379,20 +485,29 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
         const int c0 = i * W;
         const int Wc = min(W, d.C - c0);
         if (!helper) {
+            if (V2 && i + 1 < nwin)  // window i + 1's rows into the other buffer
+                bad_rec |= build_rows_v2<P>(cum + (b ^ 1) * W * P, frq + (b ^ 1) * W * P, srec + (b ^ 1) * W * P, A,
+                                            (uint32_t)Tk, W, min(W, d.C - c0 - W), tid, s_ftab);
             if (tid < Tk) {
                 // shared address of this buffer's rows; frequencies follow at a fixed offset
                 const uint32_t cb = (uint32_t)__cvta_generic_to_shared(cum + b * W * P);
                 uint8_t *my = tile + tid * TS;
-                if (A == P) {
+                constexpr int PH = P > 4 ? P / 2 : P;
+                if (!V2 && A == P) {  // format 2's alphabets are odd: never equal to P
                     if (tail)
-                        decode_window<P, false, true>(s, cb, fo, amax2, my, Wc);
+                        decode_window<P, P, false, true>(s, cb, fo, amax2, my, Wc);
                     else
-                        decode_window<P, false, false>(s, cb, fo, amax2, my, Wc);
+                        decode_window<P, P, false, false>(s, cb, fo, amax2, my, Wc);
+                } else if (A <= PH) {  // the alphabet fits in half the row: one search step less
+                    if (tail)
+                        decode_window<P, PH, true, true>(s, cb, fo, amax2, my, Wc);
+                    else
+                        decode_window<P, PH, true, false>(s, cb, fo, amax2, my, Wc);
                 } else {
                     if (tail)
-                        decode_window<P, true, true>(s, cb, fo, amax2, my, Wc);
+                        decode_window<P, P, true, true>(s, cb, fo, amax2, my, Wc);
                     else
-                        decode_window<P, true, false>(s, cb, fo, amax2, my, Wc);
+                        decode_window<P, P, true, false>(s, cb, fo, amax2, my, Wc);
                 }
             }
             __syncwarp();
@@ -400,8 +515,12 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
                 write_window<P, MODE, 32>(wtile, s_unit, m1s + 32 * warp, d, kv, l, t0 + 32 * warp, wrows, c0, Wc,
                                           sym, out_k, out_v, lane);
             __syncwarp();  // the rows are read before the next window overwrites them
+        } else if (V2) {
+            if (i + 2 < nwin)  // records of window i + 2 replace window i's (its rows were built last round)
+                copy_records(srec + b * W * P, rec + side_base + (long long)(c0 + 2 * W) * A,
+                             min(W, d.C - c0 - 2 * W) * A, hl);
         } else if (i + 1 < nwin) {
-            stage_rows<P>(cum + (b ^ 1) * W * P, frq + (b ^ 1) * W * P, cdf + cdf_base + (long long)(c0 + W) * A, A,
+            stage_rows<P>(cum + (b ^ 1) * W * P, frq + (b ^ 1) * W * P, cdf + side_base + (long long)(c0 + W) * A, A,
                           min(W, d.C - c0 - W), hl, vec);
         }
         __syncthreads();
@@ -412,28 +531,40 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
         const long long consumed = (long long)len[sid] - s.rem - s.nb / 8;
         if ((corrupt || consumed != (long long)len[sid] + 3) && status) atomicOr(status, CG_FLAG_CORRUPT);
     }
+    if (bad_rec && status) atomicOr(status, CG_FLAG_CORRUPT);
+}
+
+template <int P, int MODE, bool V2>
+cudaError_t launch_pm(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off, const uint32_t *len,
+                      const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1, const Dims &d, const MaxTab &mt,
+                      uint8_t *sym, float *out_k, float *out_v, int32_t *status, cudaStream_t s) {
+    const unsigned nslices = (unsigned)(2LL * d.L * d.nch);
+    const int smem = (int)PipeSmem<P>::bytes;
+    cudaError_t err = cudaFuncSetAttribute(k_decode_pipe<P, MODE, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           smem);
+    if (err != cudaSuccess) return err;
+    k_decode_pipe<P, MODE, V2><<<nslices, kThreads + kHelpers, smem, s>>>(
+        packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v, status);
+    return cudaGetLastError();
 }
 
 template <int P>
 cudaError_t launch_p(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
-                     const uint32_t *len, const uint16_t *cdf, const uint16_t *max1, const Dims &d,
-                     const MaxTab &mt, int mode, uint8_t *sym, float *out_k, float *out_v,
+                     const uint32_t *len, const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1,
+                     const Dims &d, const MaxTab &mt, int mode, uint8_t *sym, float *out_k, float *out_v,
                      int32_t *status, cudaStream_t s) {
-    const unsigned nslices = (unsigned)(2LL * d.L * d.nch);
-    const int smem = (int)PipeSmem<P>::bytes;
-    cudaError_t err;
-    if (mode == 1) {
-        err = cudaFuncSetAttribute(k_decode_pipe<P, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        k_decode_pipe<P, 1><<<nslices, kThreads + kHelpers, smem, s>>>(
-            packed, (long long)packed_bytes, off, len, cdf, max1, d, mt, sym, out_k, out_v, status);
-    } else {
-        err = cudaFuncSetAttribute(k_decode_pipe<P, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
-        k_decode_pipe<P, 0><<<nslices, kThreads + kHelpers, smem, s>>>(
-            packed, (long long)packed_bytes, off, len, cdf, max1, d, mt, sym, out_k, out_v, status);
+    if (rec) {
+        if (mode == 1)
+            return launch_pm<P, 1, true>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v,
+                                         status, s);
+        return launch_pm<P, 0, true>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v,
+                                     status, s);
     }
-    return cudaGetLastError();
+    if (mode == 1)
+        return launch_pm<P, 1, false>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v,
+                                      status, s);
+    return launch_pm<P, 0, false>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v, status,
+                                  s);
 }
 
 }  // namespace
@@ -443,16 +574,29 @@ cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes, const ui
                           const Dims &d, const MaxTab &mt, int mode, uint8_t *sym, float *out_k,
                           float *out_v, int32_t *status, cudaStream_t s) {
     const int tmax = d.Tc < d.T ? d.Tc : d.T;
-    const int A = d.A[0] > d.A[1] ? d.A[0] : d.A[1];
     if (tmax > kThreads)
         return launch_decode_generic(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k,
                                      out_v, status, s);
-    if (A <= 8) return launch_p<8>(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 16) return launch_p<16>(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 32) return launch_p<32>(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 64) return launch_p<64>(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 128) return launch_p<128>(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    return launch_p<256>(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k, out_v, status, s);
+    return launch_decode_pipe(packed, packed_bytes, off, len, cdf, nullptr, max1, d, mt, mode, sym, out_k, out_v,
+                              status, s);
+}
+
+cudaError_t launch_decode_pipe(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
+                               const uint32_t *len, const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1,
+                               const Dims &d, const MaxTab &mt, int mode, uint8_t *sym, float *out_k, float *out_v,
+                               int32_t *status, cudaStream_t s) {
+    int A = d.A[0] > d.A[1] ? d.A[0] : d.A[1];
+    if (rec) {  // format 2: the largest layer alphabet, 2 * MAX + 1
+        A = 0;
+        for (int kv = 0; kv < 2; kv++)
+            for (int l = 0; l < d.L; l++) A = 2 * mt.v[kv][l] + 1 > A ? 2 * mt.v[kv][l] + 1 : A;
+    }
+    if (A <= 8) return launch_p<8>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
+    if (A <= 16) return launch_p<16>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
+    if (A <= 32) return launch_p<32>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
+    if (A <= 64) return launch_p<64>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
+    if (A <= 128) return launch_p<128>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
+    return launch_p<256>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
 }
 
 }  // namespace cg

@@ -58,7 +58,8 @@ def assemble(parts: list[dict]) -> dict:
     """Join per-rank outputs (in rank order) into the whole tensor's output.
 
     Each part holds host arrays of one rank's compress call on its token range:
-    max1 uint16 [2][L][T_r], cdf uint16 (chunk-major), packed uint8 (exactly
+    max1 uint16 [2][L][T_r], cdf uint16 (chunk-major; format 2: rec uint8
+    count records, chunk-major too), packed uint8 (exactly
     off[-1] bytes), len uint32 [2 L T_r], off uint64 [2 L T_r + 1]. The result
     is byte-identical to compressing the whole tensor in one call.
     """
@@ -73,9 +74,10 @@ def assemble(parts: list[dict]) -> dict:
         offs.append(off[:-1] + np.uint64(base))
         base += int(off[-1])
     offs.append(np.array([base], dtype=np.uint64))
+    side = "cdf" if "cdf" in parts[0] else "rec"  # format 1 CDF entries or format 2 count records
     return {
         "max1": np.concatenate([np.asarray(p["max1"], np.uint16) for p in parts], axis=2),
-        "cdf": np.concatenate([np.asarray(p["cdf"], np.uint16) for p in parts]),
+        side: np.concatenate([np.asarray(p[side], np.uint16 if side == "cdf" else np.uint8) for p in parts]),
         "packed": np.concatenate([np.asarray(p["packed"], np.uint8) for p in parts]),
         "len": np.concatenate([np.asarray(p["len"], np.uint32) for p in parts]),
         "off": np.concatenate(offs),

@@ -89,13 +89,15 @@ class HostPiece:
     packed: torch.Tensor   # uint8 [capacity]; bytes [0, nbytes) are the streams
     len: torch.Tensor      # int32 [2 L (t1 - t0)] (uint32)
     off: torch.Tensor      # int64 [2 L (t1 - t0) + 1]
-    cdf: torch.Tensor      # int16 (uint16 entries)
+    side: torch.Tensor     # format 1: int16 CDF entries; format 2: uint8 count records
     max1: torch.Tensor     # int16 [2, L, t1 - t0] (fp16 bits)
     ready: torch.cuda.Event
+    fmt: int = 1
 
     def arrays(self) -> dict:
         """numpy views in the layout `shard.assemble` joins."""
-        return {"max1": self.max1.numpy().view(np.uint16), "cdf": self.cdf.numpy().view(np.uint16),
+        side = ("cdf", self.side.numpy().view(np.uint16)) if self.fmt == 1 else ("rec", self.side.numpy())
+        return {"max1": self.max1.numpy().view(np.uint16), side[0]: side[1],
                 "packed": self.packed[:self.nbytes].numpy(), "len": self.len.numpy().view(np.uint32),
                 "off": self.off.numpy().view(np.uint64)}
 
@@ -108,9 +110,11 @@ class StreamingCodec:
     """
 
     def __init__(self, L: int, T: int, C_: int, bins_k, bins_v=None, chunk_tokens: int = 256,
-                 piece_chunks: int = 2, device: str | torch.device = "cuda"):
+                 piece_chunks: int = 2, device: str | torch.device = "cuda", fmt: int = 1):
         if piece_chunks < 1:
             raise ValueError("piece_chunks must be >= 1")
+        self.fmt = fmt
+        self.side_key = "cdf" if fmt == 1 else "rec"
         self.L, self.T, self.C = L, T, C_
         self.bins_k = bins_k
         self.bins_v = bins_k if bins_v is None else bins_v
@@ -120,15 +124,16 @@ class StreamingCodec:
         self.k = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
         self.v = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
         mk = lambda t0, t1: _codec.Codec(L, t1 - t0, C_, self.bins_k, self.bins_v, chunk_tokens=chunk_tokens,
-                                         device=dev)
+                                         device=dev, fmt=fmt)
         self.enc = [mk(t0, t1) for t0, t1 in self.ranges]
         self.dec = [mk(t0, t1) for t0, t1 in self.ranges]
         self.host = []
         for cd in self.enc:
             o = cd.out
             pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            self.host.append(dict(packed=torch.empty(cd.capacity, dtype=torch.uint8, pin_memory=True),
-                                  len=pin(o.len), off=pin(o.off), cdf=pin(o.cdf), max1=pin(o.max1)))
+            side = o.cdf if fmt == 1 else o.rec
+            self.host.append({"packed": torch.empty(cd.capacity, dtype=torch.uint8, pin_memory=True),
+                              "len": pin(o.len), "off": pin(o.off), self.side_key: pin(side), "max1": pin(o.max1)})
         self.n_host = torch.zeros(len(self.ranges), dtype=torch.int64, pin_memory=True)
         self.status_host = torch.zeros(2 * len(self.ranges), dtype=torch.int32, pin_memory=True)
         self.s_in = torch.cuda.Stream(device=dev)
@@ -187,11 +192,12 @@ class StreamingCodec:
             o, h = self.enc[p].out, self.host[p]
             self.s_out.wait_event(self.ev_enc[p])
             _copy(h["packed"], o.packed, n, self.s_out)
-            for key in ("len", "off", "cdf", "max1"):
+            for key in ("len", "off", self.side_key, "max1"):
                 _copy(h[key], getattr(o, key), _nb(h[key]), self.s_out)
             _copy(self.status_host[2 * p:2 * p + 1], o.status, 4, self.s_out)
             self.ev_out[p].record(self.s_out)
-            yield HostPiece(t0, t1, n, h["packed"], h["len"], h["off"], h["cdf"], h["max1"], self.ev_out[p])
+            yield HostPiece(t0, t1, n, h["packed"], h["len"], h["off"], h[self.side_key], h["max1"], self.ev_out[p],
+                            self.fmt)
             if p + ahead < npc:
                 self._send(p + ahead, k_host, v_host)
 
@@ -208,8 +214,9 @@ class StreamingCodec:
         up = self.s_rx if upload is None else upload
         up.wait_event(hp.ready)
         _copy(rx.packed, hp.packed, hp.nbytes, up)
-        for key in ("len", "off", "cdf", "max1"):
+        for key in ("len", "off", "max1"):
             _copy(getattr(rx, key), getattr(hp, key), _nb(getattr(hp, key)), up)
+        _copy(getattr(rx, self.side_key), hp.side, _nb(hp.side), up)
         self.ev_rx[p].record(up)
         self.s_dec.wait_event(self.ev_rx[p])
         out = cd.decompress(rx, stream=self.s_dec)
@@ -247,7 +254,7 @@ class StreamingCodec:
     def bytes_moved(self, pieces: list[HostPiece]) -> tuple[int, int]:
         """(host-to-device, device-to-host) bytes of one compress + decompress."""
         fp16 = 2 * 2 * self.L * self.T * self.C
-        side = sum(hp.len.numel() * 4 + hp.off.numel() * 8 + hp.cdf.numel() * 2 + hp.max1.numel() * 2
+        side = sum(hp.len.numel() * 4 + hp.off.numel() * 8 + _nb(hp.side) + hp.max1.numel() * 2
                    for hp in pieces)
         comp = sum(hp.nbytes for hp in pieces)
         return fp16 + comp + side, 8 * len(pieces) + comp + side + 8 * len(pieces)

@@ -25,7 +25,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_version(lib):
-    assert lib.cg_version().decode().startswith("cachegen-gb300 format-1")
+    assert lib.cg_version().decode().startswith("cachegen-gb300 formats-1,2")
 
 
 def _shape(L, T, C_, Tc=256, ls=None):
@@ -112,3 +112,23 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(capi, "_LIB", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         capi.load()
+
+
+def test_record_bytes_match_oracle(oracle_mod):
+    from kv_cache_compression_cg_gb300 import capi, codec
+    import numpy as np
+    lib = capi.load()
+    for L, T, C_, Tc, bk, bv in [(2, 64, 64, 64, [32, 16], [16, 32]), (3, 200, 40, 64, [32, 16, 7], [8, 8, 256]),
+                                (1, 300, 8, 256, [4], [5])]:
+        shp = codec.make_shape(L, T, C_, Tc)
+        bka, bva = np.array(bk, np.int32), np.array(bv, np.int32)
+        got = lib.cg_record_bytes(ctypes_ref(shp), bka.ctypes.data, bva.ctypes.data)
+        assert got == oracle_mod.rec_bytes(L, T, C_, Tc, bk, bv)
+    shp = codec.make_shape(1, 600, 8, 300)  # format 2 needs chunks of at most 256 tokens
+    b = np.array([16], np.int32)
+    assert lib.cg_record_bytes(ctypes_ref(shp), b.ctypes.data, b.ctypes.data) == 0
+
+
+def ctypes_ref(x):
+    import ctypes
+    return ctypes.byref(x)
