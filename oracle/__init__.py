@@ -71,6 +71,8 @@ def lib() -> C.CDLL:
                                            p, p, p, p, p, u64, p, p]),
                 "orc_decompress": (C.c_int, [p, p, p, p, p] + [C.c_int] * 4 + [p, p, p, p]),
                 "orc_alphabet_v2": (C.c_int, [C.c_int]),
+                "orc_float_to_half": (C.c_uint16, [C.c_float]),
+                "orc_dequantize_half": (C.c_int, [p, p, C.c_int, C.c_int, C.c_int, p, p, p, p]),
                 "orc_rec_bytes": (i64, [C.c_int] * 4 + [p, p]),
                 "orc_rec_offset": (i64, [C.c_int, C.c_int, p, p] + [C.c_int] * 4),
                 "orc_record_from_counts": (C.c_int, [p, C.c_int, p]),
@@ -393,4 +395,25 @@ def decompress_v2(packed, off, ln, rec, max1, L, T, C_, Tc, bins_k, bins_v=None)
                                    _ptr(np.ascontiguousarray(max1, np.uint16)),
                                    L, T, C_, Tc, _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)),
            "decompress_v2")
+    return out_k, out_v
+
+
+# ----------------------------------------------------------------------------
+# serving layouts: binary16 output
+# ----------------------------------------------------------------------------
+def float_to_half(x: float) -> int:
+    """binary32 -> binary16 bits, round to nearest, ties to even."""
+    return int(lib().orc_float_to_half(float(np.float32(x))))
+
+
+def dequantize_half(sym, max1, bins_k, bins_v=None):
+    """sym [2][L][T][C] + max1 [2][L][T] -> binary16 K, V [L][T][C] (as uint16 bits)."""
+    sym = np.ascontiguousarray(sym, dtype=np.uint8)
+    _, L, T, C_ = sym.shape
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    out_k = np.empty((L, T, C_), np.uint16)
+    out_v = np.empty((L, T, C_), np.uint16)
+    _check(lib().orc_dequantize_half(_ptr(sym), _ptr(np.ascontiguousarray(max1, np.uint16)), L, T, C_,
+                                     _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)), "dequantize_half")
     return out_k, out_v

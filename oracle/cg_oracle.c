@@ -708,3 +708,69 @@ int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
     free(sym), free(rows);
     return status;
 }
+
+/* ---- serving layouts: binary16 output ---------------------------------- */
+
+/* binary32 -> binary16 bits, round to nearest, ties to even (IEEE 754):
+ * finite values keep 11 significant bits (fewer below 2^-14, where the
+ * spacing is 2^-24); too large values become infinity, NaN stays NaN. */
+uint16_t orc_float_to_half(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    uint16_t sign = (uint16_t)((b >> 16) & 0x8000u);
+    uint32_t e = (b >> 23) & 0xFFu;
+    uint32_t m = b & 0x7FFFFFu;
+    if (e == 0xFFu) /* infinity or NaN */
+        return (uint16_t)(sign | 0x7C00u | (m ? 0x200u : 0u));
+    int exp = (int)e - 127; /* unbiased; x = 1.m * 2^exp for normal x */
+    if (e == 0)             /* binary32 subnormal: far below half's smallest */
+        return sign;
+    uint32_t sig = m | 0x800000u; /* 24-bit significand, value sig * 2^(exp-23) */
+    /* half keeps the bits down to 2^-24 (subnormal range) or to 2^(exp-10) */
+    int lsb = exp - 10 < -24 ? -24 : exp - 10; /* exponent of the last kept bit */
+    int shift = lsb - (exp - 23);              /* bits of sig to drop, >= 13 */
+    if (shift > 25)
+        return sign; /* below half the smallest subnormal: rounds to zero */
+    uint32_t kept = sig >> shift;
+    uint32_t rest = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rest > half || (rest == half && (kept & 1u)))
+        kept++; /* may carry into the next binade; handled by the sum below */
+    /* value = kept * 2^lsb; encode: normal when lsb > -24 or kept >= 2^10 */
+    uint32_t h;
+    if (lsb == -24) {
+        h = kept; /* subnormal (kept < 2^10) or, after rounding, 2^10 = smallest normal */
+    } else {
+        /* kept in [2^10, 2^11]; exponent field = lsb + 10 + 15 */
+        uint32_t ef = (uint32_t)(lsb + 10 + 15);
+        h = (ef << 10) + (kept - 0x400u); /* kept == 2^11 rolls into the next exponent */
+    }
+    if (h >= 0x7C00u)
+        h = 0x7C00u; /* overflow to infinity */
+    return (uint16_t)(sign | h);
+}
+
+/* [CG §2.4(2)] dequantisation with binary16 output: the binary32 value of D
+ * rounded to nearest-even binary16 (no overflow: |x^| <= max1). */
+int orc_dequantize_half(const uint8_t *sym, const uint16_t *max1, int L, int T,
+                        int C, const int32_t *bins_k, const int32_t *bins_v,
+                        uint16_t *out_k, uint16_t *out_v)
+{
+    if (!orc_check_shape(L, T, C))
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    for (int kv = 0; kv < 2; kv++) {
+        uint16_t *out = kv ? out_v : out_k;
+        const int32_t *bins = kv ? bins_v : bins_k;
+        for (int l = 0; l < L; l++)
+            for (int t = 0; t < T; t++) {
+                int64_t g = ((int64_t)kv * L + l) * T + t;
+                for (int c = 0; c < C; c++)
+                    out[((int64_t)l * T + t) * C + c] = orc_float_to_half(
+                        orc_dequantize_value(sym[g * C + c], bins[l], max1[g]));
+            }
+    }
+    return ORC_OK;
+}

@@ -202,6 +202,14 @@ int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
                       const int32_t *bins_k, const int32_t *bins_v,
                       float *out_k, float *out_v);
 
+/* ---- serving layouts ---------------------------------------------------- */
+/* binary32 -> binary16 bits, round to nearest, ties to even. */
+uint16_t orc_float_to_half(float x);
+/* D with binary16 output (each binary32 value rounded to nearest-even). */
+int orc_dequantize_half(const uint8_t *sym, const uint16_t *max1, int L, int T,
+                        int C, const int32_t *bins_k, const int32_t *bins_v,
+                        uint16_t *out_k, uint16_t *out_v);
+
 #ifdef __cplusplus
 }
 #endif
