@@ -267,6 +267,29 @@ cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes,
                                  float *out_v, int32_t *status,
                                  cudaStream_t stream);
 
+/* ---- serving layouts ----------------------------------------------------
+ * Decompression straight into the layout a serving engine keeps its cache in
+ * [CG §3.2] (K and V of a layer side by side: [L][2][T][C], i.e. out_v =
+ * out_k + T*C and a layer stride of 2*T*C), as binary32 or as binary16 (each
+ * binary32 value of D rounded to nearest, ties to even).
+ */
+#define CG_OUT_F32 0
+#define CG_OUT_F16 1
+
+/* Decode fused with dequantisation, either format (format 1: side = uint16
+ * CDF entries; format 2: side = uint8 count records), into out_k / out_v
+ * [L][T][C] of out_dtype with layers out_layer_stride elements apart
+ * (>= T*C; tokens C apart, channels contiguous). Requires chunk_tokens <= 256.
+ * Status bits as cg_decompress_chunk / cg_decompress_chunk_v2. */
+cg_status cg_decompress_chunk_ex(const uint8_t *packed, uint64_t packed_bytes,
+                                 const uint64_t *off, const uint32_t *len,
+                                 const void *side, const uint16_t *max1,
+                                 const cg_shape *shape, const int32_t *bins_k,
+                                 const int32_t *bins_v, int format,
+                                 int out_dtype, void *out_k, void *out_v,
+                                 int64_t out_layer_stride, int32_t *status,
+                                 cudaStream_t stream);
+
 /* Library version string ("cachegen-gb300 <format> <build>"). */
 const char *cg_version(void);
 

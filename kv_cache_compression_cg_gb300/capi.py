@@ -17,6 +17,7 @@ CG_FLAG_NONFINITE, CG_FLAG_CAPACITY, CG_FLAG_CORRUPT, CG_FLAG_BAD_SYMBOL = 0x1, 
 CG_FLAG_TIMEOUT = 0x10
 CG_MAX_LAYERS, CG_MAX_CHUNK_TOKENS, CG_MAX_CHANNELS = 1024, 1024, 65536
 CG_NOALLOC_WORKSPACE_BYTES = 64 << 20
+CG_OUT_F32, CG_OUT_F16 = 0, 1
 
 _ERRORS = {CG_ERR_INVALID_ARG: "invalid argument", CG_ERR_WORKSPACE: "workspace too small",
            CG_ERR_CUDA: "CUDA launch failed"}
@@ -54,6 +55,8 @@ SIGNATURES = {
     "cg_compress_chunk_v2": (_i32, [_p, _p, _SHAPE, _p, _p, _p, _p, _p, _u64, _p, _p, _p, _u64,
                                     _p, _p]),
     "cg_decompress_chunk_v2": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, _p, _p, _p, _p]),
+    "cg_decompress_chunk_ex": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, C.c_int, C.c_int, _p, _p,
+                                      C.c_int64, _p, _p]),
     "cg_version": (C.c_char_p, []),
 }
 

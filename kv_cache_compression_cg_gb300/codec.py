@@ -160,6 +160,29 @@ class Codec:
         return self.out_k, self.out_v
 
 
+    def decompress_into(self, out_k: torch.Tensor, out_v: torch.Tensor, c: Compressed | None = None,
+                        stream=None) -> None:
+        """Decompress straight into a serving layout: out_k / out_v are
+        float32 or float16 [L, T, C] views with contiguous [T, C] planes and
+        the same layer stride (e.g. buf[:, 0] and buf[:, 1] of a [L, 2, T, C]
+        cache). float16 gets each binary32 value rounded to nearest-even."""
+        c = self.out if c is None else c
+        if out_k.dtype != out_v.dtype or out_k.dtype not in (torch.float32, torch.float16):
+            raise TypeError("outputs must both be float32 or both float16")
+        if tuple(out_k.shape) != (c.L, c.T, c.C) or out_v.shape != out_k.shape:
+            raise ValueError("outputs must be [L, T, C]")
+        if out_k.stride(2) != 1 or out_k.stride(1) != c.C or out_v.stride() != out_k.stride():
+            raise ValueError("outputs need contiguous [T, C] planes with equal layer strides")
+        shp = make_shape(c.L, c.T, c.C, c.chunk_tokens)
+        side = c.cdf if c.fmt == 1 else c.rec
+        capi.check(capi.load().cg_decompress_chunk_ex(
+            _ptr(c.packed), c.packed.numel(), _ptr(c.off), _ptr(c.len), _ptr(side), _ptr(c.max1),
+            C.byref(shp), _np_ptr(c.bins_k), _np_ptr(c.bins_v), c.fmt,
+            capi.CG_OUT_F16 if out_k.dtype == torch.float16 else capi.CG_OUT_F32,
+            _ptr(out_k), _ptr(out_v), out_k.stride(0), _ptr(self.dstatus), _stream(stream)),
+            "cg_decompress_chunk_ex")
+
+
 # ---------------------------------------------------------------------------
 # one-shot step functions (allocate their outputs with torch)
 # ---------------------------------------------------------------------------

@@ -318,8 +318,32 @@ cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes, c
     if (!aligned(packed, 4) || !aligned(off, 8) || !aligned(len, 4) || !aligned(max1, 2) ||
         !aligned(out_k, 16) || !aligned(out_v, 16))
         return CG_ERR_INVALID_ARG;
-    return launched(cg::launch_decode_pipe(packed, packed_bytes, off, len, nullptr, rec, max1, d, mt, 1, nullptr,
-                                           out_k, out_v, status, stream));
+    return launched(cg::launch_decode_pipe(packed, packed_bytes, off, len, nullptr, rec, max1, d, mt, 1, out_k,
+                                           out_v, (long long)d.T * d.C, status, stream));
+}
+
+cg_status cg_decompress_chunk_ex(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
+                                 const uint32_t *len, const void *side, const uint16_t *max1,
+                                 const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v, int format,
+                                 int out_dtype, void *out_k, void *out_v, int64_t out_layer_stride,
+                                 int32_t *status, cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return CG_ERR_INVALID_ARG;
+    if ((format != 1 && format != 2) || (out_dtype != CG_OUT_F32 && out_dtype != CG_OUT_F16))
+        return CG_ERR_INVALID_ARG;
+    if (out_layer_stride < (int64_t)d.T * d.C) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    const uintptr_t es = out_dtype == CG_OUT_F16 ? 2 : 4;
+    if (!packed || !off || !len || !side || !max1 || !out_k || !out_v) return CG_ERR_INVALID_ARG;
+    if (!aligned(packed, 4) || !aligned(off, 8) || !aligned(len, 4) || !aligned(max1, 2) ||
+        !aligned(side, format == 1 ? 2 : 1) || !aligned(out_k, es) || !aligned(out_v, es))
+        return CG_ERR_INVALID_ARG;
+    const uint16_t *cdf = format == 1 ? static_cast<const uint16_t *>(side) : nullptr;
+    const uint8_t *rec = format == 2 ? static_cast<const uint8_t *>(side) : nullptr;
+    return launched(cg::launch_decode_pipe(packed, packed_bytes, off, len, cdf, rec, max1, d, mt,
+                                           out_dtype == CG_OUT_F16 ? 2 : 1, out_k, out_v, out_layer_stride, status,
+                                           stream));
 }
 
 }  // extern "C"

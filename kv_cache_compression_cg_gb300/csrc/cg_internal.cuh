@@ -151,12 +151,13 @@ cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes,
                           cudaStream_t s);
 
 // Chunks of up to 256 tokens; rec != nullptr selects format 2 (CDF rows from
-// the count records, cdf unused).
+// the count records, cdf unused). out_dtype 1: binary32, 2: binary16 (rounded
+// to nearest-even); outputs [L][T][C] with layers `ols` elements apart.
 cudaError_t launch_decode_pipe(const uint8_t *packed, uint64_t packed_bytes,
                                const uint64_t *off, const uint32_t *len,
                                const uint16_t *cdf, const uint8_t *rec,
                                const uint16_t *max1, const Dims &d, const MaxTab &mt,
-                               int mode, uint8_t *sym, float *out_k, float *out_v,
+                               int out_dtype, void *out_k, void *out_v, long long ols,
                                int32_t *status, cudaStream_t s);
 
 // Any chunk size up to CG_MAX_CHUNK_TOKENS (used by launch_decode beyond 256).

@@ -315,37 +315,32 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
     return v;
 }
 
-// Write the decoded window in `tile` out as rows: dequantised binary32
-// (MODE 1: unit[s] * max1, with unit[s] = (s - MAX) / MAX) or symbols (MODE
-// 0). NTHR threads with index `id` share the work. With 4s in the tile bytes
-// and the table 256-byte aligned, one byte permute makes each entry's shared
-// address (table base with the low byte replaced).
+// Write the decoded window in `tile` out as rows of the dequantised values
+// unit[s] * max1 (unit[s] = (s - MAX) / MAX), binary32 (MODE 1) or rounded to
+// nearest-even binary16 (MODE 2), into [L][T][C] with layers `ols` elements
+// apart. NTHR threads with index `id` share the work. With 4s in the tile
+// bytes and the table 256-byte aligned, one byte permute makes each entry's
+// shared address (table base with the low byte replaced). `vec` says the
+// output rows allow 16-byte (binary32) or 8-byte (binary16) stores.
 template <int P, int MODE, int NTHR>
 __device__ __forceinline__ void write_window(const uint8_t *tile, const float *unit, const float *m1s,
-                                             const Dims &d, int kv, int l, long long t0, int Tk, int c0,
-                                             int Wc, uint8_t *sym, float *out_k, float *out_v, int id) {
+                                             const Dims &d, int kv, int l, long long t0, int Tk, int c0, int Wc,
+                                             void *out_k, void *out_v, long long ols, bool vec, int id) {
     constexpr int W = DecodeCfg<P>::W;
     constexpr int TS = DecodeCfg<P>::TS;
     constexpr int SH = DecodeCfg<P>::SYM_SHIFT;
-    if (MODE == 0) {
-        uint8_t *dst = sym + group_index(d, kv, l, t0) * d.C + c0;
-        for (int i = id; i < Tk * W; i += NTHR) {
-            const int r = i / W, j = i % W;
-            if (j < Wc) dst[(long long)r * d.C + j] = (uint8_t)(tile[r * TS + j] >> SH);
-        }
-        return;
-    }
-    float *out = (kv ? out_v : out_k) + ((long long)l * d.T + t0) * d.C + c0;
-    if (SH == 2 && Wc == W && (d.C & 3) == 0 && NTHR % (W / 4) == 0) {
-        constexpr int PR = W / 4;        // float4 per row
+    constexpr int ES = MODE == 2 ? 2 : 4;  // output element bytes
+    char *out = static_cast<char *>(kv ? out_v : out_k) + ((long long)l * ols + t0 * d.C + c0) * ES;
+    if (SH == 2 && Wc == W && vec && NTHR % (W / 4) == 0) {
+        constexpr int PR = W / 4;        // four-value groups per row
         constexpr int RPI = NTHR / PR;   // rows per pass
         const int j = id % PR;
         int r = id / PR;
         const uint32_t us = (uint32_t)__cvta_generic_to_shared(unit);
         uint32_t ts = (uint32_t)__cvta_generic_to_shared(tile) + r * TS + 4 * j;
         uint32_t ms = (uint32_t)__cvta_generic_to_shared(m1s) + 4 * r;
-        float4 *o = reinterpret_cast<float4 *>(out + (long long)r * d.C) + j;
-        const long long ostep = (long long)RPI * d.C / 4;
+        char *o = out + ((long long)r * d.C + 4 * j) * ES;
+        const long long ostep = (long long)RPI * d.C * ES;
 #pragma unroll 1
         for (; r < Tk; r += RPI, ts += RPI * TS, ms += 4 * RPI, o += ostep) {
             const uint32_t q4 = lds_u32(ts) & 0xFCFCFCFCu;  // 4s: keeps every table load aligned
@@ -354,12 +349,26 @@ __device__ __forceinline__ void write_window(const uint8_t *tile, const float *u
             const float u1 = lds_f32(__byte_perm(q4, us, 0x7651));
             const float u2 = lds_f32(__byte_perm(q4, us, 0x7652));
             const float u3 = lds_f32(__byte_perm(q4, us, 0x7653));
-            *o = make_float4(__fmul_rn(u0, m), __fmul_rn(u1, m), __fmul_rn(u2, m), __fmul_rn(u3, m));
+            const float x0 = __fmul_rn(u0, m), x1 = __fmul_rn(u1, m), x2 = __fmul_rn(u2, m), x3 = __fmul_rn(u3, m);
+            if (MODE == 2) {
+                const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+                *reinterpret_cast<uint2 *>(o) = make_uint2(*reinterpret_cast<const uint32_t *>(&h01),
+                                                           *reinterpret_cast<const uint32_t *>(&h23));
+            } else {
+                *reinterpret_cast<float4 *>(o) = make_float4(x0, x1, x2, x3);
+            }
         }
     } else {
         for (int i = id; i < Tk * W; i += NTHR) {
             const int r = i / W, j = i % W;
-            if (j < Wc) out[(long long)r * d.C + j] = __fmul_rn(unit[tile[r * TS + j] >> SH], m1s[r]);
+            if (j < Wc) {
+                const float x = __fmul_rn(unit[tile[r * TS + j] >> SH], m1s[r]);
+                char *e = out + ((long long)r * d.C + j) * ES;
+                if (MODE == 2)
+                    *reinterpret_cast<__half *>(e) = __float2half_rn(x);
+                else
+                    *reinterpret_cast<float *>(e) = x;
+            }
         }
     }
 }
@@ -403,8 +412,8 @@ template <int P, int MODE, bool V2>
 __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     const uint8_t *__restrict__ packed, long long packed_bytes, const uint64_t *__restrict__ off,
     const uint32_t *__restrict__ len, const uint16_t *__restrict__ cdf, const uint8_t *__restrict__ rec,
-    const uint16_t *__restrict__ max1, Dims d, MaxTab mt, uint8_t *__restrict__ sym,
-    float *__restrict__ out_k, float *__restrict__ out_v, int32_t *status) {
+    const uint16_t *__restrict__ max1, Dims d, MaxTab mt, void *__restrict__ out_k, void *__restrict__ out_v,
+    long long ols, int32_t *status) {
     using L = PipeSmem<P>;
     constexpr int W = L::W;
     constexpr int TS = L::TS;
@@ -434,7 +443,7 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     if (v2)
         for (int n = tid; n <= Tk; n += kThreads + kHelpers)
             s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kM - (uint32_t)A)) / (uint32_t)Tk);
-    if (MODE == 1 && !helper) {
+    if (!helper) {
         const int MAX = mt.v[kv][l];
         s_unit[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
         if (tid < Tk) m1s[tid] = __half2float(__ushort_as_half(max1[group_index(d, kv, l, t0 + tid)]));
@@ -477,6 +486,10 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     __syncthreads();
 
     const uint32_t fo = (uint32_t)(L::frq - L::cum);
+    // whole four-value groups per store: rows, layers and both outputs aligned to the group
+    const uintptr_t galign = MODE == 2 ? 8 : 16;
+    const bool ovec = (d.C & 3) == 0 && (ols & 3) == 0 &&
+                      ((reinterpret_cast<uintptr_t>(out_k) | reinterpret_cast<uintptr_t>(out_v)) & (galign - 1)) == 0;
     const int warp = tid >> 5, lane = tid & 31;
     const int wrows = min(32, Tk - 32 * warp);  // rows of this decoder warp
     uint8_t *wtile = tile + warp * 32 * TS;
@@ -513,7 +526,7 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
             __syncwarp();
             if (wrows > 0)
                 write_window<P, MODE, 32>(wtile, s_unit, m1s + 32 * warp, d, kv, l, t0 + 32 * warp, wrows, c0, Wc,
-                                          sym, out_k, out_v, lane);
+                                          out_k, out_v, ols, ovec, lane);
             __syncwarp();  // the rows are read before the next window overwrites them
         } else if (V2) {
             if (i + 2 < nwin)  // records of window i + 2 replace window i's (its rows were built last round)
@@ -537,33 +550,32 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
 template <int P, int MODE, bool V2>
 cudaError_t launch_pm(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off, const uint32_t *len,
                       const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1, const Dims &d, const MaxTab &mt,
-                      uint8_t *sym, float *out_k, float *out_v, int32_t *status, cudaStream_t s) {
+                      void *out_k, void *out_v, long long ols, int32_t *status, cudaStream_t s) {
     const unsigned nslices = (unsigned)(2LL * d.L * d.nch);
     const int smem = (int)PipeSmem<P>::bytes;
     cudaError_t err = cudaFuncSetAttribute(k_decode_pipe<P, MODE, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            smem);
     if (err != cudaSuccess) return err;
     k_decode_pipe<P, MODE, V2><<<nslices, kThreads + kHelpers, smem, s>>>(
-        packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v, status);
+        packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols, status);
     return cudaGetLastError();
 }
 
 template <int P>
-cudaError_t launch_p(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
-                     const uint32_t *len, const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1,
-                     const Dims &d, const MaxTab &mt, int mode, uint8_t *sym, float *out_k, float *out_v,
-                     int32_t *status, cudaStream_t s) {
+cudaError_t launch_p(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off, const uint32_t *len,
+                     const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1, const Dims &d, const MaxTab &mt,
+                     int out_dtype, void *out_k, void *out_v, long long ols, int32_t *status, cudaStream_t s) {
     if (rec) {
-        if (mode == 1)
-            return launch_pm<P, 1, true>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v,
+        if (out_dtype == 2)
+            return launch_pm<P, 2, true>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols,
                                          status, s);
-        return launch_pm<P, 0, true>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v,
+        return launch_pm<P, 1, true>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols,
                                      status, s);
     }
-    if (mode == 1)
-        return launch_pm<P, 1, false>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v,
+    if (out_dtype == 2)
+        return launch_pm<P, 2, false>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols,
                                       status, s);
-    return launch_pm<P, 0, false>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, sym, out_k, out_v, status,
+    return launch_pm<P, 1, false>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols, status,
                                   s);
 }
 
@@ -574,29 +586,32 @@ cudaError_t launch_decode(const uint8_t *packed, uint64_t packed_bytes, const ui
                           const Dims &d, const MaxTab &mt, int mode, uint8_t *sym, float *out_k,
                           float *out_v, int32_t *status, cudaStream_t s) {
     const int tmax = d.Tc < d.T ? d.Tc : d.T;
-    if (tmax > kThreads)
+    if (tmax > kThreads || mode == 0)  // symbols out (the step API) or long chunks: one thread per stream
         return launch_decode_generic(packed, packed_bytes, off, len, cdf, max1, d, mt, mode, sym, out_k,
                                      out_v, status, s);
-    return launch_decode_pipe(packed, packed_bytes, off, len, cdf, nullptr, max1, d, mt, mode, sym, out_k, out_v,
-                              status, s);
+    return launch_decode_pipe(packed, packed_bytes, off, len, cdf, nullptr, max1, d, mt, 1, out_k, out_v,
+                              (long long)d.T * d.C, status, s);
 }
 
 cudaError_t launch_decode_pipe(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
                                const uint32_t *len, const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1,
-                               const Dims &d, const MaxTab &mt, int mode, uint8_t *sym, float *out_k, float *out_v,
-                               int32_t *status, cudaStream_t s) {
+                               const Dims &d, const MaxTab &mt, int out_dtype, void *out_k, void *out_v,
+                               long long ols, int32_t *status, cudaStream_t s) {
     int A = d.A[0] > d.A[1] ? d.A[0] : d.A[1];
     if (rec) {  // format 2: the largest layer alphabet, 2 * MAX + 1
         A = 0;
         for (int kv = 0; kv < 2; kv++)
             for (int l = 0; l < d.L; l++) A = 2 * mt.v[kv][l] + 1 > A ? 2 * mt.v[kv][l] + 1 : A;
     }
-    if (A <= 8) return launch_p<8>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 16) return launch_p<16>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 32) return launch_p<32>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 64) return launch_p<64>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    if (A <= 128) return launch_p<128>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
-    return launch_p<256>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, mode, sym, out_k, out_v, status, s);
+#define CG_LAUNCH_P(PP) \
+    return launch_p<PP>(packed, packed_bytes, off, len, cdf, rec, max1, d, mt, out_dtype, out_k, out_v, ols, status, s)
+    if (A <= 8) CG_LAUNCH_P(8);
+    if (A <= 16) CG_LAUNCH_P(16);
+    if (A <= 32) CG_LAUNCH_P(32);
+    if (A <= 64) CG_LAUNCH_P(64);
+    if (A <= 128) CG_LAUNCH_P(128);
+    CG_LAUNCH_P(256);
+#undef CG_LAUNCH_P
 }
 
 }  // namespace cg

@@ -106,6 +106,28 @@ def test_null_and_misaligned_pointers_rejected(lib):
                                  ws, 1 << 40, None, None) == 1  # off is required
 
 
+def test_serving_layout_arguments_rejected(lib):
+    """cg_decompress_chunk_ex rejects, before touching the device: unknown
+    format or output type, a layer stride below T*C, chunks over 256 tokens,
+    outputs not aligned to their element size."""
+    s = _shape(2, 64, 64, 64)
+    b, pb = _b([16, 16])
+    fake = C.c_void_p(0x1000)
+    odd = C.c_void_p(0x1001)
+    ls = 64 * 64
+
+    def call(shape, fmt, dtype, ok, ov, stride):
+        return lib.cg_decompress_chunk_ex(fake, 10, fake, fake, fake, fake, C.byref(shape), pb, None, fmt, dtype,
+                                          ok, ov, stride, None, None)
+    assert call(s, 3, 0, fake, fake, ls) == 1
+    assert call(s, 1, 2, fake, fake, ls) == 1
+    assert call(s, 2, 1, fake, fake, ls - 1) == 1
+    assert call(_shape(2, 600, 64, 300), 1, 0, fake, fake, 600 * 64) == 1
+    assert call(s, 1, 1, odd, fake, ls) == 1
+    assert call(s, 2, 0, fake, C.c_void_p(0x1002), ls) == 1
+    assert call(s, 1, 0, None, fake, ls) == 1
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     from kv_cache_compression_cg_gb300 import capi
     monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "missing.so"))
