@@ -81,6 +81,12 @@ def lib() -> C.CDLL:
                 "orc_compress_v2": (C.c_int, [p, p, C.c_int, C.c_int, C.c_int, C.c_int, i64,
                                               p, p, p, p, p, u64, p, p]),
                 "orc_decompress_v2": (C.c_int, [p, p, p, p, p] + [C.c_int] * 4 + [p, p, p, p]),
+                "orc_half_up": (C.c_uint16, [C.c_float]),
+                "orc_floats_to_half": (None, [p, i64, p]),
+                "orc_quantize_delta": (C.c_int, [p, p] + [C.c_int] * 5 + [i64, p, p, p, p]),
+                "orc_dequantize_delta": (C.c_int, [p, p] + [C.c_int] * 5 + [p, p, p, p]),
+                "orc_compress_ex": (C.c_int, [p, p] + [C.c_int] * 6 + [i64, p, p, p, p, p, u64, p, p]),
+                "orc_decompress_ex": (C.c_int, [p, p, p, p, p] + [C.c_int] * 6 + [p, p, p, p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -416,4 +422,92 @@ def dequantize_half(sym, max1, bins_k, bins_v=None):
     out_v = np.empty((L, T, C_), np.uint16)
     _check(lib().orc_dequantize_half(_ptr(sym), _ptr(np.ascontiguousarray(max1, np.uint16)), L, T, C_,
                                      _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)), "dequantize_half")
+    return out_k, out_v
+
+
+# ----------------------------------------------------------------------------
+# token-locality delta (specification G)
+# ----------------------------------------------------------------------------
+def half_up(m: float) -> int:
+    """The smallest binary16 value >= m, as bits (65504's bits above it)."""
+    return int(lib().orc_half_up(float(np.float32(m))))
+
+
+def floats_to_half(x) -> np.ndarray:
+    """binary32 array -> binary16 bits (uint16), round to nearest-even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().orc_floats_to_half(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def quantize_delta(k, v, Tc: int, G: int, bins_k, bins_v=None):
+    """QA + QD: symbols [2][L][T][C] and max1 [2][L][T] (fp16 bits)."""
+    k, v = _bits(k), _bits(v)
+    L, T, C_ = k.shape
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    sym = np.empty((2, L, T, C_), np.uint8)
+    max1 = np.empty((2, L, T), np.uint16)
+    _check(lib().orc_quantize_delta(_ptr(k), _ptr(v), L, T, C_, Tc, G, T * C_, _ptr(bk), _ptr(bv),
+                                    _ptr(sym), _ptr(max1)), "quantize_delta")
+    return sym, max1
+
+
+def dequantize_delta(sym, max1, Tc: int, G: int, bins_k, bins_v=None):
+    """D on anchors, DD elsewhere: binary32 K, V [L][T][C]."""
+    sym = np.ascontiguousarray(sym, dtype=np.uint8)
+    _, L, T, C_ = sym.shape
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    out_k = np.empty((L, T, C_), np.float32)
+    out_v = np.empty((L, T, C_), np.float32)
+    _check(lib().orc_dequantize_delta(_ptr(sym), _ptr(np.ascontiguousarray(max1, np.uint16)), L, T, C_,
+                                      Tc, G, _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)),
+           "dequantize_delta")
+    return out_k, out_v
+
+
+def compress_ex(k, v, Tc: int, bins_k, bins_v=None, fmt: int = 1, group: int = 1):
+    """Quantise with token groups of `group` (1: plain) and code in format
+    `fmt`. Returns max1, side ("cdf" or "rec"), packed, len, off."""
+    k, v = _bits(k), _bits(v)
+    L, T, C_ = k.shape
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    ns = num_streams(L, T)
+    cap = max_compressed_bytes(L, T, C_)
+    max1 = np.empty((2, L, T), np.uint16)
+    if fmt == 1:
+        side = np.empty(max(cdf_elems(L, T, C_, Tc, alphabet(bk), alphabet(bv)), 1), np.uint16)
+    else:
+        side = np.zeros(max(rec_bytes(L, T, C_, Tc, bk, bv), 1), np.uint8)
+    packed = np.zeros(max(cap, 1), np.uint8)
+    ln = np.empty(max(ns, 1), np.uint32)
+    off = np.empty(ns + 1, np.uint64)
+    _check(lib().orc_compress_ex(_ptr(k), _ptr(v), L, T, C_, Tc, group, fmt, T * C_, _ptr(bk), _ptr(bv),
+                                 _ptr(max1), _ptr(side), _ptr(packed), cap, _ptr(ln), _ptr(off)),
+           "compress_ex")
+    n_side = cdf_elems(L, T, C_, Tc, alphabet(bk), alphabet(bv)) if fmt == 1 else rec_bytes(L, T, C_, Tc, bk, bv)
+    return {"max1": max1, "cdf" if fmt == 1 else "rec": side[:n_side].copy(),
+            "packed": packed[:int(off[-1])].copy(), "len": ln[:ns], "off": off}
+
+
+def decompress_ex(packed, off, ln, side, max1, L, T, C_, Tc, bins_k, bins_v=None, fmt: int = 1,
+                  group: int = 1):
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    if packed.size == 0:
+        packed = np.zeros(1, np.uint8)
+    side = np.ascontiguousarray(side, dtype=np.uint16 if fmt == 1 else np.uint8)
+    if side.size == 0:
+        side = np.zeros(1, side.dtype)
+    out_k = np.empty((L, T, C_), np.float32)
+    out_v = np.empty((L, T, C_), np.float32)
+    _check(lib().orc_decompress_ex(_ptr(packed), _ptr(np.ascontiguousarray(off, np.uint64)),
+                                   _ptr(np.ascontiguousarray(ln, np.uint32)), _ptr(side),
+                                   _ptr(np.ascontiguousarray(max1, np.uint16)),
+                                   L, T, C_, Tc, group, fmt, _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)),
+           "decompress_ex")
     return out_k, out_v

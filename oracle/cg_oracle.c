@@ -579,29 +579,23 @@ int orc_cdf_from_counts_mode(const uint32_t *n, int A, uint32_t Tk, int mode,
 /* [CG §2.3(1)-(3), §1.2(3)] format 2: quantise, count per (chunk, kv, layer,
  * channel), store the counts as records, build each CDF over the layer's own
  * alphabet and code the streams as in format 1. */
-int orc_compress_v2(const uint16_t *k, const uint16_t *v, int L, int T, int C,
-                    int Tc, int64_t layer_stride, const int32_t *bins_k,
-                    const int32_t *bins_v, uint16_t *max1, uint8_t *rec,
-                    uint8_t *packed, uint64_t capacity, uint32_t *len,
-                    uint64_t *off)
+/* Format 2 coding of given symbols: counts -> records and CDFs -> streams. */
+static int orc_code_v2(const uint8_t *sym, int L, int T, int C, int Tc,
+                       const int32_t *bins_k, const int32_t *bins_v,
+                       uint8_t *rec, uint8_t *packed, uint64_t capacity,
+                       uint32_t *len, uint64_t *off)
 {
-    if (!orc_check_shape(L, T, C) || Tc < 1 || Tc > 256)
-        return ORC_ERR_ARG;
-    if (!bins_v)
-        bins_v = bins_k;
-    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
     uint16_t *rows = (uint16_t *)malloc((size_t)C * 256 * sizeof(uint16_t));
     int64_t cap1 = 2 * (int64_t)C + 8;
     uint8_t *buf = (uint8_t *)malloc((size_t)cap1);
-    if (!sym || !rows || !buf) {
-        free(sym), free(rows), free(buf);
+    if (!rows || !buf) {
+        free(rows), free(buf);
         return ORC_ERR_NOMEM;
     }
-    int status = orc_quantize(k, v, L, T, C, layer_stride, bins_k, bins_v, sym,
-                              max1);
+    int status = ORC_OK;
     int nch = (T + Tc - 1) / Tc;
     uint64_t total = 0;
-    for (int kc = 0; kc < nch && status != ORC_ERR_NONFINITE && status != ORC_ERR_ARG; kc++) {
+    for (int kc = 0; kc < nch; kc++) {
         int Tk = orc_chunk_tokens(T, Tc, kc);
         for (int kv = 0; kv < 2; kv++) {
             const int32_t *bins = kv ? bins_v : bins_k;
@@ -620,7 +614,7 @@ int orc_compress_v2(const uint16_t *k, const uint16_t *v, int L, int T, int C,
                         st = orc_cdf_from_counts_mode(n, A, (uint32_t)Tk, r[0],
                                                       rows + (int64_t)c * A);
                     if (st != ORC_OK) {
-                        free(sym), free(rows), free(buf);
+                        free(rows), free(buf);
                         return st;
                     }
                 }
@@ -631,7 +625,7 @@ int orc_compress_v2(const uint16_t *k, const uint16_t *v, int L, int T, int C,
                     const uint8_t *s = sym + (((int64_t)kv * L + l) * T + t) * C;
                     int64_t n = orc_encode_stream(s, C, rows, A, A, buf, cap1);
                     if (n < 0) {
-                        free(sym), free(rows), free(buf);
+                        free(rows), free(buf);
                         return ORC_ERR_ARG;
                     }
                     off[sid] = total;
@@ -648,28 +642,30 @@ int orc_compress_v2(const uint16_t *k, const uint16_t *v, int L, int T, int C,
             }
         }
     }
-    if (status == ORC_OK || status == ORC_ERR_CAPACITY)
-        off[orc_num_streams(L, T)] = total;
-    free(sym), free(rows), free(buf);
+    off[orc_num_streams(L, T)] = total;
+    free(rows), free(buf);
     return status;
 }
 
-int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
-                      const uint32_t *len, const uint8_t *rec,
-                      const uint16_t *max1, int L, int T, int C, int Tc,
-                      const int32_t *bins_k, const int32_t *bins_v,
-                      float *out_k, float *out_v)
+int orc_compress_v2(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                    int Tc, int64_t layer_stride, const int32_t *bins_k,
+                    const int32_t *bins_v, uint16_t *max1, uint8_t *rec,
+                    uint8_t *packed, uint64_t capacity, uint32_t *len,
+                    uint64_t *off)
 {
-    if (!orc_check_shape(L, T, C) || Tc < 1 || Tc > 256)
-        return ORC_ERR_ARG;
-    if (!bins_v)
-        bins_v = bins_k;
-    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
+    return orc_compress_ex(k, v, L, T, C, Tc, 1, 2, layer_stride, bins_k,
+                           bins_v, max1, rec, packed, capacity, len, off);
+}
+
+/* Format 2 decoding: records -> CDFs -> symbols [2][L][T][C]. */
+static int orc_decode_v2(const uint8_t *packed, const uint64_t *off,
+                         const uint32_t *len, const uint8_t *rec, int L, int T,
+                         int C, int Tc, const int32_t *bins_k,
+                         const int32_t *bins_v, uint8_t *sym)
+{
     uint16_t *rows = (uint16_t *)malloc((size_t)C * 256 * sizeof(uint16_t));
-    if (!sym || !rows) {
-        free(sym), free(rows);
+    if (!rows)
         return ORC_ERR_NOMEM;
-    }
     int status = ORC_OK;
     int nch = (T + Tc - 1) / Tc;
     for (int kc = 0; kc < nch; kc++) {
@@ -686,7 +682,7 @@ int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
                         st = orc_cdf_from_counts_mode(n, A, (uint32_t)Tk, r[0],
                                                       rows + (int64_t)c * A);
                     if (st != ORC_OK) {
-                        free(sym), free(rows);
+                        free(rows);
                         return st;
                     }
                 }
@@ -703,10 +699,18 @@ int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
             }
         }
     }
-    if (status == ORC_OK)
-        status = orc_dequantize(sym, max1, L, T, C, bins_k, bins_v, out_k, out_v);
-    free(sym), free(rows);
+    free(rows);
     return status;
+}
+
+int orc_decompress_v2(const uint8_t *packed, const uint64_t *off,
+                      const uint32_t *len, const uint8_t *rec,
+                      const uint16_t *max1, int L, int T, int C, int Tc,
+                      const int32_t *bins_k, const int32_t *bins_v,
+                      float *out_k, float *out_v)
+{
+    return orc_decompress_ex(packed, off, len, rec, max1, L, T, C, Tc, 1, 2,
+                             bins_k, bins_v, out_k, out_v);
 }
 
 /* ---- serving layouts: binary16 output ---------------------------------- */
@@ -773,4 +777,186 @@ int orc_dequantize_half(const uint8_t *sym, const uint16_t *max1, int L, int T,
             }
     }
     return ORC_OK;
+}
+
+/* ---- token-locality delta (specification G) ------------------------------ */
+
+uint16_t orc_half_up(float m)
+{
+    if (!(m <= 65504.0f))
+        return 0x7BFFu; /* above the largest finite binary16 */
+    uint16_t h = orc_float_to_half(m); /* nearest; at most one step below m */
+    if (h >= 0x7C00u)
+        return 0x7BFFu;
+    if (orc_half_to_float(h) < m)
+        h++; /* the next binary16 up (positive values order like their bits) */
+    return h;
+}
+
+void orc_floats_to_half(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = orc_float_to_half(x[i]);
+}
+
+/* [CG §1.2(1)] QD: one non-anchor row, given its anchor's reconstruction. */
+static int orc_quantize_delta_row(const uint16_t *x, const float *anchor, int C,
+                                  int bins, float *d, uint8_t *q,
+                                  uint16_t *max1_out)
+{
+    int MAX = bins / 2 - 1;
+    float m = 0.0f;
+    for (int c = 0; c < C; c++) {
+        float xv = orc_half_to_float(x[c]);
+        if (!isfinite(xv))
+            return ORC_ERR_NONFINITE;
+        d[c] = xv - anchor[c];
+        if (fabsf(d[c]) > m)
+            m = fabsf(d[c]);
+    }
+    uint16_t max1 = m == 0.0f ? 0 : orc_half_up(m);
+    *max1_out = max1;
+    if (max1 == 0) {
+        for (int c = 0; c < C; c++)
+            q[c] = (uint8_t)MAX;
+        return ORC_OK;
+    }
+    float factor = (float)MAX / orc_half_to_float(max1);
+    for (int c = 0; c < C; c++) {
+        float scaled = d[c] * factor;
+        float y = scaled + (float)MAX;
+        float r = rintf(y);
+        if (r < 0.0f)
+            r = 0.0f;
+        if (r > (float)(2 * MAX))
+            r = (float)(2 * MAX);
+        q[c] = (uint8_t)r;
+    }
+    return ORC_OK;
+}
+
+int orc_quantize_delta(const uint16_t *k, const uint16_t *v, int L, int T,
+                       int C, int Tc, int G, int64_t layer_stride,
+                       const int32_t *bins_k, const int32_t *bins_v,
+                       uint8_t *sym, uint16_t *max1)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1 || G < 1)
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    float *anchor = (float *)malloc((size_t)C * sizeof(float));
+    float *d = (float *)malloc((size_t)C * sizeof(float));
+    if (!anchor || !d) {
+        free(anchor), free(d);
+        return ORC_ERR_NOMEM;
+    }
+    int st = ORC_OK;
+    for (int kv = 0; kv < 2 && st == ORC_OK; kv++) {
+        const uint16_t *x = kv ? v : k;
+        const int32_t *bins = kv ? bins_v : bins_k;
+        for (int l = 0; l < L && st == ORC_OK; l++) {
+            if (bins[l] < 4 || bins[l] > 256) {
+                st = ORC_ERR_ARG;
+                break;
+            }
+            for (int t = 0; t < T && st == ORC_OK; t++) {
+                int64_t g = ((int64_t)kv * L + l) * T + t;
+                const uint16_t *row = x + (int64_t)l * layer_stride + (int64_t)t * C;
+                int tl = t % Tc; /* position in the chunk */
+                if (tl % G == 0) {
+                    st = orc_quantize_group(row, C, bins[l], sym + g * C, max1 + g);
+                    for (int c = 0; c < C && st == ORC_OK; c++)
+                        anchor[c] = orc_dequantize_value(sym[g * C + c], bins[l], max1[g]);
+                } else {
+                    st = orc_quantize_delta_row(row, anchor, C, bins[l], d, sym + g * C,
+                                                max1 + g);
+                }
+            }
+        }
+    }
+    free(anchor), free(d);
+    return st;
+}
+
+int orc_dequantize_delta(const uint8_t *sym, const uint16_t *max1, int L,
+                         int T, int C, int Tc, int G, const int32_t *bins_k,
+                         const int32_t *bins_v, float *out_k, float *out_v)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1 || G < 1)
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    for (int kv = 0; kv < 2; kv++) {
+        float *out = kv ? out_v : out_k;
+        const int32_t *bins = kv ? bins_v : bins_k;
+        for (int l = 0; l < L; l++)
+            for (int t = 0; t < T; t++) {
+                int64_t g = ((int64_t)kv * L + l) * T + t;
+                int tl = t % Tc;
+                int64_t a = g - tl % G; /* the anchor's row */
+                for (int c = 0; c < C; c++) {
+                    float x = orc_dequantize_value(sym[g * C + c], bins[l], max1[g]);
+                    if (a != g)
+                        x = orc_dequantize_value(sym[a * C + c], bins[l], max1[a]) + x;
+                    out[((int64_t)l * T + t) * C + c] = x;
+                }
+            }
+    }
+    return ORC_OK;
+}
+
+int orc_compress_ex(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                    int Tc, int G, int fmt, int64_t layer_stride,
+                    const int32_t *bins_k, const int32_t *bins_v,
+                    uint16_t *max1, void *side, uint8_t *packed,
+                    uint64_t capacity, uint32_t *len, uint64_t *off)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1 || G < 1 || (fmt != 1 && fmt != 2) ||
+        (fmt == 2 && Tc > 256))
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
+    if (!sym)
+        return ORC_ERR_NOMEM;
+    int st = orc_quantize_delta(k, v, L, T, C, Tc, G, layer_stride, bins_k, bins_v, sym, max1);
+    if (st == ORC_OK && fmt == 1) {
+        int A_k = orc_alphabet(bins_k, L), A_v = orc_alphabet(bins_v, L);
+        st = orc_calculate_cdf(sym, L, T, C, Tc, A_k, A_v, (uint16_t *)side);
+        if (st == ORC_OK)
+            st = orc_encode(sym, (const uint16_t *)side, L, T, C, Tc, A_k, A_v, packed,
+                            capacity, len, off);
+    } else if (st == ORC_OK) {
+        st = orc_code_v2(sym, L, T, C, Tc, bins_k, bins_v, (uint8_t *)side, packed, capacity,
+                         len, off);
+    }
+    free(sym);
+    return st;
+}
+
+int orc_decompress_ex(const uint8_t *packed, const uint64_t *off,
+                      const uint32_t *len, const void *side,
+                      const uint16_t *max1, int L, int T, int C, int Tc, int G,
+                      int fmt, const int32_t *bins_k, const int32_t *bins_v,
+                      float *out_k, float *out_v)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1 || G < 1 || (fmt != 1 && fmt != 2) ||
+        (fmt == 2 && Tc > 256))
+        return ORC_ERR_ARG;
+    if (!bins_v)
+        bins_v = bins_k;
+    uint8_t *sym = (uint8_t *)malloc((size_t)(2 * (int64_t)L * T * C));
+    if (!sym)
+        return ORC_ERR_NOMEM;
+    int st;
+    if (fmt == 1)
+        st = orc_decode(packed, off, len, (const uint16_t *)side, L, T, C, Tc,
+                        orc_alphabet(bins_k, L), orc_alphabet(bins_v, L), sym);
+    else
+        st = orc_decode_v2(packed, off, len, (const uint8_t *)side, L, T, C, Tc, bins_k,
+                           bins_v, sym);
+    if (st == ORC_OK)
+        st = orc_dequantize_delta(sym, max1, L, T, C, Tc, G, bins_k, bins_v, out_k, out_v);
+    free(sym);
+    return st;
 }

@@ -83,6 +83,29 @@
  *    then V likewise }.
  * F2 (CDF) F over the layer's A symbols, the remainder going to the record's
  *    mode byte.
+ *
+ * ---------------------------------------------------------------------------
+ * Token-locality delta: the change-based encoding of [CG §1.2(1)]
+ * ---------------------------------------------------------------------------
+ * The page's design codes each token's change from a nearby token rather than
+ * its raw values, since neighbouring tokens' K/V are similar [CG §1.2(1)];
+ * LMCache's code skips this step [CG §2.3(1)]. The page gives no group size,
+ * anchor rule or precision; this specification reads it as follows. It
+ * changes Q and D only (F, F2, S, R and P see symbols as before), so it
+ * applies to either format. Group size G >= 1; G = 1 is plain Q and D.
+ *
+ * G  (groups) within chunk k the tokens tl = 0..Tc_k-1 form groups of G
+ *    consecutive tokens from tl = 0; the first token of each group
+ *    (tl % G == 0) is the group's anchor.
+ * QA (anchor rows) exactly Q. The anchor's reconstruction is
+ *    a^_c = D(q_a,c, max1_a), binary32, as the decoder will see it.
+ * QD (other rows) d_c = x_c - a^_c (binary32, rounded once); m = max_c |d_c|;
+ *    max1 = the smallest binary16 value >= m (stored as fp16; the largest
+ *    finite binary16, 65504, if m exceeds it); then Q's steps on d with this
+ *    max1: factor = (float)MAX / max1, y = (d * factor) + (float)MAX,
+ *    q = rint(y) clamped to [0, 2*MAX]; max1 == 0 gives q = MAX.
+ * DD (other rows) x^_c = a^_c + D(q_c, max1) (binary32, the sum rounded
+ *    once); anchor rows are D. A binary16 output rounds x^ to nearest-even.
  */
 #ifndef CG_ORACLE_H
 #define CG_ORACLE_H
@@ -209,6 +232,35 @@ uint16_t orc_float_to_half(float x);
 int orc_dequantize_half(const uint8_t *sym, const uint16_t *max1, int L, int T,
                         int C, const int32_t *bins_k, const int32_t *bins_v,
                         uint16_t *out_k, uint16_t *out_v);
+
+/* ---- token-locality delta (specification G) ------------------------------ */
+/* The smallest binary16 value >= m (m finite, >= 0), as bits; 0x7BFF (the
+ * largest finite binary16) when m > 65504. */
+uint16_t orc_half_up(float m);
+/* binary32 -> binary16 (round to nearest-even) over n values. */
+void orc_floats_to_half(const float *x, int64_t n, uint16_t *out);
+/* QA + QD over the whole tensor: symbols [2][L][T][C], max1 [2][L][T]. */
+int orc_quantize_delta(const uint16_t *k, const uint16_t *v, int L, int T,
+                       int C, int Tc, int G, int64_t layer_stride,
+                       const int32_t *bins_k, const int32_t *bins_v,
+                       uint8_t *sym, uint16_t *max1);
+/* D on anchors, DD on the other rows; binary32 output [L][T][C]. */
+int orc_dequantize_delta(const uint8_t *sym, const uint16_t *max1, int L,
+                         int T, int C, int Tc, int G, const int32_t *bins_k,
+                         const int32_t *bins_v, float *out_k, float *out_v);
+/* Quantise with groups of G tokens (G = 1: plain Q) and code in format fmt
+ * (1: side = uint16 CDF entries, 2: side = uint8 count records). */
+int orc_compress_ex(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                    int Tc, int G, int fmt, int64_t layer_stride,
+                    const int32_t *bins_k, const int32_t *bins_v,
+                    uint16_t *max1, void *side, uint8_t *packed,
+                    uint64_t capacity, uint32_t *len, uint64_t *off);
+/* The inverse of orc_compress_ex, binary32 output. */
+int orc_decompress_ex(const uint8_t *packed, const uint64_t *off,
+                      const uint32_t *len, const void *side,
+                      const uint16_t *max1, int L, int T, int C, int Tc, int G,
+                      int fmt, const int32_t *bins_k, const int32_t *bins_v,
+                      float *out_k, float *out_v);
 
 #ifdef __cplusplus
 }
