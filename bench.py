@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--piece-chunks", type=int, default=2,
                     help="chunks per piece of the streamed end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--group", type=int, default=1,
+                    help="token-locality delta group size (1: none, the page's LMCache code path)")
     return ap.parse_args()
 
 
@@ -164,12 +166,16 @@ def workload_config(w, extra=None):
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, single thread, on a bounded sample
 # ---------------------------------------------------------------------------
-def oracle_step_time(k, v, w, tokens, fmt=2):
+def oracle_step_time(k, v, w, tokens, fmt=2, group=1):
     import oracle
     ks = k[:, :tokens].copy()
     vs = v[:, :tokens].copy()
     t0 = time.perf_counter()
-    if fmt == 2:
+    if group > 1:
+        r = oracle.compress_ex(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v, fmt=fmt, group=group)
+        oracle.decompress_ex(r["packed"], r["off"], r["len"], r["cdf" if fmt == 1 else "rec"], r["max1"], w.L,
+                             tokens, w.C, w.chunk_tokens, w.bins_k, w.bins_v, fmt=fmt, group=group)
+    elif fmt == 2:
         r = oracle.compress_v2(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v)
         oracle.decompress_v2(r["packed"], r["off"], r["len"], r["rec"], r["max1"], w.L, tokens, w.C,
                              w.chunk_tokens, w.bins_k, w.bins_v)
@@ -192,11 +198,11 @@ def run_reference(args):
     tokens = min(w.T, w.chunk_tokens)
     k, v = synth.generate(w, T=tokens)
     for _ in range(args.warmup):
-        oracle_step_time(k, v, w, tokens, args.format)
+        oracle_step_time(k, v, w, tokens, args.format, args.group)
     times = []
     nbytes = 0
     for _ in range(args.steps):
-        dt, nbytes = oracle_step_time(k, v, w, tokens, args.format)
+        dt, nbytes = oracle_step_time(k, v, w, tokens, args.format, args.group)
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = nbytes / (ms * 1e-3) / 1e9
@@ -205,7 +211,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(w, {"sample": sample, "format": args.format}),
+        "config": workload_config(w, {"sample": sample, "format": args.format, "delta_group": args.group}),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
@@ -242,7 +248,8 @@ def run_ours(args):
     v_pin.copy_(v)
     k_h, v_h = k_pin.numpy(), v_pin.numpy()
     stream = torch.cuda.current_stream()
-    cd = codec.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens, fmt=args.format)
+    cd = codec.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens, fmt=args.format,
+                     group=args.group)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
 
     def step():
@@ -255,6 +262,10 @@ def run_ours(args):
     out = cd.out
     total = out.total_bytes()
     status = int(out.status.item()) | int(cd.dstatus.item())
+    # reconstruction error of the output (reported, outside any timed region)
+    rk, rv = cd.decompress()
+    rel_rmse = {name: float((((o - x.float()) ** 2).mean() / (x.float() ** 2).mean()).sqrt())
+                for name, o, x in (("k", rk, k), ("v", rv, v))}
 
     # timed region
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
@@ -318,7 +329,7 @@ def run_ours(args):
         "compress": ("k_compress_tma (quantise + CDF + encode + pack)", comp_kernel_ms,
                      alg_ops_encode(), comp_alg_bytes, ["compress.cu", "coder.cuh", "cg_internal.cuh"]),
         "decompress": ("k_decode_pipe (decode + dequantise)", dec_kernel_ms,
-                       alg_ops_decode(P), dec_alg_bytes, ["decode.cu", "cg_internal.cuh"]),
+                       alg_ops_decode(P), dec_alg_bytes, ["decode_pipe.cuh", "decode.cu", "cg_internal.cuh"]),
     }
     dom = "compress" if comp_kernel_ms >= dec_kernel_ms else "decompress"
     kname, kms, ops, kbytes, srcs = kern[dom]
@@ -342,7 +353,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": workload_config(w, {"parallelism": f"chunk-sharded x{world}" if world > 1 else "1 GPU",
-                                      "format": args.format}),
+                                      "format": args.format, "delta_group": args.group}),
         "compress_gbs": comp_gbs, "decompress_gbs": dec_gbs,
         "compress_ms": statistics.mean(comp_ms), "decompress_ms": statistics.mean(dec_ms),
         "compress_frac_of_hbm": {"fp16_in": comp_gbs / hbm,
@@ -352,6 +363,7 @@ def run_ours(args):
         "compression_ratio": {"total": fp16_bytes / (total + side), "payload": fp16_bytes / total,
                               "bits_per_symbol": 8 * total / n_el},
         "roofline": roofline,
+        "reconstruction_rel_rmse": rel_rmse,
         "status_word": status, "clocks": clocks, "wall_s_timed_region": wall,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
     }
@@ -359,11 +371,11 @@ def run_ours(args):
     if not args.no_e2e:
         result["e2e"] = e2e(args, w, cd, k_pin, v_pin, fp16_bytes)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens), args.format)
+        cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens), args.format, args.group)
         reps = max(1, int(10.0 / max(cpu_dt, 1e-3)))
         times = [cpu_dt]
         for _ in range(min(reps, 20) - 1):
-            times.append(oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens), args.format)[0])
+            times.append(oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens), args.format, args.group)[0])
         cpu_gbs = cpu_bytes / statistics.mean(times) / 1e9
         result["cpu_baseline"] = {
             "value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -386,7 +398,7 @@ def e2e(args, w, cd, k_pin, v_pin, fp16_bytes):
     import torch
     from kv_cache_compression_cg_gb300.stream import StreamingCodec
     sc = StreamingCodec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens, fmt=args.format,
-                        piece_chunks=args.piece_chunks)
+                        piece_chunks=args.piece_chunks, group=args.group)
     times = []
     pieces = outs = None
     for i in range(max(args.warmup, 3) + args.steps):

@@ -277,20 +277,70 @@ cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes,
 #define CG_OUT_F16 1
 
 /* Decode fused with dequantisation, either format (format 1: side = uint16
- * CDF entries; format 2: side = uint8 count records), into out_k / out_v
- * [L][T][C] of out_dtype with layers out_layer_stride elements apart
- * (>= T*C; tokens C apart, channels contiguous). Requires chunk_tokens <= 256.
- * Status bits as cg_decompress_chunk / cg_decompress_chunk_v2. */
+ * CDF entries; format 2: side = uint8 count records) and token-locality delta
+ * group (1: none; see below), into out_k / out_v [L][T][C] of out_dtype with
+ * layers out_layer_stride elements apart (>= T*C; tokens C apart, channels
+ * contiguous). Requires chunk_tokens <= 256. Status bits as
+ * cg_decompress_chunk / cg_decompress_chunk_v2. */
 cg_status cg_decompress_chunk_ex(const uint8_t *packed, uint64_t packed_bytes,
                                  const uint64_t *off, const uint32_t *len,
                                  const void *side, const uint16_t *max1,
                                  const cg_shape *shape, const int32_t *bins_k,
                                  const int32_t *bins_v, int format,
-                                 int out_dtype, void *out_k, void *out_v,
-                                 int64_t out_layer_stride, int32_t *status,
-                                 cudaStream_t stream);
+                                 int32_t group, int out_dtype, void *out_k,
+                                 void *out_v, int64_t out_layer_stride,
+                                 int32_t *status, cudaStream_t stream);
 
-/* Library version string ("cachegen-gb300 <format> <build>"). */
+/* ---- token-locality delta ------------------------------------------------
+ * The page's design codes each token's change from a nearby token, since
+ * neighbouring tokens' K/V are similar [CG §1.2(1)] (LMCache's code skips
+ * this step, [CG §2.3(1)]). Read here as follows; it changes Q and D only
+ * (F, S, F2, R, P code the symbols as before), for either format, with a
+ * group size G >= 1 (G = 1: plain Q and D; G <= CG_MAX_CHUNK_TOKENS):
+ *
+ * G  within chunk k the tokens tl = 0..Tc_k-1 form groups of G consecutive
+ *    tokens from tl = 0; the first of each group (tl % G == 0) is its anchor.
+ * QA anchor rows: Q. The anchor's reconstruction a^_c = D(q_a,c, max1_a).
+ * QD other rows: d_c = x_c - a^_c (binary32); max1 = the smallest binary16
+ *    value >= max_c |d_c| (65504 when above it); q = Q's steps on d with that
+ *    max1, clamped to [0, 2*MAX] (max1 == 0: q = MAX).
+ * DD other rows: x^_c = a^_c + D(q_c, max1) in binary32; anchors: D. The
+ *    binary16 output of cg_decompress_chunk_ex rounds x^ to nearest-even.
+ * The decoder needs nothing beyond G: the anchors' symbols and max1 are in
+ * the chunk.
+ */
+
+/* QA + QD over the whole tensor: outputs as cg_quantize (sym, max1). */
+cg_status cg_quantize_delta(const uint16_t *k, const uint16_t *v,
+                            const cg_shape *shape, const int32_t *bins_k,
+                            const int32_t *bins_v, int32_t group, uint8_t *sym,
+                            uint16_t *max1, int32_t *status,
+                            cudaStream_t stream);
+
+/* D / DD: sym, max1 as from cg_quantize_delta with the same group ->
+ * binary32 out_k, out_v [L][T][C] contiguous (16-byte aligned). */
+cg_status cg_dequantize_delta(const uint8_t *sym, const uint16_t *max1,
+                              const cg_shape *shape, const int32_t *bins_k,
+                              const int32_t *bins_v, int32_t group,
+                              float *out_k, float *out_v, int32_t *status,
+                              cudaStream_t stream);
+
+/* Quantise (with the delta when group > 1) -> CDF or count records -> encode
+ * -> pack, either format: side = uint16 CDF entries (format 1,
+ * cg_cdf_elems) or uint8 count records (format 2, cg_record_bytes).
+ * Workspace: cg_compress_workspace_bytes. Format 2 has the limits of
+ * cg_compress_chunk_v2; format 1 takes any shape. Decode with
+ * cg_decompress_chunk_ex and the same format and group. */
+cg_status cg_compress_chunk_ex(const uint16_t *k, const uint16_t *v,
+                               const cg_shape *shape, const int32_t *bins_k,
+                               const int32_t *bins_v, int format,
+                               int32_t group, uint16_t *max1, void *side,
+                               uint8_t *packed, uint64_t capacity,
+                               uint32_t *len, uint64_t *off, void *workspace,
+                               uint64_t workspace_bytes, int32_t *status,
+                               cudaStream_t stream);
+
+/* Library version string ("cachegen-gb300 <formats> <options> <build>"). */
 const char *cg_version(void);
 
 #ifdef __cplusplus

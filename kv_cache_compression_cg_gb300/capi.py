@@ -55,8 +55,12 @@ SIGNATURES = {
     "cg_compress_chunk_v2": (_i32, [_p, _p, _SHAPE, _p, _p, _p, _p, _p, _u64, _p, _p, _p, _u64,
                                     _p, _p]),
     "cg_decompress_chunk_v2": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, _p, _p, _p, _p]),
-    "cg_decompress_chunk_ex": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, C.c_int, C.c_int, _p, _p,
-                                      C.c_int64, _p, _p]),
+    "cg_decompress_chunk_ex": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, C.c_int, C.c_int32, C.c_int,
+                                      _p, _p, C.c_int64, _p, _p]),
+    "cg_quantize_delta": (_i32, [_p, _p, _SHAPE, _p, _p, C.c_int32, _p, _p, _p, _p]),
+    "cg_dequantize_delta": (_i32, [_p, _p, _SHAPE, _p, _p, C.c_int32, _p, _p, _p, _p]),
+    "cg_compress_chunk_ex": (_i32, [_p, _p, _SHAPE, _p, _p, C.c_int, C.c_int32, _p, _p, _p, _u64, _p, _p, _p,
+                                    _u64, _p, _p]),
     "cg_version": (C.c_char_p, []),
 }
 

@@ -16,7 +16,7 @@ import torch
 from . import capi
 
 __all__ = ["Codec", "Compressed", "quantize", "calculate_cdf", "encode", "decode", "dequantize",
-           "compress_chunk", "decompress_chunk", "make_shape"]
+           "quantize_delta", "dequantize_delta", "compress_chunk", "decompress_chunk", "make_shape"]
 
 
 def _ptr(t: torch.Tensor | None):
@@ -74,6 +74,7 @@ class Compressed:
     status: torch.Tensor    # int32 [1]
     fmt: int = 1            # 1: CDF entries in `cdf`; 2: count records in `rec`
     rec: torch.Tensor | None = None  # uint8 [record bytes] (format 2)
+    group: int = 1          # token-locality delta group (1: none)
 
     @property
     def shape(self) -> capi.cg_shape:
@@ -91,10 +92,19 @@ class Codec:
     """
 
     def __init__(self, L: int, T: int, C_: int, bins_k, bins_v=None, chunk_tokens: int = 256,
-                 capacity: int | None = None, device: str | torch.device = "cuda", fmt: int = 1):
+                 capacity: int | None = None, device: str | torch.device = "cuda", fmt: int = 1,
+                 group: int = 1):
+        """fmt: 1 (CDF entries) or 2 (count records); group: token-locality
+        delta group size [CG §1.2(1)] (1: no delta; > 1 needs chunk_tokens
+        <= 256 to decode)."""
         if fmt not in (1, 2):
             raise ValueError("fmt must be 1 (CDF entries) or 2 (count records)")
+        if not 1 <= group <= 1024:
+            raise ValueError("group must be in [1, 1024]")
+        if group > 1 and chunk_tokens > 256:
+            raise ValueError("the delta decodes only chunks of at most 256 tokens")
         self.fmt = fmt
+        self.group = group
         self.L, self.T, self.C, self.chunk_tokens = L, T, C_, chunk_tokens
         self.bins_k = _bins(bins_k, L)
         self.bins_v = _bins(bins_k if bins_v is None else bins_v, L)
@@ -120,7 +130,8 @@ class Codec:
             len=torch.empty(max(self.nstreams, 1), dtype=torch.int32, device=dev),
             off=torch.empty(self.nstreams + 1, dtype=torch.int64, device=dev),
             status=torch.zeros(1, dtype=torch.int32, device=dev), fmt=fmt,
-            rec=torch.empty(max(self.rec_bytes, 1), dtype=torch.uint8, device=dev) if fmt == 2 else None)
+            rec=torch.empty(max(self.rec_bytes, 1), dtype=torch.uint8, device=dev) if fmt == 2 else None,
+            group=group)
         self.out_k = torch.empty((L, T, C_), dtype=torch.float32, device=dev)
         self.out_v = torch.empty((L, T, C_), dtype=torch.float32, device=dev)
         self.dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -130,6 +141,13 @@ class Codec:
         if (shp.L, shp.T, shp.C) != (self.L, self.T, self.C):
             raise ValueError("K/V shape differs from the codec's")
         o = self.out
+        if self.group > 1:
+            capi.check(capi.load().cg_compress_chunk_ex(
+                _ptr(k), _ptr(v), C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v), self.fmt, self.group,
+                _ptr(o.max1), _ptr(o.cdf if self.fmt == 1 else o.rec), _ptr(o.packed), self.capacity, _ptr(o.len),
+                _ptr(o.off), _ptr(self.workspace), self.ws_bytes, _ptr(o.status), _stream(stream)),
+                "cg_compress_chunk_ex")
+            return o
         if self.fmt == 2:
             capi.check(capi.load().cg_compress_chunk_v2(
                 _ptr(k), _ptr(v), C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v),
@@ -147,6 +165,9 @@ class Codec:
     def decompress(self, c: Compressed | None = None, stream=None):
         c = self.out if c is None else c
         shp = make_shape(c.L, c.T, c.C, c.chunk_tokens)
+        if c.group > 1:
+            self.decompress_into(self.out_k, self.out_v, c, stream)
+            return self.out_k, self.out_v
         if c.fmt == 2:
             capi.check(capi.load().cg_decompress_chunk_v2(
                 _ptr(c.packed), c.packed.numel(), _ptr(c.off), _ptr(c.len), _ptr(c.rec), _ptr(c.max1),
@@ -177,7 +198,7 @@ class Codec:
         side = c.cdf if c.fmt == 1 else c.rec
         capi.check(capi.load().cg_decompress_chunk_ex(
             _ptr(c.packed), c.packed.numel(), _ptr(c.off), _ptr(c.len), _ptr(side), _ptr(c.max1),
-            C.byref(shp), _np_ptr(c.bins_k), _np_ptr(c.bins_v), c.fmt,
+            C.byref(shp), _np_ptr(c.bins_k), _np_ptr(c.bins_v), c.fmt, c.group,
             capi.CG_OUT_F16 if out_k.dtype == torch.float16 else capi.CG_OUT_F32,
             _ptr(out_k), _ptr(out_v), out_k.stride(0), _ptr(self.dstatus), _stream(stream)),
             "cg_decompress_chunk_ex")
@@ -259,6 +280,34 @@ def dequantize(sym, max1, bins_k, bins_v=None, chunk_tokens: int = 256, stream=N
     capi.check(capi.load().cg_dequantize(_ptr(sym), _ptr(max1), C.byref(shp), _np_ptr(bk),
                                          _np_ptr(bv), _ptr(ok), _ptr(ov), None, _stream(stream)),
                "cg_dequantize")
+    return ok, ov
+
+
+def quantize_delta(k, v, group: int, bins_k, bins_v=None, chunk_tokens: int = 256, status=None,
+                   stream=None):
+    """[CG §1.2(1)] anchors + deltas per token group -> (sym, max1) as quantize."""
+    shp = _kv_shape(k, v, chunk_tokens)
+    bk = _bins(bins_k, shp.L)
+    bv = _bins(bins_k if bins_v is None else bins_v, shp.L)
+    sym = torch.empty((2, shp.L, shp.T, shp.C), dtype=torch.uint8, device=k.device)
+    max1 = torch.empty((2, shp.L, shp.T), dtype=torch.int16, device=k.device)
+    capi.check(capi.load().cg_quantize_delta(_ptr(k), _ptr(v), C.byref(shp), _np_ptr(bk), _np_ptr(bv), group,
+                                             _ptr(sym), _ptr(max1), _ptr(status), _stream(stream)),
+               "cg_quantize_delta")
+    return sym, max1
+
+
+def dequantize_delta(sym, max1, group: int, bins_k, bins_v=None, chunk_tokens: int = 256, stream=None):
+    """The inverse of quantize_delta's symbols -> (out_k, out_v) float32 [L, T, C]."""
+    _, L, T, C_ = sym.shape
+    shp = make_shape(L, T, C_, chunk_tokens)
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    ok = torch.empty((L, T, C_), dtype=torch.float32, device=sym.device)
+    ov = torch.empty((L, T, C_), dtype=torch.float32, device=sym.device)
+    capi.check(capi.load().cg_dequantize_delta(_ptr(sym), _ptr(max1), C.byref(shp), _np_ptr(bk), _np_ptr(bv),
+                                               group, _ptr(ok), _ptr(ov), None, _stream(stream)),
+               "cg_dequantize_delta")
     return ok, ov
 
 

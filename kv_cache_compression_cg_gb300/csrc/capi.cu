@@ -58,6 +58,7 @@ bool prepare(const cg_shape *s, const int32_t *bins_k, const int32_t *bins_v, Di
     d.layer_stride = s->layer_stride;
     d.nstreams = 2LL * s->L * s->T;
     d.stage_bytes = (long long)stage_bytes_per_stream(s->C);
+    d.G = 1;
     if (mt) {
         std::memset(mt, 0, sizeof(*mt));
         for (int l = 0; l < s->L; l++) {
@@ -117,6 +118,8 @@ int max_alphabet_v2(const Dims &d, const MaxTab &mt) {
 
 cg_status launched(cudaError_t e) { return e == cudaSuccess ? CG_OK : CG_ERR_CUDA; }
 
+bool group_ok(int32_t g) { return g >= 1 && g <= CG_MAX_CHUNK_TOKENS; }
+
 // Empty token range: only off[0] = 0 has to be written.
 cg_status empty_offsets(uint64_t *off, cudaStream_t stream) {
     if (!off) return CG_OK;
@@ -160,7 +163,7 @@ uint64_t cg_compress_workspace_bytes(const cg_shape *shape) {
     return encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d);
 }
 
-const char *cg_version(void) { return "cachegen-gb300 formats-1,2 sm_103a"; }
+const char *cg_version(void) { return "cachegen-gb300 formats-1,2 delta sm_103a"; }
 
 cg_status cg_quantize(const uint16_t *k, const uint16_t *v, const cg_shape *shape,
                       const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym, uint16_t *max1,
@@ -325,13 +328,14 @@ cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes, c
 cg_status cg_decompress_chunk_ex(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
                                  const uint32_t *len, const void *side, const uint16_t *max1,
                                  const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v, int format,
-                                 int out_dtype, void *out_k, void *out_v, int64_t out_layer_stride,
-                                 int32_t *status, cudaStream_t stream) {
+                                 int32_t group, int out_dtype, void *out_k, void *out_v,
+                                 int64_t out_layer_stride, int32_t *status, cudaStream_t stream) {
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return CG_ERR_INVALID_ARG;
-    if ((format != 1 && format != 2) || (out_dtype != CG_OUT_F32 && out_dtype != CG_OUT_F16))
+    if ((format != 1 && format != 2) || (out_dtype != CG_OUT_F32 && out_dtype != CG_OUT_F16) || !group_ok(group))
         return CG_ERR_INVALID_ARG;
+    d.G = group;
     if (out_layer_stride < (int64_t)d.T * d.C) return CG_ERR_INVALID_ARG;
     if (d.T == 0) return CG_OK;
     const uintptr_t es = out_dtype == CG_OUT_F16 ? 2 : 4;
@@ -344,6 +348,70 @@ cg_status cg_decompress_chunk_ex(const uint8_t *packed, uint64_t packed_bytes, c
     return launched(cg::launch_decode_pipe(packed, packed_bytes, off, len, cdf, rec, max1, d, mt,
                                            out_dtype == CG_OUT_F16 ? 2 : 1, out_k, out_v, out_layer_stride, status,
                                            stream));
+}
+
+cg_status cg_quantize_delta(const uint16_t *k, const uint16_t *v, const cg_shape *shape, const int32_t *bins_k,
+                            const int32_t *bins_v, int32_t group, uint8_t *sym, uint16_t *max1, int32_t *status,
+                            cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || !group_ok(group)) return CG_ERR_INVALID_ARG;
+    if (!k || !v || !sym || !max1 || !aligned(k, 2) || !aligned(v, 2) || !aligned(max1, 2))
+        return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    d.G = group;
+    if (group == 1) return launched(cg::launch_quantize(k, v, d, mt, sym, max1, status, stream));
+    return launched(cg::launch_quantize_delta(k, v, d, mt, sym, max1, status, stream));
+}
+
+cg_status cg_dequantize_delta(const uint8_t *sym, const uint16_t *max1, const cg_shape *shape,
+                              const int32_t *bins_k, const int32_t *bins_v, int32_t group, float *out_k,
+                              float *out_v, int32_t *status, cudaStream_t stream) {
+    (void)status;
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || !group_ok(group)) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    if (!sym || !max1 || !out_k || !out_v || !aligned(max1, 2) || !aligned(out_k, 16) || !aligned(out_v, 16) ||
+        !aligned(sym, 4))
+        return CG_ERR_INVALID_ARG;
+    d.G = group;
+    if (group == 1) return launched(cg::launch_dequantize(sym, max1, d, mt, out_k, out_v, stream));
+    return launched(cg::launch_dequantize_delta(sym, max1, d, mt, out_k, out_v, stream));
+}
+
+cg_status cg_compress_chunk_ex(const uint16_t *k, const uint16_t *v, const cg_shape *shape, const int32_t *bins_k,
+                               const int32_t *bins_v, int format, int32_t group, uint16_t *max1, void *side,
+                               uint8_t *packed, uint64_t capacity, uint32_t *len, uint64_t *off, void *workspace,
+                               uint64_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || !group_ok(group) || (format != 1 && format != 2))
+        return CG_ERR_INVALID_ARG;
+    if (format == 2 && d.Tc > 256) return CG_ERR_INVALID_ARG;
+    if (!off) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return empty_offsets(off, stream);
+    if (!k || !v || !max1 || !side || !len || !workspace || (!packed && capacity > 0)) return CG_ERR_INVALID_ARG;
+    if (!aligned(k, 2) || !aligned(v, 2) || !aligned(max1, 2) || !aligned(side, format == 1 ? 2 : 1) ||
+        !aligned(len, 4) || !aligned(off, 8) || !aligned(workspace, kAlign))
+        return CG_ERR_INVALID_ARG;
+    if (workspace_bytes < encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d)) return CG_ERR_WORKSPACE;
+    d.G = group;
+    Workspace w = carve(workspace, d, true);
+    uint16_t *cdf = format == 1 ? static_cast<uint16_t *>(side) : nullptr;
+    uint8_t *rec = format == 2 ? static_cast<uint8_t *>(side) : nullptr;
+    Dims df = d;  // the fused kernel's limits, with format 2's alphabet
+    if (format == 2) df.A[0] = df.A[1] = max_alphabet_v2(d, mt);
+    if (cg::compress_fused_applies(df, k, v))
+        return launched(cg::launch_compress_fused(k, v, d, mt, max1, cdf, rec, w.stage, len, off, packed, capacity,
+                                                  w.state, status, stream));
+    if (format == 2) return CG_ERR_INVALID_ARG;  // format 2 runs on the fused path only
+    cudaError_t e = group == 1 ? cg::launch_quantize(k, v, d, mt, w.sym, max1, status, stream)
+                               : cg::launch_quantize_delta(k, v, d, mt, w.sym, max1, status, stream);
+    if (e != cudaSuccess) return CG_ERR_CUDA;
+    if (cg::launch_code_slices(w.sym, nullptr, cdf, w.stage, len, d, 2, status, stream) != cudaSuccess)
+        return CG_ERR_CUDA;
+    return launched(cg::launch_scan_and_pack(len, off, w.stage, packed, capacity, w.partials, d, status, stream));
 }
 
 }  // extern "C"

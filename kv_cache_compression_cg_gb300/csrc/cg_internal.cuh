@@ -1,6 +1,6 @@
 // cg_internal.cuh - shared device-side definitions of the sm_103a codec.
 //
-// Layouts follow the codec specification in include/cachegen.h (format 1).
+// Layouts follow the codec specification in include/cachegen.h.
 // Citation key: [CG] = web page "CacheGen 技术详解：KV Cache 的高效压缩与流式传输".
 #pragma once
 
@@ -19,6 +19,7 @@ struct Dims {
     long long layer_stride;  // elements between layers of the fp16 input
     long long nstreams;      // 2*L*T
     long long stage_bytes;   // per-stream staging bytes in the workspace
+    int G;                   // token-locality delta group (1: none) [CG §1.2(1)]
 };
 
 // MAX = bins / 2 - 1 per (kv, layer) [CG §2.3(1)], in kernel parameter space.
@@ -160,6 +161,14 @@ cudaError_t launch_decode_pipe(const uint8_t *packed, uint64_t packed_bytes,
                                int out_dtype, void *out_k, void *out_v, long long ols,
                                int32_t *status, cudaStream_t s);
 
+// launch_decode_pipe for d.G > 1 (the token-locality delta).
+cudaError_t launch_decode_pipe_delta(const uint8_t *packed, uint64_t packed_bytes,
+                                     const uint64_t *off, const uint32_t *len,
+                                     const uint16_t *cdf, const uint8_t *rec,
+                                     const uint16_t *max1, const Dims &d, const MaxTab &mt,
+                                     int out_dtype, void *out_k, void *out_v, long long ols,
+                                     int32_t *status, cudaStream_t s);
+
 // Any chunk size up to CG_MAX_CHUNK_TOKENS (used by launch_decode beyond 256).
 cudaError_t launch_decode_generic(const uint8_t *packed, uint64_t packed_bytes,
                                   const uint64_t *off, const uint32_t *len,
@@ -171,5 +180,34 @@ cudaError_t launch_decode_generic(const uint8_t *packed, uint64_t packed_bytes,
 cudaError_t launch_dequantize(const uint8_t *sym, const uint16_t *max1,
                               const Dims &d, const MaxTab &mt, float *out_k,
                               float *out_v, cudaStream_t s);
+
+// Token-locality delta (d.G > 1): anchors quantised as above, the other rows
+// of each group as deltas from the anchor's reconstruction; dequantisation
+// adds the reconstruction back. Binary32 output [L][T][C].
+cudaError_t launch_quantize_delta(const uint16_t *k, const uint16_t *v, const Dims &d,
+                                  const MaxTab &mt, uint8_t *sym, uint16_t *max1,
+                                  int32_t *status, cudaStream_t s);
+cudaError_t launch_dequantize_delta(const uint8_t *sym, const uint16_t *max1,
+                                    const Dims &d, const MaxTab &mt, float *out_k,
+                                    float *out_v, cudaStream_t s);
+
+// Token groups of the delta: chunk-local, G tokens from each chunk's first.
+__host__ __device__ inline long long delta_groups_per_chunk(const Dims &d) {
+    return (d.Tc + d.G - 1) / d.G;
+}
+// Work unit `task` -> (kv, l), the anchor's token t_a and the group's rows n
+// (n <= 0: past the end of a short last chunk).
+__host__ __device__ inline void delta_task(const Dims &d, long long task, int &kv, int &l, long long &t_a, int &n) {
+    const long long gpc = delta_groups_per_chunk(d);
+    const int g = (int)(task % gpc);
+    long long r = task / gpc;
+    const int k = (int)(r % d.nch);
+    r /= d.nch;
+    l = (int)(r % d.L);
+    kv = (int)(r / d.L);
+    const int Tk = chunk_tokens(d, k);
+    t_a = (long long)k * d.Tc + (long long)g * d.G;
+    n = min(d.G, Tk - g * d.G);
+}
 
 }  // namespace cg

@@ -146,6 +146,52 @@ __device__ __forceinline__ void quant_pair(uint32_t h2, float f, unsigned long l
         : "f"(p0), "f"(p1), "l"(fm), "l"(mg));
 }
 
+// quant_pair for two binary32 values (the delta's d).
+__device__ __forceinline__ void quant_pair_f(float d0, float d1, float f, unsigned long long fm,
+                                             unsigned long long mg, uint32_t &b0, uint32_t &b1) {
+    const float p0 = __fmul_rn(d0, f), p1 = __fmul_rn(d1, f);
+    asm("{\n\t.reg .b64 t;\n\t"
+        "mov.b64 t, {%2, %3};\n\t"
+        "add.rn.f32x2 t, t, %4;\n\t"
+        "add.rn.f32x2 t, t, %5;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t}"
+        : "=r"(b0), "=r"(b1)
+        : "f"(p0), "f"(p1), "l"(fm), "l"(mg));
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+
+// Smallest binary16 >= m (m >= 0), as bits; 65504's bits above it or for NaN.
+__device__ __forceinline__ uint32_t half_up_bits(float m) {
+    const uint32_t h = __half_as_ushort(__float2half_ru(m));
+    return h >= 0x7C00u ? 0x7BFFu : h;
+}
+
+// The delta [CG §1.2(1)] on one quad of row r, given the anchor row's quad xa:
+// a^ = D(Q(xa)) (the anchor's q recomputed with its factor fa, its table
+// entry times ma; ma = 0 makes an anchor its own zero reference), d = x - a^.
+__device__ __forceinline__ void delta_quad(uint2 x, uint2 xa, float fa, float ma, uint32_t us, uint32_t qmax,
+                                           unsigned long long fm, unsigned long long mg, float (&dv)[4]) {
+    uint32_t c0, c1, c2, c3;
+    quant_pair(xa.x, fa, fm, mg, c0, c1);
+    quant_pair(xa.y, fa, fm, mg, c2, c3);
+    // table index clamped to [0, 2 MAX]: in bounds whatever the box holds
+    const float a0 = __fmul_rn(lds_f32(us + 4u * min(c0 - kMagic, qmax)), ma);
+    const float a1 = __fmul_rn(lds_f32(us + 4u * min(c1 - kMagic, qmax)), ma);
+    const float a2 = __fmul_rn(lds_f32(us + 4u * min(c2 - kMagic, qmax)), ma);
+    const float a3 = __fmul_rn(lds_f32(us + 4u * min(c3 - kMagic, qmax)), ma);
+    const float2 x01 = __half22float2(*reinterpret_cast<const __half2 *>(&x.x));
+    const float2 x23 = __half22float2(*reinterpret_cast<const __half2 *>(&x.y));
+    dv[0] = __fsub_rn(x01.x, a0);
+    dv[1] = __fsub_rn(x01.y, a1);
+    dv[2] = __fsub_rn(x23.x, a2);
+    dv[3] = __fsub_rn(x23.y, a3);
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -198,13 +244,55 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
     }
 }
 
+// The reference max1 of row r with anchor row ra: the anchor's, or 0 for an
+// anchor itself.
+__device__ __forceinline__ float anchor_m1(const uint16_t *m1, int ra, int r) {
+    return ra == r ? 0.0f : __half2float(__ushort_as_half(m1[ra]));
+}
+
+// Step 2 with the delta: every row as d = x - a^ (anchors against +-0), q
+// clamped to [0, 2 MAX] (max1 rounded to 65504 can sit below max |d|).
+__device__ __forceinline__ void quantise_window_delta(const unsigned char *box, const float *fac,
+                                                      const uint8_t *anchor, const uint16_t *m1, uint32_t us,
+                                                      uint8_t *sym, uint32_t cnt_lane, int rbase, int kq, int Tk,
+                                                      unsigned long long fm, unsigned long long mg, uint32_t qmax) {
+#pragma unroll 2
+    for (int i = 0; i < kNT / 32 * 2; i++) {
+        const int r = rbase + 2 * i;
+        if (r >= Tk) break;
+        const int ra = anchor[r];
+        const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
+        const uint2 xa = *reinterpret_cast<const uint2 *>(box + ra * (kW * 2) + 8 * kq);
+        float dv[4];
+        delta_quad(x, xa, fac[ra], anchor_m1(m1, ra, r), us, qmax, fm, mg, dv);
+        const float f = fac[r];
+        uint32_t b0, b1, b2, b3;
+        quant_pair_f(dv[0], dv[1], f, fm, mg, b0, b1);
+        quant_pair_f(dv[2], dv[3], f, fm, mg, b2, b3);
+        b0 = (uint32_t)min(max((int)(b0 - kMagic), 0), (int)qmax) + kMagic;
+        b1 = (uint32_t)min(max((int)(b1 - kMagic), 0), (int)qmax) + kMagic;
+        b2 = (uint32_t)min(max((int)(b2 - kMagic), 0), (int)qmax) + kMagic;
+        b3 = (uint32_t)min(max((int)(b3 - kMagic), 0), (int)qmax) + kMagic;
+        const uint32_t lo2 = __byte_perm(b0, b1, 0x0040), hi2 = __byte_perm(b2, b3, 0x0040);
+        *reinterpret_cast<uint32_t *>(sym + r * kSymRow + 4 * kq) = __byte_perm(lo2, hi2, 0x5410) << 3;
+        red_add(b0 * (kCntRow * 2) + cnt_lane, 1u);
+        red_add(b1 * (kCntRow * 2) + cnt_lane, 1u << 16);
+        red_add(b2 * (kCntRow * 2) + cnt_lane + 4, 1u);
+        red_add(b3 * (kCntRow * 2) + cnt_lane + 4, 1u << 16);
+    }
+}
+
 // V2 (format 2): the alphabet is the layer's 2*MAX + 1 symbols and the side
 // output is the count records (uint8) instead of the CDF entries (uint16).
-template <bool V2>
+// DELTA: the token-locality delta [CG §1.2(1)] with groups of d.G tokens; the
+// anchors' max1 comes from a pre-pass over the anchor rows (plain loads of
+// kin / vin), then pass 1 takes max |x - a^| per row and step 2 quantises d.
+template <bool V2, bool DELTA>
 __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
-    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, Dims d, MaxTab mt,
-    int box_rows, uint16_t *__restrict__ max1_out, void *__restrict__ side_out, uint8_t *__restrict__ stage,
-    uint32_t *__restrict__ len, unsigned long long *state, int32_t *status) {
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const uint16_t *kin,
+    const uint16_t *vin, Dims d, MaxTab mt, int box_rows, uint16_t *__restrict__ max1_out,
+    void *__restrict__ side_out, uint8_t *__restrict__ stage, uint32_t *__restrict__ len,
+    unsigned long long *state, int32_t *status) {
     __shared__ __align__(1024) unsigned char s_union[kUnionBytes];
     __shared__ unsigned long long s_scan[kNW + 4];
     __shared__ unsigned long long s_bar[2];
@@ -212,6 +300,10 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     __shared__ uint16_t s_m1[kNT];
     __shared__ uint16_t s_ftab[kNT + 2];
     __shared__ int s_ticket;
+    // the delta: each row's anchor row and the table (q - MAX) / MAX (an
+    // anchor row keeps its max1 in s_m1 from the pre-pass on)
+    __shared__ uint8_t s_anchor[DELTA ? kNT : 1];
+    __shared__ float s_unitc[DELTA ? 64 : 1];
     extern __shared__ __align__(128) unsigned char dsm[];
 
     uint2 *cdfw = reinterpret_cast<uint2 *>(s_union);
@@ -258,7 +350,42 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         for (int m = 2; m < 4 && m < nwin; m++) tma_prefetch_l2(tm, m * kW, t0, l);
     }
 
-    // 1. max1 pass over the slice's boxes (buffers alternate)
+    const float fmax = (float)MAX;
+    const unsigned long long fm = pair(fmax, fmax);
+    const unsigned long long mg = pair(12582912.0f, 12582912.0f);
+    const uint32_t qmax = 2u * (uint32_t)MAX;
+    const uint32_t us = smem_u32(s_unitc);
+    if (DELTA) {
+        // 0. anchors' max1 (rows 0, G, 2G, ... of the chunk), one warp per anchor row
+        const uint16_t *xb = (kv ? vin : kin) + (long long)l * d.layer_stride + (long long)t0 * d.C;
+        const int na = (Tk + d.G - 1) / d.G;
+        const int nv = d.C >> 3;
+        for (int j = warp; j < na; j += kNW) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(xb + (long long)j * d.G * d.C);
+            uint32_t m = 0;
+            for (int c = lane; c < nv; c += 32) {
+                const uint4 q = __ldg(row + c);
+                m = __vmaxu2(m, q.x & 0x7FFF7FFFu);
+                m = __vmaxu2(m, q.y & 0x7FFF7FFFu);
+                m = __vmaxu2(m, q.z & 0x7FFF7FFFu);
+                m = __vmaxu2(m, q.w & 0x7FFF7FFFu);
+            }
+            m = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+            if (lane == 0) s_m1[j * d.G] = (uint16_t)m;
+        }
+        __syncthreads();
+        const int ra = tid - tid % d.G;
+        s_anchor[tid] = (uint8_t)ra;
+        if (tid < Tk && ra == tid) {
+            const unsigned mb = s_m1[tid];
+            s_fac[tid] = mb ? __fdiv_rn(fmax, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
+        }
+        if (tid < 64) s_unitc[tid] = __fdiv_rn((float)(tid - MAX), fmax);
+        __syncthreads();
+    }
+
+    // 1. max1 pass over the slice's boxes (buffers alternate); with the delta,
+    // max |x - a^| as binary32 bits (non-negative floats order like their bits)
     uint32_t ph0 = 0, ph1 = 0;
     uint32_t mx[16];
 #pragma unroll
@@ -276,8 +403,18 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
             const int r = rbase + 2 * i;
             if (r < Tk) {
                 const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
-                mx[i] = __vmaxu2(mx[i], x.x & 0x7FFF7FFFu);
-                mx[i] = __vmaxu2(mx[i], x.y & 0x7FFF7FFFu);
+                if (DELTA) {
+                    const int ra = s_anchor[r];
+                    const uint2 xa = *reinterpret_cast<const uint2 *>(box + ra * (kW * 2) + 8 * kq);
+                    float dv[4];
+                    delta_quad(x, xa, s_fac[ra], anchor_m1(s_m1, ra, r), us, qmax, fm, mg, dv);
+                    const uint32_t m01 = max(__float_as_uint(dv[0]) & 0x7FFFFFFFu, __float_as_uint(dv[1]) & 0x7FFFFFFFu);
+                    const uint32_t m23 = max(__float_as_uint(dv[2]) & 0x7FFFFFFFu, __float_as_uint(dv[3]) & 0x7FFFFFFFu);
+                    mx[i] = max(mx[i], max(m01, m23));
+                } else {
+                    mx[i] = __vmaxu2(mx[i], x.x & 0x7FFF7FFFu);
+                    mx[i] = __vmaxu2(mx[i], x.y & 0x7FFF7FFFu);
+                }
             }
         }
         __syncthreads();  // the buffer is free again
@@ -294,7 +431,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         uint32_t mine = 0;
 #pragma unroll
         for (int i = 0; i < 16; i++) {
-            uint32_t v = max(mx[i] & 0xFFFFu, mx[i] >> 16);
+            uint32_t v = DELTA ? mx[i] : max(mx[i] & 0xFFFFu, mx[i] >> 16);
             v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
             v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
             v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
@@ -303,25 +440,24 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         }
         const int r = rbase + 2 * kq;
         if (r < Tk) {
-            s_m1[r] = (uint16_t)mine;
-            max1_out[group_index(d, kv, l, t0 + r)] = (uint16_t)mine;
-            nonfinite = mine >= 0x7C00u;
+            // the delta: max1 = max |d| rounded up to binary16 (an anchor's d is
+            // x itself, so its max1 is the plain one)
+            const uint32_t mh = DELTA ? half_up_bits(__uint_as_float(mine)) : mine;
+            s_m1[r] = (uint16_t)mh;
+            max1_out[group_index(d, kv, l, t0 + r)] = (uint16_t)mh;
+            nonfinite = DELTA ? mine >= 0x7F800000u : mine >= 0x7C00u;
         }
     }
     for (int n = tid; n <= Tk; n += kNT)
         s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kTotal - (uint32_t)A)) / (uint32_t)Tk);
     for (int i = tid; i < kCntBytes / 4; i += kNT) cnt32[i] = 0;
     nonfinite = __syncthreads_or(nonfinite) != 0;
-    const float fmax = (float)MAX;
     if (tid < Tk) {
         const unsigned mb = s_m1[tid];
         s_fac[tid] = mb ? __fdiv_rn(fmax, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
     }
     __syncthreads();
 
-    const unsigned long long fm = pair(fmax, fmax);
-    const unsigned long long mg = pair(12582912.0f, 12582912.0f);
-    const uint32_t qmax = 2u * (uint32_t)MAX;
     // counter byte address of (q, channel 4 kq) is cnt_lane + 132 * (kMagic + q)
     const uint32_t cnt_lane = smem_u32(cnt32) + 8u * (uint32_t)kq - (uint32_t)(kCntRow * 2) * kMagic;
     Enc e;
@@ -335,7 +471,9 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         // 2. quantise + count
         if (4 * kq < Wc) {
             // a box that did not arrive in time holds stale values: clamp those too
-            if (nonfinite || timed_out)
+            if (DELTA)
+                quantise_window_delta(box0, s_fac, s_anchor, s_m1, us, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+            else if (nonfinite || timed_out)
                 quantise_window<true>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
             else
                 quantise_window<false>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
@@ -634,14 +772,15 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
     if (!make_map(&tmk, k, d, box_rows) || !make_map(&tmv, v, d, box_rows)) return cudaErrorNotSupported;
     const int dyn = 128 + box_rows * kW * 2;
     const bool v2 = cdf == nullptr;
-    auto kern = v2 ? k_compress_tma<true> : k_compress_tma<false>;
+    auto kern = d.G > 1 ? (v2 ? k_compress_tma<true, true> : k_compress_tma<false, true>)
+                        : (v2 ? k_compress_tma<true, false> : k_compress_tma<false, false>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     const long long nslices = 2LL * d.L * d.nch;
     k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
-    kern<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1,
+    kern<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, k, v, d, mt, box_rows, max1,
                                               v2 ? static_cast<void *>(rec) : static_cast<void *>(cdf), stage, len,
                                               state, status);
     k_pack<<<(unsigned)nslices, kNT, 0, s>>>(d, stage, len, off, packed, capacity, state, status);

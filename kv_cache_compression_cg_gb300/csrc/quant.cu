@@ -171,6 +171,215 @@ __global__ void __launch_bounds__(256) k_dequantize(const uint8_t *__restrict__ 
     }
 }
 
+// ---- token-locality delta [CG §1.2(1)] -----------------------------------
+// One warp per token group: the anchor row first (plain quantisation, its
+// reconstruction kept), then each other row as d = x - a^ with max1 the
+// binary16 value rounded up from max |d| (65504 above it), q clamped to
+// [0, 2 MAX]. HBM-bound like the plain kernels.
+
+// Smallest binary16 >= m (m >= 0; NaN and values above 65504 give 65504).
+__device__ __forceinline__ unsigned half_up_bits(float m) {
+    const unsigned h = __half_as_ushort(__float2half_ru(m));
+    return h >= 0x7C00u ? 0x7BFFu : h;
+}
+
+__device__ __forceinline__ float dequant_one(unsigned q, int MAX, float fmax, float m1) {
+    return __fmul_rn(__fdiv_rn((float)((int)q - MAX), fmax), m1);
+}
+
+__device__ __forceinline__ unsigned quant_delta_one(float dv, float factor, float fmax, int MAX, bool z) {
+    if (z) return (unsigned)MAX;
+    int q = __float2int_rn(__fadd_rn(__fmul_rn(dv, factor), fmax));
+    q = q < 0 ? 0 : q;
+    return (unsigned)(q > 2 * MAX ? 2 * MAX : q);
+}
+
+// Vector path: C % 8 == 0, 16-byte aligned rows, C <= 256 VPL.
+template <int VPL>
+__global__ void __launch_bounds__(256) k_quantize_delta_vec(const uint16_t *__restrict__ kin,
+                                                            const uint16_t *__restrict__ vin, Dims d,
+                                                            MaxTab mt, uint8_t *__restrict__ sym,
+                                                            uint16_t *__restrict__ max1,
+                                                            int32_t *status) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long tasks = 2LL * d.L * d.nch * delta_groups_per_chunk(d);
+    const int nvec = d.C >> 3;
+    for (long long task = warp; task < tasks; task += nwarps) {
+        int kv, l, n;
+        long long ta;
+        delta_task(d, task, kv, l, ta, n);
+        if (n <= 0) continue;
+        const int MAX = mt.v[kv][l];
+        const float fmax = (float)MAX;
+        const uint16_t *xb = (kv ? vin : kin) + (long long)l * d.layer_stride;
+        float a[VPL][8];
+        bool bad = false;
+        for (int r = 0; r < n; r++) {
+            const long long t = ta + r;
+            const long long row = group_index(d, kv, l, t);
+            const uint16_t *x = xb + t * d.C;
+            uint4 val[VPL];
+#pragma unroll
+            for (int i = 0; i < VPL; i++) {
+                const int vi = lane + 32 * i;
+                val[i] = vi < nvec ? __ldg(reinterpret_cast<const uint4 *>(x) + vi) : make_uint4(0, 0, 0, 0);
+            }
+            // max1: the anchor's |x| (as fp16 bits), the others' |x - a^| rounded up
+            unsigned mh;
+            if (r == 0) {
+                unsigned m = 0;
+#pragma unroll
+                for (int i = 0; i < VPL; i++) {
+                    m = __vmaxu2(m, val[i].x & 0x7FFF7FFFu);
+                    m = __vmaxu2(m, val[i].y & 0x7FFF7FFFu);
+                    m = __vmaxu2(m, val[i].z & 0x7FFF7FFFu);
+                    m = __vmaxu2(m, val[i].w & 0x7FFF7FFFu);
+                }
+                mh = __reduce_max_sync(0xFFFFFFFFu, max(m & 0xFFFFu, m >> 16));
+                bad |= mh >= 0x7C00u;
+            } else {
+                unsigned mb = 0;  // |d| bits: non-negative floats order like their bits
+#pragma unroll
+                for (int i = 0; i < VPL; i++) {
+                    if (lane + 32 * i >= nvec) continue;  // no channels (and no a^) there
+                    const uint32_t *w = reinterpret_cast<const uint32_t *>(&val[i]);
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        const float dv = __fsub_rn(half_bits_to_float((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu), a[i][j]);
+                        mb = max(mb, __float_as_uint(dv) & 0x7FFFFFFFu);
+                    }
+                }
+                mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+                bad |= mb >= 0x7F800000u;
+                mh = half_up_bits(__uint_as_float(mb));
+            }
+            if (lane == 0) max1[row] = (uint16_t)mh;
+            const bool z = mh == 0;
+            const float m1 = half_bits_to_float(mh);
+            const float factor = z ? 0.0f : __fdiv_rn(fmax, m1);
+            uint8_t *out = sym + row * d.C;
+#pragma unroll
+            for (int i = 0; i < VPL; i++) {
+                const int vi = lane + 32 * i;
+                if (vi >= nvec) continue;
+                const uint32_t *w = reinterpret_cast<const uint32_t *>(&val[i]);
+                unsigned q[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const float xv = half_bits_to_float((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+                    if (r == 0) {
+                        q[j] = quant_one((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, factor, fmax, MAX, z);
+                        a[i][j] = dequant_one(q[j], MAX, fmax, m1);
+                    } else {
+                        q[j] = quant_delta_one(__fsub_rn(xv, a[i][j]), factor, fmax, MAX, z);
+                    }
+                }
+                uint2 o;
+                o.x = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+                o.y = q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24);
+                reinterpret_cast<uint2 *>(out)[vi] = o;
+            }
+        }
+        if (bad && lane == 0 && status) atomicOr(status, CG_FLAG_NONFINITE);
+    }
+}
+
+// Generic path: any C and alignment. A lane reads back the anchor symbols it
+// wrote itself (same channels), so no cross-lane ordering is needed.
+__global__ void __launch_bounds__(256) k_quantize_delta_any(const uint16_t *__restrict__ kin,
+                                                            const uint16_t *__restrict__ vin, Dims d,
+                                                            MaxTab mt, uint8_t *sym,
+                                                            uint16_t *__restrict__ max1,
+                                                            int32_t *status) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long tasks = 2LL * d.L * d.nch * delta_groups_per_chunk(d);
+    for (long long task = warp; task < tasks; task += nwarps) {
+        int kv, l, n;
+        long long ta;
+        delta_task(d, task, kv, l, ta, n);
+        if (n <= 0) continue;
+        const int MAX = mt.v[kv][l];
+        const float fmax = (float)MAX;
+        const uint16_t *xb = (kv ? vin : kin) + (long long)l * d.layer_stride;
+        const long long arow = group_index(d, kv, l, ta);
+        const uint8_t *qa = sym + arow * d.C;
+        bool bad = false;
+        float m1a = 0.0f;
+        for (int r = 0; r < n; r++) {
+            const long long t = ta + r;
+            const long long row = group_index(d, kv, l, t);
+            const uint16_t *x = xb + t * d.C;
+            unsigned mh;
+            if (r == 0) {
+                unsigned m = 0;
+                for (int c = lane; c < d.C; c += 32) m = max(m, (unsigned)(x[c] & 0x7FFFu));
+                mh = __reduce_max_sync(0xFFFFFFFFu, m);
+                bad |= mh >= 0x7C00u;
+            } else {
+                unsigned mb = 0;
+                for (int c = lane; c < d.C; c += 32) {
+                    const float dv = __fsub_rn(half_bits_to_float(x[c]), dequant_one(qa[c], MAX, fmax, m1a));
+                    mb = max(mb, __float_as_uint(dv) & 0x7FFFFFFFu);
+                }
+                mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+                bad |= mb >= 0x7F800000u;
+                mh = half_up_bits(__uint_as_float(mb));
+            }
+            if (lane == 0) max1[row] = (uint16_t)mh;
+            const bool z = mh == 0;
+            const float m1 = half_bits_to_float(mh);
+            const float factor = z ? 0.0f : __fdiv_rn(fmax, m1);
+            uint8_t *out = sym + row * d.C;
+            for (int c = lane; c < d.C; c += 32) {
+                if (r == 0)
+                    out[c] = (uint8_t)quant_one(x[c], factor, fmax, MAX, z);
+                else
+                    out[c] = (uint8_t)quant_delta_one(
+                        __fsub_rn(half_bits_to_float(x[c]), dequant_one(qa[c], MAX, fmax, m1a)), factor, fmax, MAX, z);
+            }
+            if (r == 0) m1a = m1;
+        }
+        if (bad && lane == 0 && status) atomicOr(status, CG_FLAG_NONFINITE);
+    }
+}
+
+// Dequantisation with the delta: warp per group; x^ = a^ + D(q) off the anchor.
+__global__ void __launch_bounds__(256) k_dequantize_delta(const uint8_t *__restrict__ sym,
+                                                          const uint16_t *__restrict__ max1, Dims d,
+                                                          MaxTab mt, float *__restrict__ out_k,
+                                                          float *__restrict__ out_v) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long tasks = 2LL * d.L * d.nch * delta_groups_per_chunk(d);
+    for (long long task = warp; task < tasks; task += nwarps) {
+        int kv, l, n;
+        long long ta;
+        delta_task(d, task, kv, l, ta, n);
+        if (n <= 0) continue;
+        const int MAX = mt.v[kv][l];
+        const float fmax = (float)MAX;
+        const long long arow = group_index(d, kv, l, ta);
+        const uint8_t *qa = sym + arow * d.C;
+        const float m1a = half_bits_to_float(max1[arow]);
+        for (int r = 0; r < n; r++) {
+            const long long row = arow + r;
+            const float m1 = half_bits_to_float(max1[row]);
+            const uint8_t *q = sym + row * d.C;
+            float *o = (kv ? out_v : out_k) + ((long long)l * d.T + ta + r) * d.C;
+            for (int c = lane; c < d.C; c += 32) {
+                float x = dequant_one(q[c], MAX, fmax, m1);
+                if (r > 0) x = __fadd_rn(dequant_one(qa[c], MAX, fmax, m1a), x);
+                o[c] = x;
+            }
+        }
+    }
+}
+
 int grid_for_rows(long long rows) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
@@ -209,6 +418,34 @@ cudaError_t launch_dequantize(const uint8_t *sym, const uint16_t *max1, const Di
                               const MaxTab &mt, float *out_k, float *out_v, cudaStream_t s) {
     const long long rows = 2LL * d.L * d.T;
     k_dequantize<<<grid_for_rows(rows), 256, 0, s>>>(sym, max1, d, mt, out_k, out_v);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_delta(const uint16_t *k, const uint16_t *v, const Dims &d,
+                                  const MaxTab &mt, uint8_t *sym, uint16_t *max1, int32_t *status,
+                                  cudaStream_t s) {
+    const long long tasks = 2LL * d.L * d.nch * delta_groups_per_chunk(d);
+    const int grid = grid_for_rows(tasks);
+    const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(sym) & 7) == 0 && (d.layer_stride % 8) == 0 &&
+                         (d.C % 8) == 0;
+    const int nvec = d.C / 8;
+    if (aligned && nvec <= 32) {
+        k_quantize_delta_vec<1><<<grid, 256, 0, s>>>(k, v, d, mt, sym, max1, status);
+    } else if (aligned && nvec <= 64) {
+        k_quantize_delta_vec<2><<<grid, 256, 0, s>>>(k, v, d, mt, sym, max1, status);
+    } else if (aligned && nvec <= 128) {
+        k_quantize_delta_vec<4><<<grid, 256, 0, s>>>(k, v, d, mt, sym, max1, status);
+    } else {
+        k_quantize_delta_any<<<grid, 256, 0, s>>>(k, v, d, mt, sym, max1, status);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize_delta(const uint8_t *sym, const uint16_t *max1, const Dims &d,
+                                    const MaxTab &mt, float *out_k, float *out_v, cudaStream_t s) {
+    const long long tasks = 2LL * d.L * d.nch * delta_groups_per_chunk(d);
+    k_dequantize_delta<<<grid_for_rows(tasks), 256, 0, s>>>(sym, max1, d, mt, out_k, out_v);
     return cudaGetLastError();
 }
 

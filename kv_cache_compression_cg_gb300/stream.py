@@ -110,7 +110,9 @@ class StreamingCodec:
     """
 
     def __init__(self, L: int, T: int, C_: int, bins_k, bins_v=None, chunk_tokens: int = 256,
-                 piece_chunks: int = 2, device: str | torch.device = "cuda", fmt: int = 1):
+                 piece_chunks: int = 2, device: str | torch.device = "cuda", fmt: int = 1, group: int = 1):
+        """fmt, group: the codec's format and token-locality delta group (as
+        Codec); pieces are whole chunks, so they code independently."""
         if piece_chunks < 1:
             raise ValueError("piece_chunks must be >= 1")
         self.fmt = fmt
@@ -124,7 +126,7 @@ class StreamingCodec:
         self.k = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
         self.v = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
         mk = lambda t0, t1: _codec.Codec(L, t1 - t0, C_, self.bins_k, self.bins_v, chunk_tokens=chunk_tokens,
-                                         device=dev, fmt=fmt)
+                                         device=dev, fmt=fmt, group=group)
         self.enc = [mk(t0, t1) for t0, t1 in self.ranges]
         self.dec = [mk(t0, t1) for t0, t1 in self.ranges]
         self.host = []

@@ -116,9 +116,9 @@ def test_serving_layout_arguments_rejected(lib):
     odd = C.c_void_p(0x1001)
     ls = 64 * 64
 
-    def call(shape, fmt, dtype, ok, ov, stride):
-        return lib.cg_decompress_chunk_ex(fake, 10, fake, fake, fake, fake, C.byref(shape), pb, None, fmt, dtype,
-                                          ok, ov, stride, None, None)
+    def call(shape, fmt, dtype, ok, ov, stride, group=1):
+        return lib.cg_decompress_chunk_ex(fake, 10, fake, fake, fake, fake, C.byref(shape), pb, None, fmt, group,
+                                          dtype, ok, ov, stride, None, None)
     assert call(s, 3, 0, fake, fake, ls) == 1
     assert call(s, 1, 2, fake, fake, ls) == 1
     assert call(s, 2, 1, fake, fake, ls - 1) == 1
@@ -126,6 +126,30 @@ def test_serving_layout_arguments_rejected(lib):
     assert call(s, 1, 1, odd, fake, ls) == 1
     assert call(s, 2, 0, fake, C.c_void_p(0x1002), ls) == 1
     assert call(s, 1, 0, None, fake, ls) == 1
+    assert call(s, 1, 0, fake, fake, ls, group=0) == 1
+    assert call(s, 1, 0, fake, fake, ls, group=1025) == 1
+
+
+def test_delta_arguments_rejected(lib):
+    """The token-locality delta's entry points reject a group outside
+    [1, 1024], an unknown format and format 2 with chunks over 256 tokens,
+    before touching the device."""
+    s = _shape(2, 64, 64, 64)
+    b, pb = _b([16, 16])
+    fake = C.c_void_p(0x1000)
+    ws = C.c_void_p(0x10000)
+    for g in (0, -3, 1025):
+        assert lib.cg_quantize_delta(fake, fake, C.byref(s), pb, None, g, fake, fake, None, None) == 1
+        assert lib.cg_dequantize_delta(fake, fake, C.byref(s), pb, None, g, fake, fake, None, None) == 1
+        assert lib.cg_compress_chunk_ex(fake, fake, C.byref(s), pb, None, 1, g, fake, fake, fake, 10, fake, fake,
+                                        ws, 1 << 40, None, None) == 1
+    assert lib.cg_compress_chunk_ex(fake, fake, C.byref(s), pb, None, 3, 4, fake, fake, fake, 10, fake, fake,
+                                    ws, 1 << 40, None, None) == 1
+    big = _shape(2, 600, 64, 300)
+    assert lib.cg_compress_chunk_ex(fake, fake, C.byref(big), pb, None, 2, 4, fake, fake, fake, 10, fake, fake,
+                                    ws, 1 << 40, None, None) == 1
+    assert lib.cg_compress_chunk_ex(fake, fake, C.byref(s), pb, None, 1, 4, fake, fake, fake, 10, fake, fake,
+                                    ws, 16, None, None) == 2  # workspace too small
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
