@@ -73,10 +73,12 @@ __device__ __forceinline__ void refill(Stream &s) {
     if (!TAIL) {
         if (s.nb < 32) {
             uint32_t v = __byte_perm(s.raw, 0, 0x0123);
-            const int t = max(32 - 8 * s.rem, 0);  // bits past the stream's end
-            v &= t >= 32 ? 0u : (0xFFFFFFFFu << t);
+            if (s.rem < 4) {  // the stream ends inside (or before) this word
+                const int t = max(32 - 8 * s.rem, 0);  // bits past the stream's end
+                v &= t >= 32 ? 0u : (0xFFFFFFFFu << t);
+            }
             s.bhi |= v >> s.nb;
-            s.blo |= s.nb ? v << (32 - s.nb) : 0u;
+            s.blo |= __funnelshift_r(0u, v, (uint32_t)s.nb);  // v << (32 - nb), 0 for nb = 0
             s.nb += 32;
             if (s.rem > 4) s.wp++;
             s.rem -= 4;
@@ -252,9 +254,7 @@ __device__ __forceinline__ void copy_records(uint8_t *srec, const uint8_t *recw,
 template <int P>
 __device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, const uint8_t *srec, int A, uint32_t Tk,
                                               int W, int Wc, int t, const uint16_t *ftab) {
-    constexpr int SP = P / 4;              // symbols per thread
-    constexpr int NR = SP <= 8 ? SP : 1;   // counts held in registers (one read pass) up to 8
-    constexpr int UNR = SP <= 8 ? SP : 1;  // wider rows: plain loops (registers, code size)
+    constexpr int SP = P / 4;  // symbols per thread
     const int c = t >> 2, p = t & 3;
     if (c >= W) return false;  // whole four-lane groups
     const int j0 = p * SP;
@@ -263,51 +263,91 @@ __device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, cons
     auto count_at = [&](int j) -> uint32_t {  // stored count of symbol j != mode
         return (j < A && j != mode) ? (uint32_t)r[j < mode ? j + 1 : j] : 0u;
     };
-    uint32_t n[NR];
-    uint32_t others = 0;
-#pragma unroll UNR
-    for (int jj = 0; jj < SP; jj++) {
-        const uint32_t x = count_at(j0 + jj);
-        if (SP <= 8) n[jj < NR ? jj : 0] = x;
-        others += x;
-    }
-    others += __shfl_xor_sync(0xFFFFFFFFu, others, 1);
-    others += __shfl_xor_sync(0xFFFFFFFFu, others, 2);
-    const bool ok = mode < A && others <= Tk;
-    if (!ok) mode = mode < A ? mode : 0;
-    const uint32_t nmode = ok ? Tk - others : Tk;
-    auto f_at = [&](int jj) -> uint32_t {
-        const int j = j0 + jj;
-        if (j >= A) return 0u;
-        const uint32_t stored = SP <= 8 ? n[jj < NR ? jj : 0] : count_at(j);
-        return ftab[j == mode ? nmode : (ok ? stored : 0u)];
-    };
-    uint32_t fl = 0;  // this thread's sum of f (without the remainder)
-#pragma unroll UNR
-    for (int jj = 0; jj < SP; jj++) fl += f_at(jj);
-    uint32_t incl = fl;
-    uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
-    if (p >= 1) incl += v;
-    v = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
-    if (p >= 2) incl += v;
-    const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
-    uint32_t acc = incl - fl;
-    uint16_t *cr = cum + c * P;
-    uint16_t *fr = frq + c * P;
-#pragma unroll UNR
-    for (int jj = 0; jj < SP; jj++) {
-        const int j = j0 + jj;
-        const uint32_t f = f_at(jj);
-        if (j < A) {
-            cr[j] = (uint16_t)(acc + (j > mode ? rem : 0u));
-            fr[j] = (uint16_t)(f + (j == mode ? rem : 0u));
-        } else {
-            cr[j] = 65535u;
-            fr[j] = 0;
+    if constexpr (SP <= 8) {
+        // counts and frequencies in registers; entries leave two per 32-bit store
+        uint32_t n[SP], fv[SP];
+        uint32_t others = 0;
+#pragma unroll
+        for (int jj = 0; jj < SP; jj++) {
+            n[jj] = count_at(j0 + jj);
+            others += n[jj];
         }
-        acc += f;
+        others += __shfl_xor_sync(0xFFFFFFFFu, others, 1);
+        others += __shfl_xor_sync(0xFFFFFFFFu, others, 2);
+        const bool ok = mode < A && others <= Tk;
+        if (!ok) mode = mode < A ? mode : 0;
+        const uint32_t nmode = ok ? Tk - others : Tk;
+        uint32_t fl = 0;  // this thread's sum of f (without the remainder)
+#pragma unroll
+        for (int jj = 0; jj < SP; jj++) {
+            const int j = j0 + jj;
+            fv[jj] = j < A ? (uint32_t)ftab[j == mode ? nmode : (ok ? n[jj] : 0u)] : 0u;
+            fl += fv[jj];
+        }
+        uint32_t incl = fl;
+        uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
+        if (p >= 1) incl += v;
+        v = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
+        if (p >= 2) incl += v;
+        const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
+        uint32_t acc = incl - fl;
+        uint32_t *cr = reinterpret_cast<uint32_t *>(cum + c * P + j0);  // j0 and SP even: 4-byte aligned
+        uint32_t *fr = reinterpret_cast<uint32_t *>(frq + c * P + j0);
+#pragma unroll
+        for (int jj = 0; jj < SP; jj += 2) {
+            uint32_t cv[2], fw[2];
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int j = j0 + jj + h;
+                cv[h] = j < A ? acc + (j > mode ? rem : 0u) : 65535u;
+                fw[h] = j < A ? fv[jj + h] + (j == mode ? rem : 0u) : 0u;
+                acc += fv[jj + h];
+            }
+            cr[jj / 2] = (cv[0] & 0xFFFFu) | (cv[1] << 16);
+            fr[jj / 2] = (fw[0] & 0xFFFFu) | (fw[1] << 16);
+        }
+        return !ok && c < Wc;
+    } else {
+        uint32_t others = 0;
+#pragma unroll 1
+        for (int jj = 0; jj < SP; jj++) others += count_at(j0 + jj);
+        others += __shfl_xor_sync(0xFFFFFFFFu, others, 1);
+        others += __shfl_xor_sync(0xFFFFFFFFu, others, 2);
+        const bool ok = mode < A && others <= Tk;
+        if (!ok) mode = mode < A ? mode : 0;
+        const uint32_t nmode = ok ? Tk - others : Tk;
+        auto f_at = [&](int jj) -> uint32_t {
+            const int j = j0 + jj;
+            if (j >= A) return 0u;
+            return ftab[j == mode ? nmode : (ok ? count_at(j) : 0u)];
+        };
+        uint32_t fl = 0;
+#pragma unroll 1
+        for (int jj = 0; jj < SP; jj++) fl += f_at(jj);
+        uint32_t incl = fl;
+        uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
+        if (p >= 1) incl += v;
+        v = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
+        if (p >= 2) incl += v;
+        const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
+        uint32_t acc = incl - fl;
+        uint16_t *cr = cum + c * P;
+        uint16_t *fr = frq + c * P;
+#pragma unroll 1
+        for (int jj = 0; jj < SP; jj++) {
+            const int j = j0 + jj;
+            const uint32_t f = f_at(jj);
+            if (j < A) {
+                cr[j] = (uint16_t)(acc + (j > mode ? rem : 0u));
+                fr[j] = (uint16_t)(f + (j == mode ? rem : 0u));
+            } else {
+                cr[j] = 65535u;
+                fr[j] = 0;
+            }
+            acc += f;
+        }
+        return !ok && c < Wc;
     }
-    return !ok && c < Wc;
 }
 
 __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
