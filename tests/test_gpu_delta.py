@@ -152,3 +152,27 @@ def test_nonfinite_flagged_with_delta(cg):
         out = cd.compress(k, v)
         torch.cuda.synchronize()
         assert int(out.status.item()) & 1
+
+
+@pytest.mark.slow
+def test_fused_delta_full_workload(cg, oracle_mod, synth_mod):
+    """The benchmark's 4096-token workload with groups of 10, format 2, in
+    the launch configuration `bench.py --group 10` times: every output equal
+    to the oracle's."""
+    w = synth_mod.WORKLOADS["ctx4096"]
+    k, v = synth_mod.generate(w)
+    L, T, C_, Tc, G = w.L, w.T, w.C, w.chunk_tokens, 10
+    ref = oracle_mod.compress_ex(k, v, Tc, w.bins_k, w.bins_v, fmt=2, group=G)
+    cd = cg.Codec(L, T, C_, w.bins_k, w.bins_v, chunk_tokens=Tc, fmt=2, group=G)
+    out = cd.compress(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    ok, ov = cd.decompress()
+    torch.cuda.synchronize()
+    assert int(out.status.item()) == 0 and int(cd.dstatus.item()) == 0
+    assert np.array_equal(out.max1.cpu().numpy().view(np.uint16), ref["max1"])
+    assert np.array_equal(out.rec[:cd.rec_bytes].cpu().numpy(), ref["rec"])
+    assert np.array_equal(out.off.cpu().numpy().view(np.uint64), ref["off"])
+    assert np.array_equal(out.packed[:int(ref["off"][-1])].cpu().numpy(), ref["packed"])
+    wk, wv = oracle_mod.decompress_ex(ref["packed"], ref["off"], ref["len"], ref["rec"], ref["max1"], L, T, C_,
+                                      Tc, w.bins_k, w.bins_v, fmt=2, group=G)
+    assert np.array_equal(ok.cpu().numpy().view(np.uint32), wk.view(np.uint32))
+    assert np.array_equal(ov.cpu().numpy().view(np.uint32), wv.view(np.uint32))

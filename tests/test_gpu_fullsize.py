@@ -1,7 +1,7 @@
 """Full-size workloads (the 34B-shaped 32K-token context and the 80K-token
 low-locality stress case) on the GPU, in the launch configuration the
-benchmark times (one cg_compress_chunk and one cg_decompress_chunk over the
-whole tensor).
+benchmark times (one compress and one decompress call over the whole tensor),
+in both formats.
 
 The oracle cannot code 6-10 GB in a test, so:
 - sampled (chunk, kv, layer) slices are coded by the oracle from inputs the
@@ -37,7 +37,7 @@ def _samples(w, seed):
     return picks
 
 
-def _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l):
+def _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt):
     L, T, C_, Tc = w.L, w.T, w.C, w.chunk_tokens
     bins = (w.bins_k, w.bins_v)[kv]
     A_k, A_v = max(w.bins_k), max(w.bins_v)
@@ -48,19 +48,29 @@ def _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv,
     dev_x = (k, v)[kv][l, t0:t1].cpu().numpy()
     assert np.array_equal(dev_x.view(np.uint16), x.view(np.uint16)), "device generator differs from host"
     # the oracle on [2 layers][Tk][C]: layer 0 is the slice, layer 1 a zero
-    # layer with bins A, so that the oracle's alphabet is the tensor's A
+    # layer with bins A, so that format 1's alphabet is the tensor's A (format
+    # 2's alphabets are per layer)
     K = np.zeros((2, Tk, C_), np.float16)
     K[0] = x
     V = np.zeros((2, Tk, C_), np.float16)
-    ref = oracle_mod.compress(K, V, Tc, [bins[l], A], [A, A])
-    assert ref["A_k"] == A
+    if fmt == 1:
+        ref = oracle_mod.compress(K, V, Tc, [bins[l], A], [A, A])
+        assert ref["A_k"] == A
+    else:
+        ref = oracle_mod.compress_v2(K, V, Tc, [bins[l], A], [A, A])
     # max1
     got_m1 = out.max1[kv, l, t0:t1].cpu().numpy().view(np.uint16)
     assert np.array_equal(got_m1, ref["max1"][0, 0])
-    # CDF rows of the slice
-    g0 = oracle_mod.cdf_offset(L, C_, A_k, A_v, kc, kv, l, 0)
-    got_cdf = out.cdf[g0:g0 + C_ * A].cpu().numpy().view(np.uint16)
-    assert np.array_equal(got_cdf, ref["cdf"][:C_ * A])
+    # side information of the slice: CDF rows or count records
+    if fmt == 1:
+        g0 = oracle_mod.cdf_offset(L, C_, A_k, A_v, kc, kv, l, 0)
+        got_cdf = out.cdf[g0:g0 + C_ * A].cpu().numpy().view(np.uint16)
+        assert np.array_equal(got_cdf, ref["cdf"][:C_ * A])
+    else:
+        Al = oracle_mod.alphabet_v2(bins[l])
+        g0 = oracle_mod.rec_offset(L, C_, w.bins_k, w.bins_v, kc, kv, l, 0)
+        got_rec = out.rec[g0:g0 + C_ * Al].cpu().numpy()
+        assert np.array_equal(got_rec, ref["rec"][:C_ * Al])
     # stream lengths and bytes
     s0 = oracle_mod.stream_id(L, T, Tc, kc, kv, l, 0)
     got_len = out.len[s0:s0 + Tk].cpu().numpy().view(np.uint32)
@@ -69,8 +79,12 @@ def _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv,
     assert b1 - b0 == int(ref["off"][Tk])
     assert np.array_equal(out.packed[b0:b1].cpu().numpy(), ref["packed"][:b1 - b0])
     # dequantised output of the slice
-    rk, _ = oracle_mod.decompress(ref["packed"], ref["off"], ref["len"], ref["cdf"], ref["max1"],
-                                  2, Tk, C_, Tc, [bins[l], A], [A, A])
+    if fmt == 1:
+        rk, _ = oracle_mod.decompress(ref["packed"], ref["off"], ref["len"], ref["cdf"], ref["max1"],
+                                      2, Tk, C_, Tc, [bins[l], A], [A, A])
+    else:
+        rk, _ = oracle_mod.decompress_v2(ref["packed"], ref["off"], ref["len"], ref["rec"], ref["max1"],
+                                         2, Tk, C_, Tc, [bins[l], A], [A, A])
     got = (ok, ov)[kv][l, t0:t1].cpu().numpy()
     assert np.array_equal(got.view(np.uint32), rk[0].view(np.uint32))
 
@@ -93,12 +107,13 @@ def _check_properties(w, k, v, codec, out, ok, ov):
             assert bool((err <= bound).all()), f"error bound broken at kv={kv} layer={l}"
 
 
+@pytest.mark.parametrize("fmt", [1, 2])
 @pytest.mark.parametrize("name", ["ctx32k", "stress80k"])
-def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name):
+def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name, fmt):
     w = synth_mod.WORKLOADS[name]
     k, v = synth_mod.generate_device(w)
     codec = cg.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens,
-                     capacity=w.elements // 2)
+                     capacity=w.elements // 2, fmt=fmt)
     out = codec.compress(k, v)
     ok, ov = codec.decompress()
     torch.cuda.synchronize()
@@ -106,4 +121,4 @@ def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name)
     assert int(codec.dstatus.item()) == 0
     _check_properties(w, k, v, codec, out, ok, ov)
     for kc, kv, l in _samples(w, seed=len(name)):
-        _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l)
+        _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt)
