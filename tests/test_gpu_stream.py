@@ -53,3 +53,34 @@ def test_stream_rejects_pageable_input(synth_mod):
     sc = StreamingCodec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens)
     with pytest.raises(ValueError):
         sc.compress_from_host(torch.from_numpy(k), torch.from_numpy(v))
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_stream_with_delta_matches_oracle(synth_mod, oracle_mod, fmt):
+    """Pieces of whole chunks code independently with the token-locality
+    delta too (its groups are chunk-local): joined, they equal the oracle's
+    whole-tensor output, and the decompressed pieces its values."""
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required")
+    from kv_cache_compression_cg_gb300 import build
+    from kv_cache_compression_cg_gb300.stream import StreamingCodec
+    build.build()
+    w = synth_mod.WORKLOADS["mistral_chunk"]
+    T, Tc, G = 224, 64, 10
+    k, v = synth_mod.generate(w, T=T)
+    k_pin = torch.from_numpy(k).pin_memory()
+    v_pin = torch.from_numpy(v).pin_memory()
+    sc = StreamingCodec(w.L, T, w.C, w.bins_k, w.bins_v, chunk_tokens=Tc, piece_chunks=2, fmt=fmt, group=G)
+    pieces, outs, done = sc.roundtrip(k_pin, v_pin)
+    done.synchronize()
+    assert sc.status() == 0
+    joined = shard.assemble([hp.arrays() for hp in pieces])
+    ref = oracle_mod.compress_ex(k, v, Tc, w.bins_k, w.bins_v, fmt=fmt, group=G)
+    side = "cdf" if fmt == 1 else "rec"
+    for key in ("max1", side, "packed", "len", "off"):
+        assert np.array_equal(joined[key], ref[key]), key
+    wk, wv = oracle_mod.decompress_ex(ref["packed"], ref["off"], ref["len"], ref[side], ref["max1"], w.L, T, w.C,
+                                      Tc, w.bins_k, w.bins_v, fmt=fmt, group=G)
+    for (ok, ov), hp in zip(outs, pieces):
+        assert np.array_equal(ok.cpu().numpy().view(np.uint32), wk[:, hp.t0:hp.t1].view(np.uint32))
+        assert np.array_equal(ov.cpu().numpy().view(np.uint32), wv[:, hp.t0:hp.t1].view(np.uint32))
