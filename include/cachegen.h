@@ -330,7 +330,8 @@ cg_status cg_dequantize_delta(const uint8_t *sym, const uint16_t *max1,
  * cg_cdf_elems) or uint8 count records (format 2, cg_record_bytes).
  * Workspace: cg_compress_workspace_bytes. Format 2 has the limits of
  * cg_compress_chunk_v2; format 1 takes any shape. Decode with
- * cg_decompress_chunk_ex and the same format and group. */
+ * cg_decompress_chunk_ex and the same format and group (chunk_tokens <= 256),
+ * or, in format 1 with any chunk size, cg_decode then cg_dequantize_delta. */
 cg_status cg_compress_chunk_ex(const uint16_t *k, const uint16_t *v,
                                const cg_shape *shape, const int32_t *bins_k,
                                const int32_t *bins_v, int format,
