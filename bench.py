@@ -338,7 +338,7 @@ def run_ours(args):
     roofline = {
         "kernel": kname, "bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Tops/s",
         "frac": achieved / peak_tops,
-        "traffic": kernel_traffic(f"{kname.split()[0]}_f{args.format}_g{args.group}", srcs),
+        "traffic": kernel_traffic(f"{kname.split()[0]}_{args.workload}_f{args.format}_g{args.group}", srcs),
         "peak_kind": f"derived: {props.multi_processor_count} SMs x 4 schedulers x 32 lanes x {max_mhz:g} MHz",
         "ops_per_symbol": ops, "algorithmic_bytes": kbytes, "ms": kms,
         "hbm": {"achieved": hbm_achieved, "peak": hbm, "unit": "GB/s", "frac": hbm_achieved / hbm,

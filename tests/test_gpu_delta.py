@@ -176,3 +176,47 @@ def test_fused_delta_full_workload(cg, oracle_mod, synth_mod):
                                       Tc, w.bins_k, w.bins_v, fmt=2, group=G)
     assert np.array_equal(ok.cpu().numpy().view(np.uint32), wk.view(np.uint32))
     assert np.array_equal(ov.cpu().numpy().view(np.uint32), wv.view(np.uint32))
+
+
+def test_long_chunks_decode_through_the_steps(cg, oracle_mod):
+    """Chunks over 256 tokens: cg_compress_chunk_ex (format 1) takes the step
+    kernels, and the symbols decode with cg_decode then cg_dequantize_delta;
+    both equal the oracle's."""
+    from kv_cache_compression_cg_gb300 import capi
+    import ctypes as C
+    L, T, C_, Tc, G = 2, 700, 32, 512, 10
+    bk, bv = [16, 32], [8, 16]
+    k = _correlated(7, L, T, C_)
+    v = _correlated(8, L, T, C_)
+    ref = oracle_mod.compress_ex(k, v, Tc, bk, bv, fmt=1, group=G)
+    lib = capi.load()
+    shp = cg.make_shape(L, T, C_, Tc)
+    bka, bva = np.array(bk, np.int32), np.array(bv, np.int32)
+    n_cdf = int(lib.cg_cdf_elems(C.byref(shp), bka.ctypes.data, bva.ctypes.data))
+    cap = int(lib.cg_max_compressed_bytes(C.byref(shp)))
+    ws_n = int(lib.cg_compress_workspace_bytes(C.byref(shp)))
+    dev = "cuda"
+    kt, vt = torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)
+    max1 = torch.empty((2, L, T), dtype=torch.int16, device=dev)
+    cdf = torch.empty(n_cdf, dtype=torch.int16, device=dev)
+    packed = torch.empty(cap, dtype=torch.uint8, device=dev)
+    ln = torch.empty(2 * L * T, dtype=torch.int32, device=dev)
+    off = torch.empty(2 * L * T + 1, dtype=torch.int64, device=dev)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    p = lambda t: C.c_void_p(t.data_ptr())
+    s = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    capi.check(lib.cg_compress_chunk_ex(p(kt), p(vt), C.byref(shp), bka.ctypes.data, bva.ctypes.data, 1, G, p(max1),
+                                        p(cdf), p(packed), cap, p(ln), p(off), p(ws), ws_n, p(st), s),
+               "cg_compress_chunk_ex")
+    sym = cg.decode(packed, off, ln, cdf, L, T, C_, bk, bv, chunk_tokens=Tc, status=st)
+    ok, ov = cg.dequantize_delta(sym, max1, G, bk, bv, chunk_tokens=Tc)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(max1.cpu().numpy().view(np.uint16), ref["max1"])
+    assert np.array_equal(cdf.cpu().numpy().view(np.uint16), ref["cdf"])
+    assert np.array_equal(packed[:int(ref["off"][-1])].cpu().numpy(), ref["packed"])
+    wk, wv = oracle_mod.decompress_ex(ref["packed"], ref["off"], ref["len"], ref["cdf"], ref["max1"], L, T, C_, Tc,
+                                      bk, bv, fmt=1, group=G)
+    assert np.array_equal(ok.cpu().numpy().view(np.uint32), wk.view(np.uint32))
+    assert np.array_equal(ov.cpu().numpy().view(np.uint32), wv.view(np.uint32))
