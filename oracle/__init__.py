@@ -81,6 +81,12 @@ def lib() -> C.CDLL:
                 "orc_compress_v2": (C.c_int, [p, p, C.c_int, C.c_int, C.c_int, C.c_int, i64,
                                               p, p, p, p, p, u64, p, p]),
                 "orc_decompress_v2": (C.c_int, [p, p, p, p, p] + [C.c_int] * 4 + [p, p, p, p]),
+                "orc_v3_fixed_bytes": (i64, [C.c_int] * 4),
+                "orc_v3_max_bytes": (i64, [C.c_int] * 4 + [p, p]),
+                "orc_records_to_v3": (i64, [p] + [C.c_int] * 4 + [p, p, p, i64]),
+                "orc_v3_to_records": (C.c_int, [p, i64] + [C.c_int] * 4 + [p, p, p]),
+                "orc_compress_v3": (C.c_int, [p, p] + [C.c_int] * 5 + [i64, p, p, p, p, i64, p, p, u64, p, p]),
+                "orc_decompress_v3": (C.c_int, [p, p, p, i64, p] + [C.c_int] * 5 + [p, p, p, p]),
                 "orc_half_up": (C.c_uint16, [C.c_float]),
                 "orc_floats_to_half": (None, [p, i64, p]),
                 "orc_quantize_delta": (C.c_int, [p, p] + [C.c_int] * 5 + [i64, p, p, p, p]),
@@ -510,4 +516,76 @@ def decompress_ex(packed, off, ln, side, max1, L, T, C_, Tc, bins_k, bins_v=None
                                    _ptr(np.ascontiguousarray(max1, np.uint16)),
                                    L, T, C_, Tc, group, fmt, _ptr(bk), _ptr(bv), _ptr(out_k), _ptr(out_v)),
            "decompress_ex")
+    return out_k, out_v
+
+
+# ----------------------------------------------------------------------------
+# format 3: compact count records
+# ----------------------------------------------------------------------------
+def v3_fixed_bytes(L, T, C_, Tc) -> int:
+    return int(lib().orc_v3_fixed_bytes(L, T, C_, Tc))
+
+
+def v3_max_bytes(L, T, C_, Tc, bins_k, bins_v=None) -> int:
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    return int(lib().orc_v3_max_bytes(L, T, C_, Tc, _ptr(bk), _ptr(bv)))
+
+
+def records_to_v3(rec, L, T, C_, Tc, bins_k, bins_v=None) -> np.ndarray:
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    cap = v3_max_bytes(L, T, C_, Tc, bk, bv)
+    side = np.zeros(max(cap, 1), np.uint8)
+    n = lib().orc_records_to_v3(_ptr(np.ascontiguousarray(rec, np.uint8)), L, T, C_, Tc, _ptr(bk), _ptr(bv),
+                                _ptr(side), cap)
+    if n < 0:
+        raise OracleError(int(-n), "records_to_v3")
+    return side[:n].copy()
+
+
+def v3_to_records(side, L, T, C_, Tc, bins_k, bins_v=None) -> np.ndarray:
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    side = np.ascontiguousarray(side, np.uint8)
+    rec = np.zeros(max(rec_bytes(L, T, C_, Tc, bk, bv), 1), np.uint8)
+    _check(lib().orc_v3_to_records(_ptr(side if side.size else np.zeros(1, np.uint8)), side.size, L, T, C_, Tc,
+                                   _ptr(bk), _ptr(bv), _ptr(rec)), "v3_to_records")
+    return rec[:rec_bytes(L, T, C_, Tc, bk, bv)]
+
+
+def compress_v3(k, v, Tc: int, bins_k, bins_v=None, group: int = 1):
+    """Format 3: returns max1, side (the whole side buffer), packed, len, off."""
+    k, v = _bits(k), _bits(v)
+    L, T, C_ = k.shape
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    ns = num_streams(L, T)
+    cap = max_compressed_bytes(L, T, C_)
+    scap = v3_max_bytes(L, T, C_, Tc, bk, bv)
+    max1 = np.empty((2, L, T), np.uint16)
+    side = np.zeros(max(scap, 1), np.uint8)
+    nside = np.zeros(1, np.int64)
+    packed = np.zeros(max(cap, 1), np.uint8)
+    ln = np.empty(max(ns, 1), np.uint32)
+    off = np.empty(ns + 1, np.uint64)
+    _check(lib().orc_compress_v3(_ptr(k), _ptr(v), L, T, C_, Tc, group, T * C_, _ptr(bk), _ptr(bv), _ptr(max1),
+                                 _ptr(side), scap, _ptr(nside), _ptr(packed), cap, _ptr(ln), _ptr(off)),
+           "compress_v3")
+    return {"max1": max1, "side": side[:int(nside[0])].copy(), "packed": packed[:int(off[-1])].copy(),
+            "len": ln[:ns], "off": off}
+
+
+def decompress_v3(packed, ln, side, max1, L, T, C_, Tc, bins_k, bins_v=None, group: int = 1):
+    bk = _bins(bins_k, L)
+    bv = _bins(bins_k if bins_v is None else bins_v, L)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    if packed.size == 0:
+        packed = np.zeros(1, np.uint8)
+    side = np.ascontiguousarray(side, np.uint8)
+    out_k = np.empty((L, T, C_), np.float32)
+    out_v = np.empty((L, T, C_), np.float32)
+    _check(lib().orc_decompress_v3(_ptr(packed), _ptr(np.ascontiguousarray(ln, np.uint32)), _ptr(side), side.size,
+                                   _ptr(np.ascontiguousarray(max1, np.uint16)), L, T, C_, Tc, group, _ptr(bk),
+                                   _ptr(bv), _ptr(out_k), _ptr(out_v)), "decompress_v3")
     return out_k, out_v

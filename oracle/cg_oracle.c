@@ -960,3 +960,218 @@ int orc_decompress_ex(const uint8_t *packed, const uint64_t *off,
     free(sym);
     return st;
 }
+
+/* ---- format 3: compact count records ------------------------------------- */
+
+static void orc_put_le(uint8_t *p, uint64_t v, int nbytes)
+{
+    for (int i = 0; i < nbytes; i++)
+        p[i] = (uint8_t)(v >> (8 * i));
+}
+
+static uint64_t orc_get_le(const uint8_t *p, int nbytes)
+{
+    uint64_t v = 0;
+    for (int i = 0; i < nbytes; i++)
+        v |= (uint64_t)p[i] << (8 * i);
+    return v;
+}
+
+/* Byte offsets of M, B and V in the side buffer; 0 when format 3 does not
+ * apply to the shape. */
+static int64_t orc_v3_layout(int L, int T, int C, int Tc, int64_t *offM,
+                             int64_t *offB, int64_t *nslice)
+{
+    if (!orc_check_shape(L, T, C) || Tc < 1 || Tc > 256)
+        return 0;
+    int64_t nch = (T + Tc - 1) / Tc;
+    int64_t ns = 2 * (int64_t)L * nch, nrec = ns * C;
+    *nslice = ns;
+    *offM = 8 * (ns + 1);
+    *offB = (*offM + nrec + 3) / 4 * 4;
+    return *offB + 4 * nrec; /* offV */
+}
+
+static int orc_v3_bins_ok(int L, const int32_t *bins_k, const int32_t *bins_v)
+{
+    for (int l = 0; l < L; l++)
+        if (bins_k[l] < 4 || bins_v[l] < 4 || orc_alphabet_v2(bins_k[l]) > 32 ||
+            orc_alphabet_v2(bins_v[l]) > 32)
+            return 0;
+    return 1;
+}
+
+int64_t orc_v3_fixed_bytes(int L, int T, int C, int Tc)
+{
+    int64_t offM, offB, ns;
+    return orc_v3_layout(L, T, C, Tc, &offM, &offB, &ns);
+}
+
+int64_t orc_v3_max_bytes(int L, int T, int C, int Tc, const int32_t *bins_k,
+                         const int32_t *bins_v)
+{
+    if (!bins_v)
+        bins_v = bins_k;
+    int64_t offM, offB, ns;
+    int64_t offV = orc_v3_layout(L, T, C, Tc, &offM, &offB, &ns);
+    if (offV == 0 || !orc_v3_bins_ok(L, bins_k, bins_v))
+        return 0;
+    int64_t per_chunk = 0;
+    for (int l = 0; l < L; l++)
+        per_chunk += (int64_t)C * (orc_alphabet_v2(bins_k[l]) - 1 + orc_alphabet_v2(bins_v[l]) - 1);
+    return offV + per_chunk * ((T + Tc - 1) / Tc);
+}
+
+/* A record's byte 1 + i holds the count of the i-th symbol other than the
+ * mode, in increasing order. */
+static int orc_other_symbol(int i, int mode)
+{
+    return i < mode ? i : i + 1;
+}
+
+int64_t orc_records_to_v3(const uint8_t *rec, int L, int T, int C, int Tc,
+                          const int32_t *bins_k, const int32_t *bins_v,
+                          uint8_t *side, int64_t capacity)
+{
+    if (!bins_v)
+        bins_v = bins_k;
+    int64_t offM, offB, ns;
+    int64_t offV = orc_v3_layout(L, T, C, Tc, &offM, &offB, &ns);
+    if (offV == 0 || !orc_v3_bins_ok(L, bins_k, bins_v) || capacity < offV)
+        return -ORC_ERR_ARG;
+    memset(side, 0, (size_t)offV);
+    int nch = (T + Tc - 1) / Tc;
+    int64_t pos = 0; /* bytes of V so far */
+    for (int kc = 0; kc < nch; kc++)
+        for (int kv = 0; kv < 2; kv++)
+            for (int l = 0; l < L; l++) {
+                int64_t s = ((int64_t)kc * 2 + kv) * L + l;
+                int A = orc_alphabet_v2((kv ? bins_v : bins_k)[l]);
+                orc_put_le(side + 8 * s, (uint64_t)pos, 8);
+                for (int c = 0; c < C; c++) {
+                    const uint8_t *r = rec + orc_rec_offset(L, C, bins_k, bins_v, kc, kv, l, c);
+                    int mode = r[0];
+                    if (mode >= A)
+                        return -ORC_ERR_CORRUPT;
+                    uint32_t bits = 0;
+                    for (int i = 0; i < A - 1; i++) {
+                        if (r[1 + i] == 0)
+                            continue;
+                        bits |= 1u << orc_other_symbol(i, mode);
+                        if (offV + pos >= capacity)
+                            return -ORC_ERR_CAPACITY;
+                        side[offV + pos++] = r[1 + i];
+                    }
+                    side[offM + s * C + c] = (uint8_t)mode;
+                    orc_put_le(side + offB + 4 * (s * C + c), bits, 4);
+                }
+            }
+    orc_put_le(side + 8 * ns, (uint64_t)pos, 8);
+    return offV + pos;
+}
+
+int orc_v3_to_records(const uint8_t *side, int64_t nbytes, int L, int T, int C,
+                      int Tc, const int32_t *bins_k, const int32_t *bins_v,
+                      uint8_t *rec)
+{
+    if (!bins_v)
+        bins_v = bins_k;
+    int64_t offM, offB, ns;
+    int64_t offV = orc_v3_layout(L, T, C, Tc, &offM, &offB, &ns);
+    if (offV == 0 || !orc_v3_bins_ok(L, bins_k, bins_v))
+        return ORC_ERR_ARG;
+    if (nbytes < offV || orc_get_le(side, 8) != 0)
+        return ORC_ERR_CORRUPT;
+    uint64_t vtotal = orc_get_le(side + 8 * ns, 8);
+    if (vtotal > (uint64_t)(nbytes - offV))
+        return ORC_ERR_CORRUPT;
+    int nch = (T + Tc - 1) / Tc;
+    for (int kc = 0; kc < nch; kc++)
+        for (int kv = 0; kv < 2; kv++)
+            for (int l = 0; l < L; l++) {
+                int64_t s = ((int64_t)kc * 2 + kv) * L + l;
+                int A = orc_alphabet_v2((kv ? bins_v : bins_k)[l]);
+                uint64_t pos = orc_get_le(side + 8 * s, 8);
+                uint64_t end = orc_get_le(side + 8 * (s + 1), 8);
+                if (pos > end || end > vtotal)
+                    return ORC_ERR_CORRUPT;
+                for (int c = 0; c < C; c++) {
+                    uint8_t *r = rec + orc_rec_offset(L, C, bins_k, bins_v, kc, kv, l, c);
+                    int mode = side[offM + s * C + c];
+                    uint32_t bits = (uint32_t)orc_get_le(side + offB + 4 * (s * C + c), 4);
+                    if (mode >= A || (A < 32 && (bits >> A) != 0) || ((bits >> mode) & 1u))
+                        return ORC_ERR_CORRUPT;
+                    r[0] = (uint8_t)mode;
+                    for (int i = 0; i < A - 1; i++) {
+                        int t = orc_other_symbol(i, mode);
+                        r[1 + i] = 0;
+                        if ((bits >> t) & 1u) {
+                            if (pos >= end || side[offV + pos] == 0)
+                                return ORC_ERR_CORRUPT;
+                            r[1 + i] = side[offV + pos++];
+                        }
+                    }
+                }
+                if (pos != end)
+                    return ORC_ERR_CORRUPT;
+            }
+    return ORC_OK;
+}
+
+int orc_compress_v3(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                    int Tc, int G, int64_t layer_stride, const int32_t *bins_k,
+                    const int32_t *bins_v, uint16_t *max1, uint8_t *side,
+                    int64_t side_capacity, int64_t *side_bytes,
+                    uint8_t *packed, uint64_t capacity, uint32_t *len,
+                    uint64_t *off)
+{
+    if (!bins_v)
+        bins_v = bins_k;
+    int64_t nrec = orc_rec_bytes(L, T, C, Tc, bins_k, bins_v);
+    if (nrec <= 0 || orc_v3_fixed_bytes(L, T, C, Tc) == 0 || !orc_v3_bins_ok(L, bins_k, bins_v))
+        return ORC_ERR_ARG;
+    uint8_t *rec = (uint8_t *)malloc((size_t)nrec);
+    if (!rec)
+        return ORC_ERR_NOMEM;
+    int st = orc_compress_ex(k, v, L, T, C, Tc, G, 2, layer_stride, bins_k, bins_v, max1, rec,
+                             packed, capacity, len, off);
+    if (st == ORC_OK || st == ORC_ERR_CAPACITY) {
+        int64_t n = orc_records_to_v3(rec, L, T, C, Tc, bins_k, bins_v, side, side_capacity);
+        if (n < 0)
+            st = (int)-n;
+        else
+            *side_bytes = n;
+    }
+    free(rec);
+    return st;
+}
+
+int orc_decompress_v3(const uint8_t *packed, const uint32_t *len,
+                      const uint8_t *side, int64_t side_bytes,
+                      const uint16_t *max1, int L, int T, int C, int Tc, int G,
+                      const int32_t *bins_k, const int32_t *bins_v,
+                      float *out_k, float *out_v)
+{
+    if (!bins_v)
+        bins_v = bins_k;
+    int64_t nrec = orc_rec_bytes(L, T, C, Tc, bins_k, bins_v);
+    int64_t ns = orc_num_streams(L, T);
+    if (nrec <= 0)
+        return ORC_ERR_ARG;
+    uint8_t *rec = (uint8_t *)malloc((size_t)nrec);
+    uint64_t *off = (uint64_t *)malloc((size_t)(ns + 1) * sizeof(uint64_t));
+    if (!rec || !off) {
+        free(rec), free(off);
+        return ORC_ERR_NOMEM;
+    }
+    /* the offsets are the exclusive scan of the lengths */
+    off[0] = 0;
+    for (int64_t i = 0; i < ns; i++)
+        off[i + 1] = off[i] + len[i];
+    int st = orc_v3_to_records(side, side_bytes, L, T, C, Tc, bins_k, bins_v, rec);
+    if (st == ORC_OK)
+        st = orc_decompress_ex(packed, off, len, rec, max1, L, T, C, Tc, G, 2, bins_k, bins_v,
+                               out_k, out_v);
+    free(rec), free(off);
+    return st;
+}

@@ -85,6 +85,22 @@
  *    mode byte.
  *
  * ---------------------------------------------------------------------------
+ * Format version 3: compact count records
+ * ---------------------------------------------------------------------------
+ * Format 2's counts, stored without its zero bytes; the CDFs, and so the
+ * streams, are format 2's. Requires Tc <= 256 and every A_l <= 32. Slices
+ * s = (k*2 + kv)*L + l (nslice = 2*L*nch); records r = s*C + c
+ * (nrec = nslice*C). One side buffer, little-endian:
+ *   O  uint64 [nslice + 1] at byte 0: O[s] = offset of slice s's counts in
+ *      V, O[nslice] = |V|;
+ *   M  uint8 [nrec] at byte offM = 8*(nslice + 1): each record's mode;
+ *   B  uint32 [nrec] at byte offB = offM + nrec rounded up to a multiple
+ *      of 4: bit t set iff t != mode and n_t > 0 (t < A_l);
+ *   V  uint8 at byte offV = offB + 4*nrec: for each record in order, its
+ *      set bits' counts n_t in increasing t, one byte each.
+ * Size offV + O[nslice]. Only the stream lengths travel with it (the
+ * offsets are their exclusive scan).
+ * ---------------------------------------------------------------------------
  * Token-locality delta: the change-based encoding of [CG §1.2(1)]
  * ---------------------------------------------------------------------------
  * The page's design codes each token's change from a nearby token rather than
@@ -232,6 +248,38 @@ uint16_t orc_float_to_half(float x);
 int orc_dequantize_half(const uint8_t *sym, const uint16_t *max1, int L, int T,
                         int C, const int32_t *bins_k, const int32_t *bins_v,
                         uint16_t *out_k, uint16_t *out_v);
+
+/* ---- format 3: compact count records ------------------------------------- */
+/* Fixed part of the side buffer (offV) and its largest size; 0 when the
+ * shape, the bins or Tc do not allow format 3. */
+int64_t orc_v3_fixed_bytes(int L, int T, int C, int Tc);
+int64_t orc_v3_max_bytes(int L, int T, int C, int Tc, const int32_t *bins_k,
+                         const int32_t *bins_v);
+/* Format 2 records -> format 3 side buffer (size returned, < 0 on error). */
+int64_t orc_records_to_v3(const uint8_t *rec, int L, int T, int C, int Tc,
+                          const int32_t *bins_k, const int32_t *bins_v,
+                          uint8_t *side, int64_t capacity);
+/* Format 3 side buffer (nbytes readable) -> format 2 records; an error for
+ * a buffer that is not one the encoder can produce (offsets out of order or
+ * past the buffer, a mode outside the alphabet, a bit at or past A or at the
+ * mode, a slice whose bits disagree with its offsets). */
+int orc_v3_to_records(const uint8_t *side, int64_t nbytes, int L, int T, int C,
+                      int Tc, const int32_t *bins_k, const int32_t *bins_v,
+                      uint8_t *rec);
+/* Compress in format 3 (with token groups of G; 1: none): max1, side
+ * buffer (size in *side_bytes), packed, len (and off). */
+int orc_compress_v3(const uint16_t *k, const uint16_t *v, int L, int T, int C,
+                    int Tc, int G, int64_t layer_stride, const int32_t *bins_k,
+                    const int32_t *bins_v, uint16_t *max1, uint8_t *side,
+                    int64_t side_capacity, int64_t *side_bytes,
+                    uint8_t *packed, uint64_t capacity, uint32_t *len,
+                    uint64_t *off);
+/* Decompress format 3 from the lengths alone (offsets rebuilt), binary32. */
+int orc_decompress_v3(const uint8_t *packed, const uint32_t *len,
+                      const uint8_t *side, int64_t side_bytes,
+                      const uint16_t *max1, int L, int T, int C, int Tc, int G,
+                      const int32_t *bins_k, const int32_t *bins_v,
+                      float *out_k, float *out_v);
 
 /* ---- token-locality delta (specification G) ------------------------------ */
 /* The smallest binary16 value >= m (m finite, >= 0), as bits; 0x7BFF (the
