@@ -30,7 +30,8 @@ sys.path.insert(0, ROOT)
 METRIC = "KV encode & decode GB/s (fp16 in) at 1 GB300, % of HBM roofline; compression ratio"
 UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
-KERNELS_PER_STEP = 4  # compress_init, compress_tma, pack, decode_pipe (the ctx4096 shape takes the fused paths)
+KERNELS_PER_STEP = 4  # compress_init, compress_tma, pack, decode_pipe (the ctx4096 shape takes the fused paths);
+# format 3 adds its side-buffer packing (3), the offset scan (3) and the record unpacking (1)
 
 
 def parse():
@@ -41,8 +42,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ctx4096")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--format", type=int, choices=[1, 2], default=2,
-                    help="side information: 1 = CDF entries, 2 = symbol-count records")
+    ap.add_argument("--format", type=int, choices=[1, 2, 3], default=2,
+                    help="side information: 1 = CDF entries, 2 = symbol-count records, "
+                         "3 = compact count records (offsets rebuilt from the lengths)")
     ap.add_argument("--piece-chunks", type=int, default=2,
                     help="chunks per piece of the streamed end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -171,7 +173,11 @@ def oracle_step_time(k, v, w, tokens, fmt=2, group=1):
     ks = k[:, :tokens].copy()
     vs = v[:, :tokens].copy()
     t0 = time.perf_counter()
-    if group > 1:
+    if fmt == 3:
+        r = oracle.compress_v3(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v, group=group)
+        oracle.decompress_v3(r["packed"], r["len"], r["side"], r["max1"], w.L, tokens, w.C, w.chunk_tokens,
+                             w.bins_k, w.bins_v, group=group)
+    elif group > 1:
         r = oracle.compress_ex(ks, vs, w.chunk_tokens, w.bins_k, w.bins_v, fmt=fmt, group=group)
         oracle.decompress_ex(r["packed"], r["off"], r["len"], r["cdf" if fmt == 1 else "rec"], r["max1"], w.L,
                              tokens, w.C, w.chunk_tokens, w.bins_k, w.bins_v, fmt=fmt, group=group)
@@ -313,12 +319,14 @@ def run_ours(args):
     comp_kernel_ms = time_call(lambda: cd.compress(k, v))
     dec_kernel_ms = time_call(cd.decompress)
     n_el = 2 * w.L * w.T * w.C
-    cdf_bytes = 2 * cd.cdf_elems if args.format == 1 else cd.rec_bytes  # side information
-    side = cdf_bytes + 2 * 2 * w.L * w.T + 4 * cd.nstreams + 8 * (cd.nstreams + 1)
+    # side information that travels with the streams: CDF entries, count records or the
+    # format 3 side buffer; max1; lengths; offsets (format 3 rebuilds them from the lengths)
+    side_info = {1: 2 * cd.cdf_elems, 2: cd.rec_bytes}.get(args.format) or out.side3_bytes()
+    side = side_info + 2 * 2 * w.L * w.T + 4 * cd.nstreams + (8 * (cd.nstreams + 1) if args.format < 3 else 0)
     dec_alg_bytes = total + side + 4 * n_el
     comp_alg_bytes = fp16_bytes + total + side
     A = max(max(w.bins_k), max(w.bins_v))
-    if args.format == 2:  # the largest layer alphabet, 2 * MAX + 1
+    if args.format >= 2:  # the largest layer alphabet, 2 * MAX + 1
         A = max(2 * (b // 2 - 1) + 1 for b in list(w.bins_k) + list(w.bins_v))
     P = 1 << (A - 1).bit_length()
     props = torch.cuda.get_device_properties(local)
@@ -366,7 +374,7 @@ def run_ours(args):
         "roofline": roofline,
         "reconstruction_rel_rmse": rel_rmse,
         "status_word": status, "clocks": clocks, "wall_s_timed_region": wall,
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (KERNELS_PER_STEP + (7 if args.format == 3 else 0)) * args.steps,
     }
 
     if not args.no_e2e:

@@ -267,6 +267,60 @@ cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes,
                                  float *out_v, int32_t *status,
                                  cudaStream_t stream);
 
+/* ---- format 3: compact count records ------------------------------------
+ * Format 2's counts without their zero bytes [CG §2.3(2)]: the CDFs, and so
+ * the streams, are format 2's. Requires chunk_tokens <= 256 and every layer
+ * alphabet A_l = 2*MAX_l + 1 <= 32. Slices s = (k*2 + kv)*L + l (nslice =
+ * 2*L*nch), records r = s*C + c (nrec = nslice*C). One side buffer,
+ * little-endian:
+ * O  uint64 [nslice + 1] at byte 0: O[s] = offset of slice s's counts in V;
+ *    O[nslice] = |V|;
+ * M  uint8 [nrec] at byte offM = 8*(nslice + 1): each record's mode;
+ * B  uint32 [nrec] at offB = offM + nrec rounded up to a multiple of 4:
+ *    bit t set iff t != mode and the count of symbol t is > 0;
+ * V  uint8 at offV = offB + 4*nrec (= cg_side3_fixed_bytes): for each record
+ *    in order, the counts of its set bits in increasing t, one byte each.
+ * Its size is offV + O[nslice]. Only the stream lengths travel with it: the
+ * offsets are their exclusive scan, which the decompressor rebuilds.
+ */
+
+/* offV, or 0 when chunk_tokens > 256 or the shape is invalid. */
+uint64_t cg_side3_fixed_bytes(const cg_shape *shape);
+/* The largest side buffer for these bins (capacity to pass to
+ * cg_compress_chunk_v3); 0 when format 3 does not apply. */
+uint64_t cg_side3_max_bytes(const cg_shape *shape, const int32_t *bins_k,
+                            const int32_t *bins_v);
+/* Device workspace of cg_compress_chunk_v3 and cg_decompress_chunk_v3. */
+uint64_t cg_workspace_bytes_v3(const cg_shape *shape, const int32_t *bins_k,
+                               const int32_t *bins_v);
+
+/* Compress in format 3 with token-locality groups of `group` (1: none):
+ * max1, the side buffer (side_capacity >= cg_side3_max_bytes; its size is
+ * cg_side3_fixed_bytes + O[nslice], the uint64 at byte 8*nslice), packed,
+ * len and off. The limits of cg_compress_chunk_v2 apply. side must be 8-byte
+ * aligned. */
+cg_status cg_compress_chunk_v3(const uint16_t *k, const uint16_t *v,
+                               const cg_shape *shape, const int32_t *bins_k,
+                               const int32_t *bins_v, int32_t group,
+                               uint16_t *max1, uint8_t *side,
+                               uint64_t side_capacity, uint8_t *packed,
+                               uint64_t capacity, uint32_t *len, uint64_t *off,
+                               void *workspace, uint64_t workspace_bytes,
+                               int32_t *status, cudaStream_t stream);
+
+/* Decompress format 3 from the lengths (no offsets) and side_bytes of side
+ * buffer, into out_k / out_v as cg_decompress_chunk_ex. A side buffer the
+ * compressor cannot produce sets CG_FLAG_CORRUPT. */
+cg_status cg_decompress_chunk_v3(const uint8_t *packed, uint64_t packed_bytes,
+                                 const uint32_t *len, const uint8_t *side,
+                                 uint64_t side_bytes, const uint16_t *max1,
+                                 const cg_shape *shape, const int32_t *bins_k,
+                                 const int32_t *bins_v, int32_t group,
+                                 int out_dtype, void *out_k, void *out_v,
+                                 int64_t out_layer_stride, void *workspace,
+                                 uint64_t workspace_bytes, int32_t *status,
+                                 cudaStream_t stream);
+
 /* ---- serving layouts ----------------------------------------------------
  * Decompression straight into the layout a serving engine keeps its cache in
  * [CG §3.2] (K and V of a layer side by side: [L][2][T][C], i.e. out_v =

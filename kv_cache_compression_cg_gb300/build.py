@@ -16,8 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libcachegen_gb300.so")
-SOURCES = ["quant.cu", "codec.cu", "compress.cu", "decode.cu", "decode_delta.cu", "scan.cu", "capi.cu",
-           "noalloc.cu"]
+SOURCES = ["quant.cu", "codec.cu", "compress.cu", "decode.cu", "decode_delta.cu", "scan.cu", "records3.cu",
+           "capi.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "cg_internal.cuh"), os.path.join(CSRC, "coder.cuh"),
            os.path.join(CSRC, "decode_pipe.cuh"), os.path.join(ROOT, "include", "cachegen.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -58,6 +58,13 @@ SIGNATURES = {
     "cg_decompress_chunk_ex": (_i32, [_p, _u64, _p, _p, _p, _p, _SHAPE, _p, _p, C.c_int, C.c_int32, C.c_int,
                                       _p, _p, C.c_int64, _p, _p]),
     "cg_quantize_delta": (_i32, [_p, _p, _SHAPE, _p, _p, C.c_int32, _p, _p, _p, _p]),
+    "cg_side3_fixed_bytes": (_u64, [_SHAPE]),
+    "cg_side3_max_bytes": (_u64, [_SHAPE, _p, _p]),
+    "cg_workspace_bytes_v3": (_u64, [_SHAPE, _p, _p]),
+    "cg_compress_chunk_v3": (_i32, [_p, _p, _SHAPE, _p, _p, C.c_int32, _p, _p, _u64, _p, _u64, _p, _p, _p, _u64,
+                                    _p, _p]),
+    "cg_decompress_chunk_v3": (_i32, [_p, _u64, _p, _p, _u64, _p, _SHAPE, _p, _p, C.c_int32, C.c_int, _p, _p,
+                                      C.c_int64, _p, _u64, _p, _p]),
     "cg_dequantize_delta": (_i32, [_p, _p, _SHAPE, _p, _p, C.c_int32, _p, _p, _p, _p]),
     "cg_compress_chunk_ex": (_i32, [_p, _p, _SHAPE, _p, _p, C.c_int, C.c_int32, _p, _p, _p, _u64, _p, _p, _p,
                                     _u64, _p, _p]),

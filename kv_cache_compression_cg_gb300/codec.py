@@ -75,6 +75,14 @@ class Compressed:
     fmt: int = 1            # 1: CDF entries in `cdf`; 2: count records in `rec`
     rec: torch.Tensor | None = None  # uint8 [record bytes] (format 2)
     group: int = 1          # token-locality delta group (1: none)
+    side3: torch.Tensor | None = None  # uint8 [capacity] (format 3 side buffer)
+    side3_fixed: int = 0    # format 3: bytes before the counts (offV)
+
+    def side3_bytes(self) -> int:
+        """Format 3: the side buffer's size, offV + O[nslice]."""
+        ns = 2 * self.L * (-(-self.T // self.chunk_tokens))
+        vbytes = int(self.side3[8 * ns:8 * ns + 8].cpu().numpy().view(np.uint64)[0])
+        return self.side3_fixed + vbytes
 
     @property
     def shape(self) -> capi.cg_shape:
@@ -94,11 +102,12 @@ class Codec:
     def __init__(self, L: int, T: int, C_: int, bins_k, bins_v=None, chunk_tokens: int = 256,
                  capacity: int | None = None, device: str | torch.device = "cuda", fmt: int = 1,
                  group: int = 1):
-        """fmt: 1 (CDF entries) or 2 (count records); group: token-locality
+        """fmt: 1 (CDF entries), 2 (count records) or 3 (compact count
+        records; offsets rebuilt from the lengths); group: token-locality
         delta group size [CG §1.2(1)] (1: no delta; > 1 needs chunk_tokens
         <= 256 to decode)."""
-        if fmt not in (1, 2):
-            raise ValueError("fmt must be 1 (CDF entries) or 2 (count records)")
+        if fmt not in (1, 2, 3):
+            raise ValueError("fmt must be 1 (CDF entries), 2 (count records) or 3 (compact records)")
         if not 1 <= group <= 1024:
             raise ValueError("group must be in [1, 1024]")
         if group > 1 and chunk_tokens > 256:
@@ -113,13 +122,19 @@ class Codec:
         self.nstreams = int(lib.cg_num_streams(C.byref(shp)))
         self.cdf_elems = int(lib.cg_cdf_elems(C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v)))
         self.rec_bytes = int(lib.cg_record_bytes(C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v)))
-        if fmt == 2 and self.rec_bytes == 0 and T > 0:
-            raise ValueError("format 2 needs chunk_tokens <= 256")
+        if fmt >= 2 and self.rec_bytes == 0 and T > 0:
+            raise ValueError("formats 2 and 3 need chunk_tokens <= 256")
+        self.side3_cap = int(lib.cg_side3_max_bytes(C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v)))
+        if fmt == 3 and self.side3_cap == 0 and T > 0:
+            raise ValueError("format 3 needs every layer alphabet within 32 symbols")
         self.max_bytes = int(lib.cg_max_compressed_bytes(C.byref(shp)))
         if self.nstreams == 0 and T > 0 or self.cdf_elems == 0 and T > 0:
             raise ValueError("invalid shape or bins for the codec")
         self.capacity = self.max_bytes if capacity is None else int(capacity)
         self.ws_bytes = int(lib.cg_compress_workspace_bytes(C.byref(shp)))
+        if fmt == 3:
+            self.ws_bytes = max(self.ws_bytes, int(lib.cg_workspace_bytes_v3(
+                C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v))))
         dev = torch.device(device)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.out = Compressed(
@@ -131,7 +146,9 @@ class Codec:
             off=torch.empty(self.nstreams + 1, dtype=torch.int64, device=dev),
             status=torch.zeros(1, dtype=torch.int32, device=dev), fmt=fmt,
             rec=torch.empty(max(self.rec_bytes, 1), dtype=torch.uint8, device=dev) if fmt == 2 else None,
-            group=group)
+            group=group,
+            side3=torch.empty(max(self.side3_cap, 8), dtype=torch.uint8, device=dev) if fmt == 3 else None,
+            side3_fixed=int(lib.cg_side3_fixed_bytes(C.byref(shp))) if fmt == 3 else 0)
         self.out_k = torch.empty((L, T, C_), dtype=torch.float32, device=dev)
         self.out_v = torch.empty((L, T, C_), dtype=torch.float32, device=dev)
         self.dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -141,6 +158,12 @@ class Codec:
         if (shp.L, shp.T, shp.C) != (self.L, self.T, self.C):
             raise ValueError("K/V shape differs from the codec's")
         o = self.out
+        if self.fmt == 3:
+            capi.check(capi.load().cg_compress_chunk_v3(
+                _ptr(k), _ptr(v), C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v), self.group,
+                _ptr(o.max1), _ptr(o.side3), self.side3_cap, _ptr(o.packed), self.capacity, _ptr(o.len), _ptr(o.off),
+                _ptr(self.workspace), self.ws_bytes, _ptr(o.status), _stream(stream)), "cg_compress_chunk_v3")
+            return o
         if self.group > 1:
             capi.check(capi.load().cg_compress_chunk_ex(
                 _ptr(k), _ptr(v), C.byref(shp), _np_ptr(self.bins_k), _np_ptr(self.bins_v), self.fmt, self.group,
@@ -165,7 +188,7 @@ class Codec:
     def decompress(self, c: Compressed | None = None, stream=None):
         c = self.out if c is None else c
         shp = make_shape(c.L, c.T, c.C, c.chunk_tokens)
-        if c.group > 1:
+        if c.group > 1 or c.fmt == 3:
             self.decompress_into(self.out_k, self.out_v, c, stream)
             return self.out_k, self.out_v
         if c.fmt == 2:
@@ -195,6 +218,14 @@ class Codec:
         if out_k.stride(2) != 1 or out_k.stride(1) != c.C or out_v.stride() != out_k.stride():
             raise ValueError("outputs need contiguous [T, C] planes with equal layer strides")
         shp = make_shape(c.L, c.T, c.C, c.chunk_tokens)
+        if c.fmt == 3:
+            capi.check(capi.load().cg_decompress_chunk_v3(
+                _ptr(c.packed), c.packed.numel(), _ptr(c.len), _ptr(c.side3), c.side3.numel(), _ptr(c.max1),
+                C.byref(shp), _np_ptr(c.bins_k), _np_ptr(c.bins_v), c.group,
+                capi.CG_OUT_F16 if out_k.dtype == torch.float16 else capi.CG_OUT_F32,
+                _ptr(out_k), _ptr(out_v), out_k.stride(0), _ptr(self.workspace), self.ws_bytes,
+                _ptr(self.dstatus), _stream(stream)), "cg_decompress_chunk_v3")
+            return
         side = c.cdf if c.fmt == 1 else c.rec
         capi.check(capi.load().cg_decompress_chunk_ex(
             _ptr(c.packed), c.packed.numel(), _ptr(c.off), _ptr(c.len), _ptr(side), _ptr(c.max1),

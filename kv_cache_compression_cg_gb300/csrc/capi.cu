@@ -120,6 +120,35 @@ cg_status launched(cudaError_t e) { return e == cudaSuccess ? CG_OK : CG_ERR_CUD
 
 bool group_ok(int32_t g) { return g >= 1 && g <= CG_MAX_CHUNK_TOKENS; }
 
+// Format 3: chunks of at most 256 tokens and every layer alphabet within a
+// 32-bit presence mask.
+bool v3_ok(const Dims &d, const MaxTab &mt) { return d.Tc <= 256 && max_alphabet_v2(d, mt) <= 32; }
+
+uint64_t v3_fixed_bytes(const Dims &d) {
+    long long offM, offB, offV;
+    cg::v3_layout(d, offM, offB, offV);
+    return (uint64_t)offV;
+}
+
+uint64_t v3_max_bytes(const Dims &d, const MaxTab &mt) {
+    uint64_t per = 0;
+    for (int kv = 0; kv < 2; kv++)
+        for (int l = 0; l < d.L; l++) per += 2ull * mt.v[kv][l];  // A - 1 count bytes at most
+    return v3_fixed_bytes(d) + (uint64_t)d.nch * (uint64_t)d.C * per;
+}
+
+// Format 3 scratch: compress = the fused compress workspace, the format 2
+// records and the slice totals; decompress = offsets, scan partials and the
+// records. One size covers both.
+uint64_t v3_workspace_bytes(const Dims &d, const MaxTab &mt) {
+    const uint64_t rec = round_up(record_bytes(d, mt), kAlign);
+    const uint64_t comp = encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d) + rec +
+                          round_up(8ull * (2ull * d.L * d.nch + 1), kAlign);
+    const uint64_t dec = round_up(8ull * (d.nstreams + 1), kAlign) +
+                         round_up(8ull * (uint64_t)(cg::scan_tiles(d.nstreams) + 1), kAlign) + rec;
+    return comp > dec ? comp : dec;
+}
+
 // Empty token range: only off[0] = 0 has to be written.
 cg_status empty_offsets(uint64_t *off, cudaStream_t stream) {
     if (!off) return CG_OK;
@@ -163,7 +192,7 @@ uint64_t cg_compress_workspace_bytes(const cg_shape *shape) {
     return encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d);
 }
 
-const char *cg_version(void) { return "cachegen-gb300 formats-1,2 delta sm_103a"; }
+const char *cg_version(void) { return "cachegen-gb300 formats-1,2,3 delta sm_103a"; }
 
 cg_status cg_quantize(const uint16_t *k, const uint16_t *v, const cg_shape *shape,
                       const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym, uint16_t *max1,
@@ -412,6 +441,90 @@ cg_status cg_compress_chunk_ex(const uint16_t *k, const uint16_t *v, const cg_sh
     if (cg::launch_code_slices(w.sym, nullptr, cdf, w.stage, len, d, 2, status, stream) != cudaSuccess)
         return CG_ERR_CUDA;
     return launched(cg::launch_scan_and_pack(len, off, w.stage, packed, capacity, w.partials, d, status, stream));
+}
+
+uint64_t cg_side3_fixed_bytes(const cg_shape *shape) {
+    Dims d;
+    int32_t b[CG_MAX_LAYERS];
+    if (!shape_ok(shape)) return 0;
+    for (int l = 0; l < shape->L; l++) b[l] = 4;
+    prepare(shape, b, b, d, nullptr);
+    return d.Tc <= 256 ? v3_fixed_bytes(d) : 0;
+}
+
+uint64_t cg_side3_max_bytes(const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || !v3_ok(d, mt)) return 0;
+    return v3_max_bytes(d, mt);
+}
+
+uint64_t cg_workspace_bytes_v3(const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || !v3_ok(d, mt)) return 0;
+    return v3_workspace_bytes(d, mt);
+}
+
+cg_status cg_compress_chunk_v3(const uint16_t *k, const uint16_t *v, const cg_shape *shape, const int32_t *bins_k,
+                               const int32_t *bins_v, int32_t group, uint16_t *max1, uint8_t *side,
+                               uint64_t side_capacity, uint8_t *packed, uint64_t capacity, uint32_t *len,
+                               uint64_t *off, void *workspace, uint64_t workspace_bytes, int32_t *status,
+                               cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || !v3_ok(d, mt) || !group_ok(group)) return CG_ERR_INVALID_ARG;
+    if (!off) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return empty_offsets(off, stream);
+    if (!k || !v || !max1 || !side || !len || !workspace || (!packed && capacity > 0)) return CG_ERR_INVALID_ARG;
+    if (!aligned(k, 2) || !aligned(v, 2) || !aligned(max1, 2) || !aligned(side, 8) || !aligned(len, 4) ||
+        !aligned(off, 8) || !aligned(workspace, kAlign))
+        return CG_ERR_INVALID_ARG;
+    if (side_capacity < v3_max_bytes(d, mt)) return CG_ERR_INVALID_ARG;
+    if (workspace_bytes < v3_workspace_bytes(d, mt)) return CG_ERR_WORKSPACE;
+    d.G = group;
+    Dims d2 = d;  // the fused kernel's limits, with format 2's alphabet
+    d2.A[0] = d2.A[1] = max_alphabet_v2(d, mt);
+    if (!cg::compress_fused_applies(d2, k, v)) return CG_ERR_INVALID_ARG;
+    Workspace w = carve(workspace, d, true);
+    uint8_t *rec = static_cast<uint8_t *>(workspace) + encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d);
+    auto *totals = reinterpret_cast<unsigned long long *>(rec + round_up(record_bytes(d, mt), kAlign));
+    if (cg::launch_compress_fused(k, v, d, mt, max1, nullptr, rec, w.stage, len, off, packed, capacity, w.state,
+                                  status, stream) != cudaSuccess)
+        return CG_ERR_CUDA;
+    return launched(cg::launch_v3_pack(rec, d, mt, side, totals, stream));
+}
+
+cg_status cg_decompress_chunk_v3(const uint8_t *packed, uint64_t packed_bytes, const uint32_t *len,
+                                 const uint8_t *side, uint64_t side_bytes, const uint16_t *max1,
+                                 const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v,
+                                 int32_t group, int out_dtype, void *out_k, void *out_v, int64_t out_layer_stride,
+                                 void *workspace, uint64_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    Dims d;
+    MaxTab mt;
+    if (!prepare(shape, bins_k, bins_v, d, &mt) || !v3_ok(d, mt) || !group_ok(group)) return CG_ERR_INVALID_ARG;
+    if (out_dtype != CG_OUT_F32 && out_dtype != CG_OUT_F16) return CG_ERR_INVALID_ARG;
+    if (out_layer_stride < (int64_t)d.T * d.C) return CG_ERR_INVALID_ARG;
+    if (d.T == 0) return CG_OK;
+    const uintptr_t es = out_dtype == CG_OUT_F16 ? 2 : 4;
+    if (!packed || !len || !side || !max1 || !out_k || !out_v || !workspace) return CG_ERR_INVALID_ARG;
+    if (!aligned(packed, 4) || !aligned(len, 4) || !aligned(side, 8) || !aligned(max1, 2) || !aligned(out_k, es) ||
+        !aligned(out_v, es) || !aligned(workspace, kAlign))
+        return CG_ERR_INVALID_ARG;
+    if (side_bytes < v3_fixed_bytes(d)) return CG_ERR_INVALID_ARG;
+    if (workspace_bytes < v3_workspace_bytes(d, mt)) return CG_ERR_WORKSPACE;
+    d.G = group;
+    uint8_t *p = static_cast<uint8_t *>(workspace);
+    auto *off = reinterpret_cast<uint64_t *>(p);
+    p += round_up(8ull * (d.nstreams + 1), kAlign);
+    auto *partials = reinterpret_cast<unsigned long long *>(p);
+    p += round_up(8ull * (uint64_t)(cg::scan_tiles(d.nstreams) + 1), kAlign);
+    uint8_t *rec = p;
+    if (cg::launch_offsets(len, off, partials, d, stream) != cudaSuccess) return CG_ERR_CUDA;
+    if (cg::launch_v3_unpack(side, side_bytes, d, mt, rec, status, stream) != cudaSuccess) return CG_ERR_CUDA;
+    return launched(cg::launch_decode_pipe(packed, packed_bytes, off, len, nullptr, rec, max1, d, mt,
+                                           out_dtype == CG_OUT_F16 ? 2 : 1, out_k, out_v, out_layer_stride, status,
+                                           stream));
 }
 
 }  // extern "C"

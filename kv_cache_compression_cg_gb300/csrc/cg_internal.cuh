@@ -128,6 +128,27 @@ cudaError_t launch_scan_and_pack(const uint32_t *len, uint64_t *off,
                                  uint64_t capacity, unsigned long long *partials,
                                  const Dims &d, int32_t *status, cudaStream_t s);
 
+// off = exclusive scan of len (off[nstreams] = total); partials as for
+// launch_scan_and_pack.
+cudaError_t launch_offsets(const uint32_t *len, uint64_t *off, unsigned long long *partials, const Dims &d,
+                           cudaStream_t s);
+
+// Format 3 side buffer <-> format 2 count records (layout in include/cachegen.h).
+// pack: totals holds nslices + 1 uint64 of scratch; side must hold the
+// largest format 3 size. unpack: nbytes of side are readable; a buffer the
+// encoder cannot produce sets CG_FLAG_CORRUPT (records stay in bounds).
+cudaError_t launch_v3_pack(const uint8_t *rec, const Dims &d, const MaxTab &mt, uint8_t *side,
+                           unsigned long long *totals, cudaStream_t s);
+cudaError_t launch_v3_unpack(const uint8_t *side, unsigned long long nbytes, const Dims &d, const MaxTab &mt,
+                             uint8_t *rec, int32_t *status, cudaStream_t s);
+// Byte offsets of the format 3 parts: M at offM, B at offB, V at offV.
+__host__ __device__ inline void v3_layout(const Dims &d, long long &offM, long long &offB, long long &offV) {
+    const long long ns = 2LL * d.L * d.nch, nrec = ns * d.C;
+    offM = 8 * (ns + 1);
+    offB = (offM + nrec + 3) / 4 * 4;
+    offV = offB + 4 * nrec;
+}
+
 // Fused quantise + CDF + encode straight from fp16 (chunks <= 256 tokens,
 // A <= 64, C % 8 == 0, 16-byte aligned rows); compress_fused_applies says when.
 bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v);

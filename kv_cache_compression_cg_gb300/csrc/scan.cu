@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kScanBlock) k_offsets_and_pack(
         off[n] = total;
         if (total > capacity && status) atomicOr(status, CG_FLAG_CAPACITY);
     }
+    if (stage == nullptr) return;  // offsets only
     __syncthreads();
     // copy: one warp per stream, 4 bytes per lane per step from the aligned stage
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -132,6 +133,11 @@ cudaError_t launch_scan_and_pack(const uint32_t *len, uint64_t *off, const uint8
     k_offsets_and_pack<<<(unsigned)ntiles, kScanBlock, 0, s>>>(len, n, partials, ntiles, off, stage,
                                                                d.stage_bytes, packed, capacity, status);
     return cudaGetLastError();
+}
+
+cudaError_t launch_offsets(const uint32_t *len, uint64_t *off, unsigned long long *partials, const Dims &d,
+                           cudaStream_t s) {
+    return launch_scan_and_pack(len, off, nullptr, nullptr, 0, partials, d, nullptr, s);
 }
 
 }  // namespace cg

@@ -89,13 +89,14 @@ class HostPiece:
     packed: torch.Tensor   # uint8 [capacity]; bytes [0, nbytes) are the streams
     len: torch.Tensor      # int32 [2 L (t1 - t0)] (uint32)
     off: torch.Tensor      # int64 [2 L (t1 - t0) + 1]
-    side: torch.Tensor     # format 1: int16 CDF entries; format 2: uint8 count records
+    side: torch.Tensor     # format 1: int16 CDF entries; 2: uint8 count records; 3: uint8 side buffer
     max1: torch.Tensor     # int16 [2, L, t1 - t0] (fp16 bits)
     ready: torch.cuda.Event
     fmt: int = 1
+    side_bytes: int = 0    # format 3: the side buffer's size (the rest of `side` is unused)
 
     def arrays(self) -> dict:
-        """numpy views in the layout `shard.assemble` joins."""
+        """numpy views in the layout `shard.assemble` joins (formats 1, 2)."""
         side = ("cdf", self.side.numpy().view(np.uint16)) if self.fmt == 1 else ("rec", self.side.numpy())
         return {"max1": self.max1.numpy().view(np.uint16), side[0]: side[1],
                 "packed": self.packed[:self.nbytes].numpy(), "len": self.len.numpy().view(np.uint32),
@@ -116,7 +117,7 @@ class StreamingCodec:
         if piece_chunks < 1:
             raise ValueError("piece_chunks must be >= 1")
         self.fmt = fmt
-        self.side_key = "cdf" if fmt == 1 else "rec"
+        self.side_key = {1: "cdf", 2: "rec", 3: "side3"}[fmt]
         self.L, self.T, self.C = L, T, C_
         self.bins_k = bins_k
         self.bins_v = bins_k if bins_v is None else bins_v
@@ -133,10 +134,12 @@ class StreamingCodec:
         for cd in self.enc:
             o = cd.out
             pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            side = o.cdf if fmt == 1 else o.rec
+            side = getattr(o, self.side_key)
             self.host.append({"packed": torch.empty(cd.capacity, dtype=torch.uint8, pin_memory=True),
                               "len": pin(o.len), "off": pin(o.off), self.side_key: pin(side), "max1": pin(o.max1)})
         self.n_host = torch.zeros(len(self.ranges), dtype=torch.int64, pin_memory=True)
+        # format 3: each piece's count bytes |V| (the uint64 after its slice offsets)
+        self.v3_host = torch.zeros(len(self.ranges), dtype=torch.int64, pin_memory=True)
         self.status_host = torch.zeros(2 * len(self.ranges), dtype=torch.int32, pin_memory=True)
         self.s_in = torch.cuda.Stream(device=dev)
         self.s_code = torch.cuda.Stream(device=dev)
@@ -169,6 +172,10 @@ class StreamingCodec:
         self.ev_enc[p].record(self.s_code)
         self.s_n.wait_event(self.ev_enc[p])
         _copy(self.n_host[p:p + 1], self.enc[p].out.off[-1:], 8, self.s_n)
+        if self.fmt == 3:
+            o = self.enc[p].out
+            ns = 2 * self.L * (-(-(o.T) // o.chunk_tokens))
+            _copy(self.v3_host[p:p + 1], o.side3[8 * ns:8 * ns + 8], 8, self.s_n)
         self.ev_n[p].record(self.s_n)
 
     def stream_pieces(self, k_host: torch.Tensor, v_host: torch.Tensor, ahead: int = 2):
@@ -194,12 +201,19 @@ class StreamingCodec:
             o, h = self.enc[p].out, self.host[p]
             self.s_out.wait_event(self.ev_enc[p])
             _copy(h["packed"], o.packed, n, self.s_out)
-            for key in ("len", "off", self.side_key, "max1"):
+            side_bytes = 0
+            if self.fmt == 3:  # the side buffer's used bytes; offsets stay behind (rebuilt from the lengths)
+                side_bytes = o.side3_fixed + int(self.v3_host[p])
+                keys = ("len", "max1")
+                _copy(h["side3"], o.side3, side_bytes, self.s_out)
+            else:
+                keys = ("len", "off", self.side_key, "max1")
+            for key in keys:
                 _copy(h[key], getattr(o, key), _nb(h[key]), self.s_out)
             _copy(self.status_host[2 * p:2 * p + 1], o.status, 4, self.s_out)
             self.ev_out[p].record(self.s_out)
             yield HostPiece(t0, t1, n, h["packed"], h["len"], h["off"], h[self.side_key], h["max1"], self.ev_out[p],
-                            self.fmt)
+                            self.fmt, side_bytes)
             if p + ahead < npc:
                 self._send(p + ahead, k_host, v_host)
 
@@ -216,9 +230,14 @@ class StreamingCodec:
         up = self.s_rx if upload is None else upload
         up.wait_event(hp.ready)
         _copy(rx.packed, hp.packed, hp.nbytes, up)
-        for key in ("len", "off", "max1"):
-            _copy(getattr(rx, key), getattr(hp, key), _nb(getattr(hp, key)), up)
-        _copy(getattr(rx, self.side_key), hp.side, _nb(hp.side), up)
+        if self.fmt == 3:
+            for key in ("len", "max1"):
+                _copy(getattr(rx, key), getattr(hp, key), _nb(getattr(hp, key)), up)
+            _copy(rx.side3, hp.side, hp.side_bytes, up)
+        else:
+            for key in ("len", "off", "max1"):
+                _copy(getattr(rx, key), getattr(hp, key), _nb(getattr(hp, key)), up)
+            _copy(getattr(rx, self.side_key), hp.side, _nb(hp.side), up)
         self.ev_rx[p].record(up)
         self.s_dec.wait_event(self.ev_rx[p])
         out = cd.decompress(rx, stream=self.s_dec)
@@ -256,7 +275,10 @@ class StreamingCodec:
     def bytes_moved(self, pieces: list[HostPiece]) -> tuple[int, int]:
         """(host-to-device, device-to-host) bytes of one compress + decompress."""
         fp16 = 2 * 2 * self.L * self.T * self.C
-        side = sum(hp.len.numel() * 4 + hp.off.numel() * 8 + _nb(hp.side) + hp.max1.numel() * 2
-                   for hp in pieces)
+        if self.fmt == 3:
+            side = sum(hp.len.numel() * 4 + hp.side_bytes + hp.max1.numel() * 2 for hp in pieces)
+        else:
+            side = sum(hp.len.numel() * 4 + hp.off.numel() * 8 + _nb(hp.side) + hp.max1.numel() * 2
+                       for hp in pieces)
         comp = sum(hp.nbytes for hp in pieces)
         return fp16 + comp + side, 8 * len(pieces) + comp + side + 8 * len(pieces)
