@@ -178,3 +178,34 @@ def test_record_bytes_match_oracle(oracle_mod):
 def ctypes_ref(x):
     import ctypes
     return ctypes.byref(x)
+
+
+def test_format3_sizes_and_rejections(oracle_mod):
+    """Format 3's sizes equal the oracle's; arguments the library cannot
+    serve are refused before touching the device."""
+    from kv_cache_compression_cg_gb300 import capi, codec
+    import ctypes
+    import numpy as np
+    lib = capi.load()
+    for L, T, C_, Tc, bk, bv in [(2, 64, 64, 64, [32, 16], [16, 32]), (3, 200, 40, 64, [32, 16, 7], [8, 8, 33]),
+                                (1, 300, 8, 256, [4], [5])]:
+        shp = codec.make_shape(L, T, C_, Tc)
+        bka, bva = np.array(bk, np.int32), np.array(bv, np.int32)
+        assert lib.cg_side3_fixed_bytes(ctypes.byref(shp)) == oracle_mod.v3_fixed_bytes(L, T, C_, Tc)
+        assert lib.cg_side3_max_bytes(ctypes.byref(shp), bka.ctypes.data, bva.ctypes.data) == \
+            oracle_mod.v3_max_bytes(L, T, C_, Tc, bk, bv)
+    wide = np.array([64], np.int32)  # A = 63: past a 32-bit presence mask
+    shp = codec.make_shape(1, 64, 8, 64)
+    assert lib.cg_side3_max_bytes(ctypes.byref(shp), wide.ctypes.data, wide.ctypes.data) == 0
+    long_chunks = codec.make_shape(1, 600, 8, 300)
+    b = np.array([16], np.int32)
+    assert lib.cg_side3_max_bytes(ctypes.byref(long_chunks), b.ctypes.data, b.ctypes.data) == 0
+    fake, ws = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x10000)
+    need = lib.cg_side3_max_bytes(ctypes.byref(shp), b.ctypes.data, b.ctypes.data)
+    assert lib.cg_compress_chunk_v3(fake, fake, ctypes.byref(shp), b.ctypes.data, None, 1, fake, fake, need - 1, fake,
+                                    100, fake, fake, ws, 1 << 40, None, None) == 1  # side buffer too small
+    assert lib.cg_compress_chunk_v3(fake, fake, ctypes.byref(shp), b.ctypes.data, None, 1, fake, fake, need, fake,
+                                    100, fake, fake, ws, 16, None, None) == 2  # workspace too small
+    fixed = lib.cg_side3_fixed_bytes(ctypes.byref(shp))
+    assert lib.cg_decompress_chunk_v3(fake, 100, fake, fake, fixed - 1, fake, ctypes.byref(shp), b.ctypes.data, None,
+                                      1, 0, fake, fake, 64 * 8, ws, 1 << 40, None, None) == 1  # shorter than its fixed part
