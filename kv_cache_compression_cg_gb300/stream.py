@@ -30,7 +30,7 @@ import torch
 
 from . import codec as _codec
 
-__all__ = ["StreamingCodec", "HostPiece"]
+__all__ = ["StreamingCodec", "HostPiece", "AdaptiveLevels"]
 
 _MEMCPY_H2D = 1
 _rt = None
@@ -94,6 +94,7 @@ class HostPiece:
     ready: torch.cuda.Event
     fmt: int = 1
     side_bytes: int = 0    # format 3: the side buffer's size (the rest of `side` is unused)
+    level: int = 0         # index of the bins this piece was quantised with
 
     def arrays(self) -> dict:
         """numpy views in the layout `shard.assemble` joins (formats 1, 2)."""
@@ -103,17 +104,63 @@ class HostPiece:
                 "off": self.off.numpy().view(np.uint64)}
 
 
+class AdaptiveLevels:
+    """Bandwidth-adaptive choice of the quantisation level per piece: chunks
+    are small so the coder can follow a changing link [CG §2.3(3)]. Levels are
+    ordered finest first (most bins); a piece gets the finest level whose
+    compressed size, estimated from the pieces already sent at that level
+    (bytes per token, averaged with weight `smoothing` on the newest), fits
+    the link's rate times the time budget of a piece. A level not yet seen is
+    taken as fitting (so it gets measured); with nothing fitting, the
+    coarsest. Host logic only: the rate is the caller's measurement of its
+    link."""
+
+    def __init__(self, nlevels: int, seconds_per_piece: float, bytes_per_second: float,
+                 smoothing: float = 0.5, prior_bytes_per_token=None):
+        if nlevels < 1 or seconds_per_piece <= 0 or bytes_per_second <= 0 or not 0 < smoothing <= 1:
+            raise ValueError("need nlevels >= 1, positive budget and rate, smoothing in (0, 1]")
+        self.n = nlevels
+        self.seconds = seconds_per_piece
+        self.rate = bytes_per_second
+        self.smoothing = smoothing
+        self.est = list(prior_bytes_per_token) if prior_bytes_per_token is not None else [None] * nlevels
+        if len(self.est) != nlevels:
+            raise ValueError("one prior per level")
+
+    def set_rate(self, bytes_per_second: float):
+        if bytes_per_second <= 0:
+            raise ValueError("the rate must be positive")
+        self.rate = bytes_per_second
+
+    def level_for(self, tokens: int) -> int:
+        budget = self.rate * self.seconds
+        for lv in range(self.n):
+            e = self.est[lv]
+            if e is None or e * tokens <= budget:
+                return lv
+        return self.n - 1
+
+    def observe(self, level: int, tokens: int, nbytes: int):
+        per = nbytes / max(tokens, 1)
+        e = self.est[level]
+        self.est[level] = per if e is None else (1 - self.smoothing) * e + self.smoothing * per
+
+
 class StreamingCodec:
     """Pipelined compress from pinned host K, V and decompress of host pieces.
 
     All buffers (device staging of the fp16 input, one sender and one receiver
-    codec per piece, pinned host pieces) are allocated once here.
+    codec per piece and quantisation level, pinned host pieces) are allocated
+    once here.
     """
 
     def __init__(self, L: int, T: int, C_: int, bins_k, bins_v=None, chunk_tokens: int = 256,
-                 piece_chunks: int = 2, device: str | torch.device = "cuda", fmt: int = 1, group: int = 1):
+                 piece_chunks: int = 2, device: str | torch.device = "cuda", fmt: int = 1, group: int = 1,
+                 levels=None):
         """fmt, group: the codec's format and token-locality delta group (as
-        Codec); pieces are whole chunks, so they code independently."""
+        Codec); pieces are whole chunks, so they code independently. levels:
+        optional list of (bins_k, bins_v), finest first, that pieces may
+        switch between (`stream_pieces(policy=...)`); default the one pair."""
         if piece_chunks < 1:
             raise ValueError("piece_chunks must be >= 1")
         self.fmt = fmt
@@ -121,22 +168,29 @@ class StreamingCodec:
         self.L, self.T, self.C = L, T, C_
         self.bins_k = bins_k
         self.bins_v = bins_k if bins_v is None else bins_v
+        self.levels = [(self.bins_k, self.bins_v)] if levels is None else \
+            [(bk, bk if bv is None else bv) for bk, bv in levels]
         step = piece_chunks * chunk_tokens
         self.ranges = [(t0, min(T, t0 + step)) for t0 in range(0, T, step)]
         dev = torch.device(device)
         self.k = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
         self.v = torch.empty((L, T, C_), dtype=torch.float16, device=dev)
-        mk = lambda t0, t1: _codec.Codec(L, t1 - t0, C_, self.bins_k, self.bins_v, chunk_tokens=chunk_tokens,
-                                         device=dev, fmt=fmt, group=group)
-        self.enc = [mk(t0, t1) for t0, t1 in self.ranges]
-        self.dec = [mk(t0, t1) for t0, t1 in self.ranges]
+        mk = lambda t0, t1, bk, bv: _codec.Codec(L, t1 - t0, C_, bk, bv, chunk_tokens=chunk_tokens, device=dev,
+                                                 fmt=fmt, group=group)
+        # [level][piece]
+        self.enc = [[mk(t0, t1, bk, bv) for t0, t1 in self.ranges] for bk, bv in self.levels]
+        self.dec = [[mk(t0, t1, bk, bv) for t0, t1 in self.ranges] for bk, bv in self.levels]
         self.host = []
-        for cd in self.enc:
-            o = cd.out
-            pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            side = getattr(o, self.side_key)
-            self.host.append({"packed": torch.empty(cd.capacity, dtype=torch.uint8, pin_memory=True),
-                              "len": pin(o.len), "off": pin(o.off), self.side_key: pin(side), "max1": pin(o.max1)})
+        for lv_codecs in self.enc:
+            hl = []
+            for cd in lv_codecs:
+                o = cd.out
+                pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                side = getattr(o, self.side_key)
+                hl.append({"packed": torch.empty(cd.capacity, dtype=torch.uint8, pin_memory=True),
+                           "len": pin(o.len), "off": pin(o.off), self.side_key: pin(side), "max1": pin(o.max1)})
+            self.host.append(hl)
+        self.level = [0] * len(self.ranges)  # each piece's level in the current pass
         self.n_host = torch.zeros(len(self.ranges), dtype=torch.int64, pin_memory=True)
         # format 3: each piece's count bytes |V| (the uint64 after its slice offsets)
         self.v3_host = torch.zeros(len(self.ranges), dtype=torch.int64, pin_memory=True)
@@ -162,30 +216,38 @@ class StreamingCodec:
         if err != 0:
             raise RuntimeError(f"cudaMemcpy2DAsync failed ({err})")
 
-    def _send(self, p: int, k_host: torch.Tensor, v_host: torch.Tensor):
+    def _send(self, p: int, k_host: torch.Tensor, v_host: torch.Tensor, level: int = 0):
         t0, t1 = self.ranges[p]
+        self.level[p] = level
+        enc = self.enc[level][p]
         self._copy_in(self.k, k_host, t0, t1)
         self._copy_in(self.v, v_host, t0, t1)
         self.ev_in[p].record(self.s_in)
         self.s_code.wait_event(self.ev_in[p])
-        self.enc[p].compress(self.k[:, t0:t1], self.v[:, t0:t1], stream=self.s_code)
+        enc.compress(self.k[:, t0:t1], self.v[:, t0:t1], stream=self.s_code)
         self.ev_enc[p].record(self.s_code)
         self.s_n.wait_event(self.ev_enc[p])
-        _copy(self.n_host[p:p + 1], self.enc[p].out.off[-1:], 8, self.s_n)
+        _copy(self.n_host[p:p + 1], enc.out.off[-1:], 8, self.s_n)
         if self.fmt == 3:
-            o = self.enc[p].out
+            o = enc.out
             ns = 2 * self.L * (-(-(o.T) // o.chunk_tokens))
             _copy(self.v3_host[p:p + 1], o.side3[8 * ns:8 * ns + 8], 8, self.s_n)
         self.ev_n[p].record(self.s_n)
 
-    def stream_pieces(self, k_host: torch.Tensor, v_host: torch.Tensor, ahead: int = 2):
+    def stream_pieces(self, k_host: torch.Tensor, v_host: torch.Tensor, ahead: int = 2, policy=None):
         """fp16 [L, T, C] pinned host K, V -> compressed pieces in pinned host
         memory, yielded in order as soon as each piece's copy-out is enqueued
         (its `ready` event marks the bytes on the host). Input copies run
         `ahead` pieces in front of the piece being yielded, so copies a
         consumer enqueues for piece p (the receiver's) take their place in the
         host-to-device queue behind piece p + ahead's input rather than behind
-        every input."""
+        every input. policy: None (level 0), or an object with
+        level_for(tokens) -> level and observe(level, tokens, nbytes) (e.g.
+        AdaptiveLevels), asked when a piece is sent and told its size."""
+        if policy is None:
+            choose = lambda p: 0
+        else:
+            choose = lambda p: int(policy.level_for(self.ranges[p][1] - self.ranges[p][0]))
         for t in (k_host, v_host):
             if t.device.type != "cpu" or not t.is_pinned() or t.dtype != torch.float16 or not t.is_contiguous():
                 raise ValueError("K and V must be contiguous pinned host fp16 tensors")
@@ -194,11 +256,12 @@ class StreamingCodec:
         npc = len(self.ranges)
         ahead = max(1, ahead)
         for p in range(min(ahead, npc)):
-            self._send(p, k_host, v_host)
+            self._send(p, k_host, v_host, self._checked(choose(p)))
         for p, (t0, t1) in enumerate(self.ranges):
             self.ev_n[p].synchronize()  # the piece's byte count, needed to size its copy
             n = int(self.n_host[p])
-            o, h = self.enc[p].out, self.host[p]
+            lv = self.level[p]
+            o, h = self.enc[lv][p].out, self.host[lv][p]
             self.s_out.wait_event(self.ev_enc[p])
             _copy(h["packed"], o.packed, n, self.s_out)
             side_bytes = 0
@@ -212,21 +275,29 @@ class StreamingCodec:
                 _copy(h[key], getattr(o, key), _nb(h[key]), self.s_out)
             _copy(self.status_host[2 * p:2 * p + 1], o.status, 4, self.s_out)
             self.ev_out[p].record(self.s_out)
+            if policy is not None:
+                policy.observe(lv, t1 - t0, n + (side_bytes if self.fmt == 3 else _nb(h[self.side_key])))
             yield HostPiece(t0, t1, n, h["packed"], h["len"], h["off"], h[self.side_key], h["max1"], self.ev_out[p],
-                            self.fmt, side_bytes)
+                            self.fmt, side_bytes, lv)
             if p + ahead < npc:
-                self._send(p + ahead, k_host, v_host)
+                self._send(p + ahead, k_host, v_host, self._checked(choose(p + ahead)))
 
-    def compress_from_host(self, k_host: torch.Tensor, v_host: torch.Tensor) -> list[HostPiece]:
+    def _checked(self, level: int) -> int:
+        if not 0 <= level < len(self.levels):
+            raise ValueError(f"level {level} outside the {len(self.levels)} configured")
+        return level
+
+    def compress_from_host(self, k_host: torch.Tensor, v_host: torch.Tensor, policy=None) -> list[HostPiece]:
         """All pieces of `stream_pieces` (returns once every copy-out is enqueued)."""
-        return list(self.stream_pieces(k_host, v_host))
+        return list(self.stream_pieces(k_host, v_host, policy=policy))
 
     # -- receiver -------------------------------------------------------------
     def receive(self, p: int, hp: HostPiece, upload: torch.cuda.Stream | None = None):
         """Piece p (host) -> fp32 [L, t1 - t0, C] K, V on the device: copy in on
         `upload` (default: the receiver's own stream) once the piece is on the
         host, decompress on the decoding stream, status word back to the host."""
-        rx, cd = self.dec[p].out, self.dec[p]
+        cd = self.dec[hp.level][p]
+        rx = cd.out
         up = self.s_rx if upload is None else upload
         up.wait_event(hp.ready)
         _copy(rx.packed, hp.packed, hp.nbytes, up)
@@ -253,7 +324,7 @@ class StreamingCodec:
         self.ev_done.record(self.s_dec)
         return outs, self.ev_done
 
-    def roundtrip(self, k_host: torch.Tensor, v_host: torch.Tensor):
+    def roundtrip(self, k_host: torch.Tensor, v_host: torch.Tensor, policy=None):
         """Compress from host, ship each piece to the host and back, decompress:
         returns (pieces, outs, done event), receiver work enqueued piece by piece
         as the sender produces them. The uploads share the input-copy stream, so
@@ -261,7 +332,7 @@ class StreamingCodec:
         pieces = []
 
         def gen():
-            for hp in self.stream_pieces(k_host, v_host):
+            for hp in self.stream_pieces(k_host, v_host, policy=policy):
                 pieces.append(hp)
                 yield hp
         outs, done = self.decompress_from_host(gen(), upload=self.s_in)

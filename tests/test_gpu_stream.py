@@ -84,3 +84,54 @@ def test_stream_with_delta_matches_oracle(synth_mod, oracle_mod, fmt):
     for (ok, ov), hp in zip(outs, pieces):
         assert np.array_equal(ok.cpu().numpy().view(np.uint32), wk[:, hp.t0:hp.t1].view(np.uint32))
         assert np.array_equal(ov.cpu().numpy().view(np.uint32), wv[:, hp.t0:hp.t1].view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [2, 3])
+def test_stream_switches_levels_per_piece(synth_mod, oracle_mod, fmt):
+    """Pieces quantised with different bins (a policy alternating two
+    levels): each piece equals the oracle's compression of its tokens with its
+    level's bins, and decodes to the oracle's values."""
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required")
+    from kv_cache_compression_cg_gb300 import build
+    from kv_cache_compression_cg_gb300.stream import StreamingCodec
+    build.build()
+    w = synth_mod.WORKLOADS["mistral_chunk"]
+    T, Tc = 256, 64
+    k, v = synth_mod.generate(w, T=T)
+    levels = [(list(w.bins_k), list(w.bins_v)), ([8] * w.L, [8] * w.L)]
+
+    class Alternate:
+        def __init__(self):
+            self.calls, self.seen = 0, []
+
+        def level_for(self, tokens):
+            self.calls += 1
+            return (self.calls - 1) % 2
+
+        def observe(self, level, tokens, nbytes):
+            self.seen.append((level, tokens, nbytes))
+
+    pol = Alternate()
+    sc = StreamingCodec(w.L, T, w.C, w.bins_k, w.bins_v, chunk_tokens=Tc, piece_chunks=1, fmt=fmt, levels=levels)
+    pieces, outs, done = sc.roundtrip(torch.from_numpy(k).pin_memory(), torch.from_numpy(v).pin_memory(),
+                                      policy=pol)
+    done.synchronize()
+    assert sc.status() == 0
+    assert [hp.level for hp in pieces] == [0, 1, 0, 1]
+    assert [lv for lv, _, _ in pol.seen] == [0, 1, 0, 1]
+    for (ok, ov), hp in zip(outs, pieces):
+        bk, bv = levels[hp.level]
+        ks, vs = k[:, hp.t0:hp.t1].copy(), v[:, hp.t0:hp.t1].copy()
+        if fmt == 2:
+            ref = oracle_mod.compress_v2(ks, vs, Tc, bk, bv)
+            rk, rv = oracle_mod.decompress_v2(ref["packed"], ref["off"], ref["len"], ref["rec"], ref["max1"], w.L,
+                                              hp.t1 - hp.t0, w.C, Tc, bk, bv)
+        else:
+            ref = oracle_mod.compress_v3(ks, vs, Tc, bk, bv)
+            rk, rv = oracle_mod.decompress_v3(ref["packed"], ref["len"], ref["side"], ref["max1"], w.L,
+                                              hp.t1 - hp.t0, w.C, Tc, bk, bv)
+        assert hp.nbytes == ref["packed"].size
+        assert np.array_equal(hp.packed[:hp.nbytes].numpy(), ref["packed"])
+        assert np.array_equal(ok.cpu().numpy().view(np.uint32), rk.view(np.uint32))
+        assert np.array_equal(ov.cpu().numpy().view(np.uint32), rv.view(np.uint32))
