@@ -2,6 +2,7 @@
 import math
 
 import numpy as np
+import pytest
 
 
 def test_elementary_functions(synth_mod):
@@ -62,3 +63,20 @@ def test_statistics(synth_mod):
     t = synth_mod.generate_slice(synth_mod.WORKLOADS["stress80k"], 0, 0, T=512).astype(np.float64)
     z = t / np.median(np.abs(t), axis=0)
     assert abs(np.corrcoef(z[:-1].ravel(), z[1:].ravel())[0, 1]) < 0.02
+
+
+def _recorded_sha256():
+    from conftest import read_golden
+    return {name: digest for name, digest in read_golden("synth_sha256.txt")}
+
+
+@pytest.mark.parametrize("name", ["tiny", "mistral_chunk", "uniform", "ctx4096"])
+def test_generator_bytes_match_recorded_sha256(synth_mod, name):
+    """The generator's output is pinned: the same bytes as recorded (written by
+    tests/golden/make_synth_sha256.py), on this machine and any other."""
+    import hashlib
+    k, v = synth_mod.generate(synth_mod.WORKLOADS[name])
+    h = hashlib.sha256()
+    h.update(k.tobytes())
+    h.update(v.tobytes())
+    assert h.hexdigest() == _recorded_sha256()[name]
