@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--piece-chunks", type=int, default=2,
                     help="chunks per piece of the streamed end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chunk-parallel", action="store_true",
+                    help="skip the oracle's chunk-parallel timing on all host cores")
     ap.add_argument("--group", type=int, default=1,
                     help="token-locality delta group size (1: none, the page's LMCache code path)")
     return ap.parse_args()
@@ -193,6 +195,57 @@ def oracle_step_time(k, v, w, tokens, fmt=2, group=1):
     return dt, ks.nbytes + vs.nbytes
 
 
+def _chunk_worker(name, chunk, fmt, group, reps, barrier, results):
+    """One process of the chunk-parallel timing: regenerates its own chunk of
+    the workload, then times the oracle on it once per repetition, all
+    processes released together by the barrier."""
+    import numpy as np
+    from kv_cache_compression_cg_gb300 import synth
+    w = synth.WORKLOADS[name]
+    t0 = chunk * w.chunk_tokens
+    t1 = min(w.T, t0 + w.chunk_tokens)
+    k = np.stack([synth.generate_slice_range(w, 0, l, t0, t1) for l in range(w.L)])
+    v = np.stack([synth.generate_slice_range(w, 1, l, t0, t1) for l in range(w.L)])
+    for _ in range(reps):
+        barrier.wait()
+        dt, nbytes = oracle_step_time(k, v, w, t1 - t0, fmt, group)
+        results.put((chunk, dt, nbytes))
+
+
+def oracle_chunk_parallel(w, fmt=2, group=1, reps=3, workers=None):
+    """The oracle, unchanged, run by one process per host core over
+    independent chunks (worker i codes chunk i mod the chunk count), each
+    compress + decompress timed between a common start and the last finish.
+    Processes are spawned (no fork of a process that has a CUDA context)."""
+    import multiprocessing as mp
+    if workers is None:
+        workers = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(workers + 1)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_chunk_worker, args=(w.name, i % w.n_chunks, fmt, group, reps, barrier, results))
+             for i in range(workers)]
+    for p in procs:
+        p.start()
+    walls, nbytes = [], 0
+    try:
+        for _ in range(reps):
+            barrier.wait(timeout=600)
+            t0 = time.perf_counter()
+            got = [results.get(timeout=600) for _ in range(workers)]
+            walls.append(time.perf_counter() - t0)
+            nbytes = sum(g[2] for g in got)
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    wall = statistics.median(walls)
+    return {"value": nbytes / wall / 1e9, "unit": UNIT, "cores": workers, "kind": "oracle, chunk-parallel",
+            "sample": f"{workers} processes, one {w.chunk_tokens}-token chunk each (compress + decompress), "
+                      f"median of {reps} repetitions"}
+
+
 def run_reference(args):
     """--impl reference: the CPU oracle (the only reference implementation of
     this method here) timed on the host cores, on bounded samples."""
@@ -213,12 +266,15 @@ def run_reference(args):
     ms = 1e3 * sum(times) / len(times)
     value = nbytes / (ms * 1e-3) / 1e9
     sample = f"first chunk ({tokens} tokens x {w.L} layers x {w.C} channels, K and V) per step"
+    cpu = {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    if not args.no_chunk_parallel:
+        cpu["chunk_parallel"] = oracle_chunk_parallel(w, args.format, args.group)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(w, {"sample": sample, "format": args.format, "delta_group": args.group}),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": cpu,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -390,6 +446,8 @@ def run_ours(args):
             "value": cpu_gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {min(w.T, 2 * w.chunk_tokens)} tokens (compress + decompress), "
                       f"{len(times)} repetitions"}
+        if not args.no_chunk_parallel:
+            result["cpu_baseline"]["chunk_parallel"] = oracle_chunk_parallel(w, args.format, args.group)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
