@@ -3,18 +3,27 @@ low-locality stress case) on the GPU, in the launch configuration the
 benchmark times (one compress and one decompress call over the whole tensor),
 in both formats.
 
-The oracle cannot code 6-10 GB in a test, so:
-- sampled (chunk, kv, layer) slices are coded by the oracle from inputs the
-  host generator regenerates on its own, and every output of those slices
-  (max1, CDF rows, stream lengths, packed bytes, dequantised values) must match
-  the GPU's bit for bit;
+The oracle cannot code 6-10 GB in a test at once, so:
+- whole chunks (the first, the last and 14 drawn at random) are coded by the
+  oracle, one spawned process per chunk, from inputs the host generator
+  regenerates on its own, and every output of those chunks (max1, the side
+  information block, stream lengths, packed bytes, dequantised values) must
+  match the GPU's bit for bit, in all three side-information formats;
+- sampled (chunk, kv, layer) slices are also coded alone by the oracle and
+  compared the same way (formats 1 and 2);
 - properties that hold at any size are checked over every element on the GPU:
   status words clear, offsets the exclusive scan of the lengths, lengths within
   2C + 8, and the quantisation error bound |x - x^| <= max1/(2 MAX) + ulp(max1).
 """
+import hashlib
+import multiprocessing as mp
+import os
+
 import numpy as np
 import pytest
 import torch
+
+import oracle_chunks
 
 pytestmark = pytest.mark.gpu
 
@@ -107,18 +116,70 @@ def _check_properties(w, k, v, codec, out, ok, ov):
             assert bool((err <= bound).all()), f"error bound broken at kv={kv} layer={l}"
 
 
-@pytest.mark.parametrize("fmt", [1, 2])
+def _chunk_picks(w, seed, n=14):
+    """The first and last chunks and n distinct others drawn at random."""
+    nch = w.n_chunks
+    inner = np.arange(1, nch - 1)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(inner, size=min(n, inner.size), replace=False) if inner.size else []
+    return sorted({0, nch - 1, *(int(c) for c in mid)})
+
+
+def _check_chunk(oracle_mod, w, out, ok, ov, rec_all, ref, fmt):
+    L, T, C_, Tc = w.L, w.T, w.C, w.chunk_tokens
+    kc = ref["kc"]
+    t0, t1 = kc * Tc, min(T, (kc + 1) * Tc)
+    Tk = t1 - t0
+    assert np.array_equal(out.max1[:, :, t0:t1].cpu().numpy().view(np.uint16), ref["max1"]), kc
+    side = ref["side"]
+    if fmt == 1:
+        g0 = oracle_mod.cdf_offset(L, C_, max(w.bins_k), max(w.bins_v), kc, 0, 0, 0)
+        got = out.cdf[g0:g0 + side.size].cpu().numpy().view(np.uint16)
+    else:
+        g0 = oracle_mod.rec_offset(L, C_, w.bins_k, w.bins_v, kc, 0, 0, 0)
+        got = out.rec[g0:g0 + side.size].cpu().numpy() if fmt == 2 else rec_all[g0:g0 + side.size]
+    assert np.array_equal(got, side), kc
+    s0 = oracle_mod.stream_id(L, T, Tc, kc, 0, 0, 0)
+    ns = 2 * L * Tk
+    assert np.array_equal(out.len[s0:s0 + ns].cpu().numpy().view(np.uint32), ref["len"]), kc
+    b0, b1 = int(out.off[s0].item()), int(out.off[s0 + ns].item())
+    assert b1 - b0 == ref["packed"].size, kc
+    assert np.array_equal(out.packed[b0:b1].cpu().numpy(), ref["packed"]), kc
+    h = hashlib.sha256()
+    h.update(ok[:, t0:t1].contiguous().cpu().numpy().tobytes())
+    h.update(ov[:, t0:t1].contiguous().cpu().numpy().tobytes())
+    assert h.hexdigest() == ref["out_sha256"], kc
+
+
+@pytest.mark.parametrize("fmt", [1, 2, 3])
 @pytest.mark.parametrize("name", ["ctx32k", "stress80k"])
 def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name, fmt):
     w = synth_mod.WORKLOADS[name]
-    k, v = synth_mod.generate_device(w)
-    codec = cg.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens,
-                     capacity=w.elements // 2, fmt=fmt)
-    out = codec.compress(k, v)
-    ok, ov = codec.decompress()
-    torch.cuda.synchronize()
-    assert int(out.status.item()) == 0
-    assert int(codec.dstatus.item()) == 0
-    _check_properties(w, k, v, codec, out, ok, ov)
-    for kc, kv, l in _samples(w, seed=len(name)):
-        _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt)
+    picks = _chunk_picks(w, seed=len(name) + fmt)
+    # the oracle's chunks run on the host cores while the GPU codes the tensor
+    pool = mp.get_context("spawn").Pool(processes=min(len(picks), os.cpu_count() or 1))
+    try:
+        pending = pool.starmap_async(oracle_chunks.code_chunk, [(name, kc, fmt) for kc in picks])
+        k, v = synth_mod.generate_device(w)
+        codec = cg.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens,
+                         capacity=w.elements // 2, fmt=fmt)
+        out = codec.compress(k, v)
+        ok, ov = codec.decompress()
+        torch.cuda.synchronize()
+        assert int(out.status.item()) == 0
+        assert int(codec.dstatus.item()) == 0
+        _check_properties(w, k, v, codec, out, ok, ov)
+        rec_all = None
+        if fmt == 3:  # the whole side buffer must parse; its records are compared per chunk
+            side = out.side3[:out.side3_bytes()].cpu().numpy()
+            rec_all = oracle_mod.v3_to_records(side, w.L, w.T, w.C, w.chunk_tokens, w.bins_k, w.bins_v)
+        else:
+            for kc, kv, l in _samples(w, seed=len(name)):
+                _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt)
+        refs = pending.get(timeout=1800)
+    finally:
+        pool.close()
+        pool.join()
+    assert [r["kc"] for r in refs] == picks
+    for ref in refs:
+        _check_chunk(oracle_mod, w, out, ok, ov, rec_all, ref, fmt)
