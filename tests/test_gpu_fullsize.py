@@ -1,7 +1,7 @@
 """Full-size workloads (the 34B-shaped 32K-token context and the 80K-token
 low-locality stress case) on the GPU, in the launch configuration the
 benchmark times (one compress and one decompress call over the whole tensor),
-in both formats.
+in all three side-information formats.
 
 The oracle cannot code 6-10 GB in a test at once, so:
 - whole chunks (the first, the last and 14 drawn at random) are coded by the
