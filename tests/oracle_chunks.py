@@ -15,9 +15,11 @@ import hashlib
 import numpy as np
 
 
-def code_chunk(name: str, kc: int, fmt: int, T: int | None = None) -> dict:
+def code_chunk(name: str, kc: int, fmt: int, T: int | None = None, k=None, v=None) -> dict:
     """Chunk kc of workload `name` (its first T tokens if T is given) in
-    side-information format fmt."""
+    side-information format fmt. k, v: the chunk's host-generated values
+    [L][Tk][C] when the caller has them (an AR(1) workload's late chunks cost
+    their whole token prefix to generate alone)."""
     import oracle
     from kv_cache_compression_cg_gb300 import synth
     w = synth.WORKLOADS[name]
@@ -25,8 +27,10 @@ def code_chunk(name: str, kc: int, fmt: int, T: int | None = None) -> dict:
     T = w.T if T is None else T
     t0, t1 = kc * Tc, min(T, (kc + 1) * Tc)
     Tk = t1 - t0
-    k = np.stack([synth.generate_slice_range(w, 0, l, t0, t1) for l in range(w.L)])
-    v = np.stack([synth.generate_slice_range(w, 1, l, t0, t1) for l in range(w.L)])
+    if k is None:
+        k = np.stack([synth.generate_slice_range(w, 0, l, t0, t1) for l in range(w.L)])
+        v = np.stack([synth.generate_slice_range(w, 1, l, t0, t1) for l in range(w.L)])
+    assert k.shape == v.shape == (w.L, Tk, w.C)
     bk, bv = w.bins_k, w.bins_v
     if fmt == 1:
         r = oracle.compress(k, v, Tc, bk, bv)

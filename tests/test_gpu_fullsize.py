@@ -6,7 +6,8 @@ in all three side-information formats.
 The oracle cannot code 6-10 GB in a test at once, so:
 - whole chunks (the first, the last and 14 drawn at random) are coded by the
   oracle, one spawned process per chunk, from inputs the host generator
-  regenerates on its own, and every output of those chunks (max1, the side
+  produces on its own (the whole tensor for AR(1) workloads, whose chunks
+  cost their token prefix to generate alone; each chunk alone otherwise), and every output of those chunks (max1, the side
   information block, stream lengths, packed bytes, dequantised values) must
   match the GPU's bit for bit, in all three side-information formats;
 - sampled (chunk, kv, layer) slices are also coded alone by the oracle and
@@ -46,14 +47,14 @@ def _samples(w, seed):
     return picks
 
 
-def _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt):
+def _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt, host=None):
     L, T, C_, Tc = w.L, w.T, w.C, w.chunk_tokens
     bins = (w.bins_k, w.bins_v)[kv]
     A_k, A_v = max(w.bins_k), max(w.bins_v)
     A = (A_k, A_v)[kv]
     t0, t1 = kc * Tc, min(T, (kc + 1) * Tc)
     Tk = t1 - t0
-    x = synth_mod.generate_slice_range(w, kv, l, t0, t1)
+    x = host[kv][l, t0:t1] if host is not None else synth_mod.generate_slice_range(w, kv, l, t0, t1)
     dev_x = (k, v)[kv][l, t0:t1].cpu().numpy()
     assert np.array_equal(dev_x.view(np.uint16), x.view(np.uint16)), "device generator differs from host"
     # the oracle on [2 layers][Tk][C]: layer 0 is the slice, layer 1 a zero
@@ -151,15 +152,38 @@ def _check_chunk(oracle_mod, w, out, ok, ov, rec_all, ref, fmt):
     assert h.hexdigest() == ref["out_sha256"], kc
 
 
+_HOST = {}
+
+
+def _host_tensor(synth_mod, w):
+    """The host generator's whole K, V for w, kept for the next format's test
+    of the same workload (one workload at a time)."""
+    if w.name not in _HOST:
+        _HOST.clear()
+        _HOST[w.name] = synth_mod.generate(w)
+    return _HOST[w.name]
+
+
 @pytest.mark.parametrize("fmt", [1, 2, 3])
 @pytest.mark.parametrize("name", ["ctx32k", "stress80k"])
 def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name, fmt):
     w = synth_mod.WORKLOADS[name]
     picks = _chunk_picks(w, seed=len(name) + fmt)
+    # An AR(1) chunk generated alone costs its whole token prefix: generate the
+    # tensor once on the host (all cores) and hand each worker its chunk. An
+    # iid workload's chunks are cheap alone.
+    host = _host_tensor(synth_mod, w) if w.kind == synth_mod.AR1 else None
+
+    def job(kc):
+        if host is None:
+            return (name, kc, fmt)
+        t0, t1 = kc * w.chunk_tokens, min(w.T, (kc + 1) * w.chunk_tokens)
+        return (name, kc, fmt, None, host[0][:, t0:t1].copy(), host[1][:, t0:t1].copy())
+
     # the oracle's chunks run on the host cores while the GPU codes the tensor
     pool = mp.get_context("spawn").Pool(processes=min(len(picks), os.cpu_count() or 1))
     try:
-        pending = pool.starmap_async(oracle_chunks.code_chunk, [(name, kc, fmt) for kc in picks])
+        pending = pool.starmap_async(oracle_chunks.code_chunk, [job(kc) for kc in picks])
         k, v = synth_mod.generate_device(w)
         codec = cg.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens,
                          capacity=w.elements // 2, fmt=fmt)
@@ -175,7 +199,7 @@ def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name,
             rec_all = oracle_mod.v3_to_records(side, w.L, w.T, w.C, w.chunk_tokens, w.bins_k, w.bins_v)
         else:
             for kc, kv, l in _samples(w, seed=len(name)):
-                _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt)
+                _check_slice(cg, oracle_mod, synth_mod, w, k, v, codec, out, ok, ov, kc, kv, l, fmt, host)
         refs = pending.get(timeout=1800)
     finally:
         pool.close()
