@@ -172,7 +172,7 @@ def test_fullsize_sampled_parity_and_properties(cg, oracle_mod, synth_mod, name,
     # An AR(1) chunk generated alone costs its whole token prefix: generate the
     # tensor once on the host (all cores) and hand each worker its chunk. An
     # iid workload's chunks are cheap alone.
-    host = _host_tensor(synth_mod, w) if w.kind == synth_mod.AR1 else None
+    host = _host_tensor(synth_mod, w) if w.kind == synth_mod.AR1 else _HOST.clear()
 
     def job(kc):
         if host is None:
