@@ -38,8 +38,6 @@ def _case(synth_mod, name):
 @pytest.mark.parametrize("case", ["tiny", "ragged", "odd_bins", "t1", "mistral_chunk",
                                   pytest.param("ctx4096", marks=pytest.mark.slow)])
 def test_v3_parity_with_oracle(cg, oracle_mod, synth_mod, case, G):
-    if case == "ctx4096" and G > 1:
-        pytest.skip("one full-size case is enough")
     k, v, Tc, bk, bv = _case(synth_mod, case)
     L, T, C_ = k.shape
     ref = oracle_mod.compress_v3(k, v, Tc, bk, bv, group=G)
