@@ -512,6 +512,26 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
     }
 }
 
+// The order in which the decoder's CTAs take the (kv, layer) pairs: by
+// decreasing MAX (a wider alphabet costs a longer search and more coded bits
+// per symbol), ties in (kv, layer) order; each pair's chunks consecutively.
+// Slices of one wave finish together less often than they start, so the
+// launch's last, partial wave is cheapest when it holds the lightest slices.
+struct SliceOrder {
+    uint16_t pair[2 * CG_MAX_LAYERS];  // kv * L + l
+};
+
+inline SliceOrder make_slice_order(const Dims &d, const MaxTab &mt) {
+    SliceOrder o;
+    int start[257] = {0};  // counting sort on 255 - MAX: stable, descending MAX
+    for (int kv = 0; kv < 2; kv++)
+        for (int l = 0; l < d.L; l++) start[256 - mt.v[kv][l]]++;
+    for (int key = 1; key <= 256; key++) start[key] += start[key - 1];
+    for (int kv = 0; kv < 2; kv++)
+        for (int l = 0; l < d.L; l++) o.pair[start[255 - mt.v[kv][l]]++] = (uint16_t)(kv * d.L + l);
+    return o;
+}
+
 // CTA = kThreads decoder threads (one per token stream) + one helper warp.
 // Iteration i: decoders decode window i with rows[i & 1] and write it out
 // while the helper stages rows[(i + 1) & 1]; one barrier per window.
@@ -519,8 +539,8 @@ template <int P, int MODE, bool V2, bool DELTA>
 __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     const uint8_t *__restrict__ packed, long long packed_bytes, const uint64_t *__restrict__ off,
     const uint32_t *__restrict__ len, const uint16_t *__restrict__ cdf, const uint8_t *__restrict__ rec,
-    const uint16_t *__restrict__ max1, Dims d, MaxTab mt, void *__restrict__ out_k, void *__restrict__ out_v,
-    long long ols, int32_t *status) {
+    const uint16_t *__restrict__ max1, Dims d, MaxTab mt, SliceOrder ord, void *__restrict__ out_k,
+    void *__restrict__ out_v, long long ols, int32_t *status) {
     using L = PipeSmem<P>;
     constexpr int W = L::W;
     constexpr int TS = L::TS;
@@ -532,8 +552,12 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     float *m1s = reinterpret_cast<float *>(smem + L::m1);
     uint8_t *srec = smem + L::recs;
 
-    int k, kv, l;
-    slice_coords(d, blockIdx.x, k, kv, l);
+    // CTA b takes chunk b mod nch of the (b / nch)-th (kv, layer) pair in
+    // decreasing-alphabet order: the costliest slices start first
+    const int pair = ord.pair[blockIdx.x / d.nch];
+    const int k = (int)(blockIdx.x % d.nch);
+    const int kv = pair >= d.L ? 1 : 0;
+    const int l = pair - kv * d.L;
     constexpr bool v2 = V2;  // format 2: CDF rows from count records
     const int A = v2 ? 2 * mt.v[kv][l] + 1 : d.A[kv];
     const uint32_t amax2 = 2u * ((uint32_t)A - 1);
@@ -683,7 +707,8 @@ cudaError_t launch_pm(const uint8_t *packed, uint64_t packed_bytes, const uint64
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     k_decode_pipe<P, MODE, V2, DELTA><<<nslices, kThreads + kHelpers, smem, s>>>(
-        packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols, status);
+        packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, make_slice_order(d, mt), out_k, out_v,
+        ols, status);
     return cudaGetLastError();
 }
 
