@@ -191,7 +191,7 @@ cg_status cg_decompress_chunk(const uint8_t *packed, uint64_t packed_bytes,
                               float *out_v, int32_t *status,
                               cudaStream_t stream);
 
-/* Compress without a workspace argument. The paper has no counterpart: this
+/* Compress without a workspace argument. The method itself has no counterpart: this
  * entry point exists for callers that cannot allocate device memory at all,
  * such as code living inside a host framework whose memory pool owns every
  * device byte and hands the codec only the tensors it works on, or a
