@@ -15,7 +15,8 @@
  *    bins arrays (HOST int32, read during the call and not kept).
  *  - The library allocates nothing. Scratch comes from the caller through a
  *    workspace pointer sized with cg_workspace_bytes().
- *  - Every call is asynchronous on the caller's stream; nothing synchronises.
+ *  - Every call is asynchronous on the caller's stream; nothing synchronises,
+ *    so the calls can be captured in a CUDA graph and replayed.
  *  - fp16 values are passed as their IEEE binary16 bit patterns (uint16_t).
  *  - The return value reports argument and launch errors, detected on the
  *    host before (or at) launch. Errors that depend on the data are OR-ed as
