@@ -244,9 +244,11 @@ uint64_t cg_record_bytes(const cg_shape *shape, const int32_t *bins_k,
 
 /* cg_compress_chunk in format 2: max1 as in format 1, rec gets the count
  * records (cg_record_bytes bytes), packed/len/off the streams coded with the
- * per-layer CDFs. Workspace: cg_compress_workspace_bytes. Runs on the fused
- * path only: every bins <= 33, C % 8 == 0, k and v 16-byte aligned with
- * layer_stride % 8 == 0; other arguments give CG_ERR_INVALID_ARG. */
+ * per-layer CDFs. Workspace: cg_compress_workspace_bytes. Any bins in
+ * [4, 256] and any C; requires chunk_tokens <= 256. (Every bins <= 33 with
+ * C % 8 == 0, k and v 16-byte aligned and layer_stride % 8 == 0 takes one
+ * fused kernel; other shapes take the quantise, count-and-code and pack
+ * steps, with the same output.) */
 cg_status cg_compress_chunk_v2(const uint16_t *k, const uint16_t *v,
                                const cg_shape *shape, const int32_t *bins_k,
                                const int32_t *bins_v, uint16_t *max1,
@@ -298,8 +300,8 @@ uint64_t cg_workspace_bytes_v3(const cg_shape *shape, const int32_t *bins_k,
 /* Compress in format 3 with token-locality groups of `group` (1: none):
  * max1, the side buffer (side_capacity >= cg_side3_max_bytes; its size is
  * cg_side3_fixed_bytes + O[nslice], the uint64 at byte 8*nslice), packed,
- * len and off. The limits of cg_compress_chunk_v2 apply. side must be 8-byte
- * aligned. */
+ * len and off. Requires chunk_tokens <= 256 and every layer alphabet
+ * 2 MAX + 1 <= 32 (bins <= 33); side must be 8-byte aligned. */
 cg_status cg_compress_chunk_v3(const uint16_t *k, const uint16_t *v,
                                const cg_shape *shape, const int32_t *bins_k,
                                const int32_t *bins_v, int32_t group,
@@ -383,8 +385,8 @@ cg_status cg_dequantize_delta(const uint8_t *sym, const uint16_t *max1,
 /* Quantise (with the delta when group > 1) -> CDF or count records -> encode
  * -> pack, either format: side = uint16 CDF entries (format 1,
  * cg_cdf_elems) or uint8 count records (format 2, cg_record_bytes).
- * Workspace: cg_compress_workspace_bytes. Format 2 has the limits of
- * cg_compress_chunk_v2; format 1 takes any shape. Decode with
+ * Workspace: cg_compress_workspace_bytes. Format 2 needs chunk_tokens <=
+ * 256; format 1 takes any shape. Decode with
  * cg_decompress_chunk_ex and the same format and group (chunk_tokens <= 256),
  * or, in format 1 with any chunk size, cg_decode then cg_dequantize_delta. */
 cg_status cg_compress_chunk_ex(const uint16_t *k, const uint16_t *v,

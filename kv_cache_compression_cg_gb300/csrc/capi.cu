@@ -329,13 +329,19 @@ cg_status cg_compress_chunk_v2(const uint16_t *k, const uint16_t *v, const cg_sh
         !aligned(workspace, kAlign))
         return CG_ERR_INVALID_ARG;
     if (workspace_bytes < encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d)) return CG_ERR_WORKSPACE;
-    // the fused kernel's limits, with format 2's alphabet
+    // the fused kernel where its limits allow (with format 2's alphabet), else
+    // the step path: quantise, then count -> records and CDF rows -> code
     Dims d2 = d;
     d2.A[0] = d2.A[1] = max_alphabet_v2(d, mt);
-    if (!cg::compress_fused_applies(d2, k, v)) return CG_ERR_INVALID_ARG;
     Workspace w = carve(workspace, d, true);
-    return launched(cg::launch_compress_fused(k, v, d, mt, max1, nullptr, rec, w.stage, len, off, packed, capacity,
-                                              w.state, status, stream));
+    if (cg::compress_fused_applies(d2, k, v))
+        return launched(cg::launch_compress_fused(k, v, d, mt, max1, nullptr, rec, w.stage, len, off, packed,
+                                                  capacity, w.state, status, stream));
+    if (cg::launch_quantize(k, v, d, mt, w.sym, max1, status, stream) != cudaSuccess) return CG_ERR_CUDA;
+    if (cg::launch_code_slices(w.sym, nullptr, nullptr, w.stage, len, d, 2, status, stream, &mt, rec) !=
+        cudaSuccess)
+        return CG_ERR_CUDA;
+    return launched(cg::launch_scan_and_pack(len, off, w.stage, packed, capacity, w.partials, d, status, stream));
 }
 
 cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off,
@@ -434,11 +440,10 @@ cg_status cg_compress_chunk_ex(const uint16_t *k, const uint16_t *v, const cg_sh
     if (cg::compress_fused_applies(df, k, v))
         return launched(cg::launch_compress_fused(k, v, d, mt, max1, cdf, rec, w.stage, len, off, packed, capacity,
                                                   w.state, status, stream));
-    if (format == 2) return CG_ERR_INVALID_ARG;  // format 2 runs on the fused path only
     cudaError_t e = group == 1 ? cg::launch_quantize(k, v, d, mt, w.sym, max1, status, stream)
                                : cg::launch_quantize_delta(k, v, d, mt, w.sym, max1, status, stream);
     if (e != cudaSuccess) return CG_ERR_CUDA;
-    if (cg::launch_code_slices(w.sym, nullptr, cdf, w.stage, len, d, 2, status, stream) != cudaSuccess)
+    if (cg::launch_code_slices(w.sym, nullptr, cdf, w.stage, len, d, 2, status, stream, &mt, rec) != cudaSuccess)
         return CG_ERR_CUDA;
     return launched(cg::launch_scan_and_pack(len, off, w.stage, packed, capacity, w.partials, d, status, stream));
 }
@@ -485,13 +490,24 @@ cg_status cg_compress_chunk_v3(const uint16_t *k, const uint16_t *v, const cg_sh
     d.G = group;
     Dims d2 = d;  // the fused kernel's limits, with format 2's alphabet
     d2.A[0] = d2.A[1] = max_alphabet_v2(d, mt);
-    if (!cg::compress_fused_applies(d2, k, v)) return CG_ERR_INVALID_ARG;
     Workspace w = carve(workspace, d, true);
     uint8_t *rec = static_cast<uint8_t *>(workspace) + encode_ws_bytes(d) + sym_bytes(d) + state_bytes(d);
     auto *totals = reinterpret_cast<unsigned long long *>(rec + round_up(record_bytes(d, mt), kAlign));
-    if (cg::launch_compress_fused(k, v, d, mt, max1, nullptr, rec, w.stage, len, off, packed, capacity, w.state,
-                                  status, stream) != cudaSuccess)
-        return CG_ERR_CUDA;
+    if (cg::compress_fused_applies(d2, k, v)) {
+        if (cg::launch_compress_fused(k, v, d, mt, max1, nullptr, rec, w.stage, len, off, packed, capacity, w.state,
+                                      status, stream) != cudaSuccess)
+            return CG_ERR_CUDA;
+    } else {  // the step path (any C, unaligned inputs)
+        cudaError_t e = group == 1 ? cg::launch_quantize(k, v, d, mt, w.sym, max1, status, stream)
+                                   : cg::launch_quantize_delta(k, v, d, mt, w.sym, max1, status, stream);
+        if (e != cudaSuccess) return CG_ERR_CUDA;
+        if (cg::launch_code_slices(w.sym, nullptr, nullptr, w.stage, len, d, 2, status, stream, &mt, rec) !=
+            cudaSuccess)
+            return CG_ERR_CUDA;
+        if (cg::launch_scan_and_pack(len, off, w.stage, packed, capacity, w.partials, d, status, stream) !=
+            cudaSuccess)
+            return CG_ERR_CUDA;
+    }
     return launched(cg::launch_v3_pack(rec, d, mt, side, totals, stream));
 }
 

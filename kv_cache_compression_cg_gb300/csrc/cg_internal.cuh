@@ -117,11 +117,13 @@ cudaError_t launch_quantize(const uint16_t *k, const uint16_t *v, const Dims &d,
                             int32_t *status, cudaStream_t s);
 
 // mode: 0 = count + build CDF only (cdf_out), 1 = encode with cdf_in,
-//       2 = count + build CDF (cdf_out) + encode.
+//       2 = count + build CDF (cdf_out) + encode. rec != nullptr: format 2
+//       (per-layer alphabets from mt, count records to rec instead of cdf_out).
 cudaError_t launch_code_slices(const uint8_t *sym, const uint16_t *cdf_in,
                                uint16_t *cdf_out, uint8_t *stage, uint32_t *len,
                                const Dims &d, int mode, int32_t *status,
-                               cudaStream_t s);
+                               cudaStream_t s, const MaxTab *mt = nullptr,
+                               uint8_t *rec = nullptr);
 
 cudaError_t launch_scan_and_pack(const uint32_t *len, uint64_t *off,
                                  const uint8_t *stage, uint8_t *packed,

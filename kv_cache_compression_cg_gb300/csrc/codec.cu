@@ -63,10 +63,12 @@ __host__ __device__ inline EncSmem enc_smem_layout(int NT, int A) {
 
 // ---- CDF normalisation of one channel (specification F), one warp -------
 // counts[0..A) -> packed[s] = lo | f << 16 and, when out != nullptr, the
-// uint16 row lo[0..A). ftab[n] = 1 + floor(n * (65536 - A) / Tk).
+// uint16 row lo[0..A); when rec != nullptr, the channel's format-2 count
+// record (the mode, then the other symbols' counts in increasing s).
+// ftab[n] = 1 + floor(n * (65536 - A) / Tk).
 __device__ __forceinline__ void build_cdf_row_warp(const uint16_t *counts, int A,
                                                    const uint16_t *ftab, uint32_t *packed,
-                                                   uint16_t *out, int lane) {
+                                                   uint16_t *out, uint8_t *rec, int lane) {
     unsigned key = 0, sum = 0;
     for (int s = lane; s < A; s += 32) {
         const unsigned n = counts[s];
@@ -77,6 +79,9 @@ __device__ __forceinline__ void build_cdf_row_warp(const uint16_t *counts, int A
     sum = __reduce_add_sync(0xFFFFFFFFu, sum);
     const int best = 255 - (int)(key & 255u);
     const unsigned extra = kM - sum;
+    if (rec)  // a count other than the mode's is at most Tk / 2 <= 128
+        for (int s = lane; s < A; s += 32)
+            rec[s == best ? 0 : s + (s < best ? 1 : 0)] = (uint8_t)(s == best ? best : counts[s]);
     unsigned run = 0;
     for (int base = 0; base < A; base += 32) {
         const int s = base + lane;
@@ -98,17 +103,21 @@ __device__ __forceinline__ void build_cdf_row_warp(const uint16_t *counts, int A
 
 // ---- slice coder kernel ---------------------------------------------------
 // mode 0: counts -> CDF rows only; 1: code with the caller's CDF rows;
-// 2: counts -> CDF rows -> code.
+// 2: counts -> CDF rows -> code. rec_out != nullptr (modes 0 and 2): format 2,
+// the layer's own alphabet 2 MAX + 1 and count records out instead of CDF
+// entries.
 __global__ void __launch_bounds__(1024, 1) k_code_slices(const uint8_t *__restrict__ sym,
                                                       const uint16_t *__restrict__ cdf_in,
                                                       uint16_t *__restrict__ cdf_out,
                                                       uint8_t *__restrict__ stage,
                                                       uint32_t *__restrict__ len, Dims d,
-                                                      int mode, int vec_rows, int32_t *status) {
+                                                      int mode, int vec_rows, int32_t *status, MaxTab mt,
+                                                      uint8_t *__restrict__ rec_out) {
     extern __shared__ __align__(16) unsigned char smem[];
     int k, kv, l;
     slice_coords(d, blockIdx.x, k, kv, l);
-    const int A = d.A[kv];
+    const int A = rec_out ? 2 * mt.v[kv][l] + 1 : d.A[kv];
+    const long long rec_base = rec_out ? record_slice_offset(d, mt, k, kv, l) : 0;
     const int Tk = chunk_tokens(d, k);
     const int NT = blockDim.x;
     const int nwarps = NT >> 5;
@@ -190,8 +199,8 @@ __global__ void __launch_bounds__(1024, 1) k_code_slices(const uint8_t *__restri
             __syncthreads();
             for (int c = warp; c < Wc; c += nwarps)
                 build_cdf_row_warp(total + c * A, A, ftab, cdfw + c * A,
-                                   cdf_out ? cdf_out + cdf_base + (long long)(c0 + c) * A : nullptr,
-                                   lane);
+                                   cdf_out && !rec_out ? cdf_out + cdf_base + (long long)(c0 + c) * A : nullptr,
+                                   rec_out ? rec_out + rec_base + (long long)(c0 + c) * A : nullptr, lane);
         } else {
             const uint16_t *src = cdf_in + cdf_base + (long long)c0 * A;
             for (int i = tid; i < Wc * A; i += NT) {
@@ -451,17 +460,28 @@ int block_threads(const Dims &d) {
 
 cudaError_t launch_code_slices(const uint8_t *sym, const uint16_t *cdf_in, uint16_t *cdf_out,
                                uint8_t *stage, uint32_t *len, const Dims &d, int mode,
-                               int32_t *status, cudaStream_t s) {
+                               int32_t *status, cudaStream_t s, const MaxTab *mt, uint8_t *rec) {
     const long long nslices = 2LL * d.L * d.nch;
     const int NT = block_threads(d);
-    const size_t s0 = enc_smem_layout(NT, d.A[0]).bytes, s1 = enc_smem_layout(NT, d.A[1]).bytes;
-    const size_t smem = s0 > s1 ? s0 : s1;
+    size_t smem = 0;
+    MaxTab m{};
+    if (rec) {  // format 2: every layer's own alphabet
+        m = *mt;
+        for (int kv = 0; kv < 2; kv++)
+            for (int l = 0; l < d.L; l++) {
+                const size_t b = enc_smem_layout(NT, 2 * m.v[kv][l] + 1).bytes;
+                smem = b > smem ? b : smem;
+            }
+    } else {
+        const size_t s0 = enc_smem_layout(NT, d.A[0]).bytes, s1 = enc_smem_layout(NT, d.A[1]).bytes;
+        smem = s0 > s1 ? s0 : s1;
+    }
     cudaError_t err = cudaFuncSetAttribute(k_code_slices, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);
     if (err != cudaSuccess) return err;
     const int vec_rows = (d.C % 16) == 0 && (reinterpret_cast<uintptr_t>(sym) & 15) == 0;
     k_code_slices<<<(unsigned)nslices, NT, smem, s>>>(sym, cdf_in, cdf_out, stage, len, d, mode, vec_rows,
-                                                      status);
+                                                      status, m, rec);
     return cudaGetLastError();
 }
 

@@ -105,23 +105,41 @@ def test_fused_delta_matches_oracle(cg, oracle_mod, case, fmt):
     assert np.array_equal(got[:, 1], oracle_mod.floats_to_half(wv))
 
 
-def test_generic_compress_path_with_delta(cg, oracle_mod):
+@pytest.mark.parametrize("fmt", [1, 2, 3])
+def test_generic_compress_path_with_delta(cg, oracle_mod, fmt):
     """C % 8 != 0 takes the step kernels (quantise with the delta, slice
-    coder, scan) inside cg_compress_chunk_ex; the decoder stays fused."""
+    coder, scan) inside the compress entry points, in every format (format 2
+    with a 64-bin layer, whose alphabet is past the fused kernel's too); the
+    decoder stays fused."""
     L, T, C_, Tc, G = 2, 150, 12, 64, 5
-    bk, bv = [16, 64], [8, 16]
+    bk, bv = ([16, 32], [8, 16]) if fmt == 3 else ([16, 64], [8, 16])
     k = _correlated(5, L, T, C_)
     v = _correlated(6, L, T, C_)
-    ref = oracle_mod.compress_ex(k, v, Tc, bk, bv, fmt=1, group=G)
-    cd = cg.Codec(L, T, C_, bk, bv, chunk_tokens=Tc, group=G)
+    if fmt == 3:
+        ref = oracle_mod.compress_v3(k, v, Tc, bk, bv, group=G)
+    else:
+        ref = oracle_mod.compress_ex(k, v, Tc, bk, bv, fmt=fmt, group=G)
+    cd = cg.Codec(L, T, C_, bk, bv, chunk_tokens=Tc, fmt=fmt, group=G)
     out = cd.compress(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
     ok, ov = cd.decompress()
     torch.cuda.synchronize()
     assert int(out.status.item()) == 0 and int(cd.dstatus.item()) == 0
+    assert np.array_equal(out.max1.cpu().numpy().view(np.uint16), ref["max1"])
+    assert np.array_equal(out.len[:2 * L * T].cpu().numpy().view(np.uint32), ref["len"])
+    assert np.array_equal(out.off.cpu().numpy().view(np.uint64), ref["off"])
     assert np.array_equal(out.packed[:int(ref["off"][-1])].cpu().numpy(), ref["packed"])
-    assert np.array_equal(out.cdf[:cd.cdf_elems].cpu().numpy().view(np.uint16), ref["cdf"])
-    wk, wv = oracle_mod.decompress_ex(ref["packed"], ref["off"], ref["len"], ref["cdf"], ref["max1"],
-                                      L, T, C_, Tc, bk, bv, fmt=1, group=G)
+    if fmt == 1:
+        assert np.array_equal(out.cdf[:cd.cdf_elems].cpu().numpy().view(np.uint16), ref["cdf"])
+        wk, wv = oracle_mod.decompress_ex(ref["packed"], ref["off"], ref["len"], ref["cdf"], ref["max1"],
+                                          L, T, C_, Tc, bk, bv, fmt=1, group=G)
+    elif fmt == 2:
+        assert np.array_equal(out.rec[:cd.rec_bytes].cpu().numpy(), ref["rec"])
+        wk, wv = oracle_mod.decompress_ex(ref["packed"], ref["off"], ref["len"], ref["rec"], ref["max1"],
+                                          L, T, C_, Tc, bk, bv, fmt=2, group=G)
+    else:
+        assert np.array_equal(out.side3[:out.side3_bytes()].cpu().numpy(), ref["side"])
+        wk, wv = oracle_mod.decompress_v3(ref["packed"], ref["len"], ref["side"], ref["max1"],
+                                          L, T, C_, Tc, bk, bv, group=G)
     assert np.array_equal(ok.cpu().numpy().view(np.uint32), wk.view(np.uint32))
     assert np.array_equal(ov.cpu().numpy().view(np.uint32), wv.view(np.uint32))
 

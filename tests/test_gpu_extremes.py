@@ -48,9 +48,9 @@ def _extremes(fmt):
     k[3, 10] = 0.0
     k[3, 11] = -0.0
     v[3] = rng.standard_t(3, size=(T, C_)).astype(np.float16)
-    if fmt >= 2:  # count records run on the fused path: every bins <= 33
+    if fmt == 3:  # compact records: every layer alphabet within 32 symbols
         bk, bv = [32, 4, 32, 16], [16, 32, 8, 33]
-    else:  # format 1 also takes the widest alphabets (the generic path)
+    else:  # the widest alphabets take the step path
         bk, bv = [32, 4, 256, 16], [16, 32, 8, 255]
     return k, v, Tc, bk, bv
 

@@ -27,7 +27,8 @@ def _case(synth_mod, name):
     rng = np.random.default_rng(len(name) + 50)
     shapes = {"ragged": (3, 200, 40, 64, [32, 16, 8], [16, 16, 16]),
               "odd_bins": (2, 96, 16, 32, [7, 5], [33, 4]),
-              "t1": (2, 1, 8, 256, [16, 32], [4, 8])}
+              "t1": (2, 1, 8, 256, [16, 32], [4, 8]),
+              "odd_c": (2, 70, 13, 64, [16, 32], [8, 33])}  # C % 8 != 0: the step path
     L, T, C_, Tc, bk, bv = shapes[name]
     k = (rng.standard_normal((L, T, C_)) * rng.lognormal(0, 0.5, (1, 1, C_))).astype(np.float16)
     v = (rng.standard_normal((L, T, C_)) * 0.5).astype(np.float16)
@@ -35,7 +36,7 @@ def _case(synth_mod, name):
 
 
 @pytest.mark.parametrize("G", [1, 10])
-@pytest.mark.parametrize("case", ["tiny", "ragged", "odd_bins", "t1", "mistral_chunk",
+@pytest.mark.parametrize("case", ["tiny", "ragged", "odd_bins", "t1", "odd_c", "mistral_chunk",
                                   pytest.param("ctx4096", marks=pytest.mark.slow)])
 def test_v3_parity_with_oracle(cg, oracle_mod, synth_mod, case, G):
     k, v, Tc, bk, bv = _case(synth_mod, case)
