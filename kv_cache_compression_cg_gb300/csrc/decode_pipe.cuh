@@ -242,21 +242,23 @@ __device__ __forceinline__ void copy_records(uint8_t *srec, const uint8_t *recw,
 }
 
 // Format 2, step 2 (the 256 decoder threads): the window's CDF rows rebuilt
-// from its records in shared memory. Four threads share a channel (t >> 2),
-// each owning P / 4 consecutive symbols: counts -> f(n) through the slice's
-// table, four-lane sums of the counts, a four-lane scan of f, the remainder
-// to the record's mode (which shifts the running sum of the symbols after
-// it); entries at or past A hold 65535 / 0. A record whose mode byte is
-// outside the alphabet or whose counts exceed Tk is corrupt: its channel gets
-// every token on the mode (symbol 0 when the mode byte is invalid) and the
-// function returns true. Channels at or past Wc (a partial last window) are
-// built from unused bytes into rows no window reads, and not checked.
+// from its records in shared memory. TPC = 256 / W threads share a channel
+// (four for P <= 32, eight for P = 64, sixteen for wider rows), each owning
+// P / TPC consecutive symbols: counts -> f(n) through the slice's table,
+// TPC-lane sums of the counts, a TPC-lane scan of f, the remainder to the
+// record's mode (which shifts the running sum of the symbols after it);
+// entries at or past A hold 65535 / 0. A record whose mode byte is outside
+// the alphabet or whose counts exceed Tk is corrupt: its channel gets every
+// token on the mode (symbol 0 when the mode byte is invalid) and the function
+// returns true. Channels at or past Wc (a partial last window) are built from
+// unused bytes into rows no window reads, and not checked.
 template <int P>
 __device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, const uint8_t *srec, int A, uint32_t Tk,
                                               int W, int Wc, int t, const uint16_t *ftab) {
-    constexpr int SP = P / 4;  // symbols per thread
-    const int c = t >> 2, p = t & 3;
-    if (c >= W) return false;  // whole four-lane groups
+    constexpr int TPC = kThreads / DecodeCfg<P>::W;  // threads per channel
+    constexpr int SP = P / TPC;                       // symbols per thread
+    const int c = t / TPC, p = t % TPC;
+    if (c >= W) return false;  // whole TPC-lane groups
     const int j0 = p * SP;
     const uint8_t *r = srec + c * A;
     int mode = r[0];
@@ -272,8 +274,8 @@ __device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, cons
             n[jj] = count_at(j0 + jj);
             others += n[jj];
         }
-        others += __shfl_xor_sync(0xFFFFFFFFu, others, 1);
-        others += __shfl_xor_sync(0xFFFFFFFFu, others, 2);
+#pragma unroll
+        for (int o = 1; o < TPC; o <<= 1) others += __shfl_xor_sync(0xFFFFFFFFu, others, o);
         const bool ok = mode < A && others <= Tk;
         if (!ok) mode = mode < A ? mode : 0;
         const uint32_t nmode = ok ? Tk - others : Tk;
@@ -285,11 +287,12 @@ __device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, cons
             fl += fv[jj];
         }
         uint32_t incl = fl;
-        uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
-        if (p >= 1) incl += v;
-        v = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
-        if (p >= 2) incl += v;
-        const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
+#pragma unroll
+        for (int o = 1; o < TPC; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o, TPC);
+            if (p >= o) incl += v;
+        }
+        const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, TPC - 1, TPC);
         uint32_t acc = incl - fl;
         uint32_t *cr = reinterpret_cast<uint32_t *>(cum + c * P + j0);  // j0 and SP even: 4-byte aligned
         uint32_t *fr = reinterpret_cast<uint32_t *>(frq + c * P + j0);
@@ -311,8 +314,8 @@ __device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, cons
         uint32_t others = 0;
 #pragma unroll 1
         for (int jj = 0; jj < SP; jj++) others += count_at(j0 + jj);
-        others += __shfl_xor_sync(0xFFFFFFFFu, others, 1);
-        others += __shfl_xor_sync(0xFFFFFFFFu, others, 2);
+#pragma unroll
+        for (int o = 1; o < TPC; o <<= 1) others += __shfl_xor_sync(0xFFFFFFFFu, others, o);
         const bool ok = mode < A && others <= Tk;
         if (!ok) mode = mode < A ? mode : 0;
         const uint32_t nmode = ok ? Tk - others : Tk;
@@ -325,11 +328,12 @@ __device__ __forceinline__ bool build_rows_v2(uint16_t *cum, uint16_t *frq, cons
 #pragma unroll 1
         for (int jj = 0; jj < SP; jj++) fl += f_at(jj);
         uint32_t incl = fl;
-        uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
-        if (p >= 1) incl += v;
-        v = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
-        if (p >= 2) incl += v;
-        const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
+#pragma unroll
+        for (int o = 1; o < TPC; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o, TPC);
+            if (p >= o) incl += v;
+        }
+        const uint32_t rem = kM - __shfl_sync(0xFFFFFFFFu, incl, TPC - 1, TPC);
         uint32_t acc = incl - fl;
         uint16_t *cr = cum + c * P;
         uint16_t *fr = frq + c * P;
