@@ -53,8 +53,8 @@ __host__ __device__ inline EncSmem enc_smem_layout(int NT, int A) {
     o = (o + 15) & ~(size_t)15;
     s.cdf_off = o;  // W*A uint32: lo | f << 16
     o += (size_t)s.W * A * 4;
-    s.total_off = o;  // W*A uint16 symbol counts
-    o += (size_t)s.W * A * 2;
+    s.total_off = o;  // A x (W + 1) uint32 symbol counts, [symbol][channel]
+    o += (size_t)(s.W + 1) * A * 4;
     s.ftab_off = o;  // f(n) for n = 0..NT, uint16
     o += (size_t)(NT + 1) * 2;
     s.bytes = (o + 15) & ~(size_t)15;
@@ -62,16 +62,16 @@ __host__ __device__ inline EncSmem enc_smem_layout(int NT, int A) {
 }
 
 // ---- CDF normalisation of one channel (specification F), one warp -------
-// counts[0..A) -> packed[s] = lo | f << 16 and, when out != nullptr, the
+// counts[s * cs] for s in [0, A) -> packed[s] = lo | f << 16 and, when out != nullptr, the
 // uint16 row lo[0..A); when rec != nullptr, the channel's format-2 count
 // record (the mode, then the other symbols' counts in increasing s).
 // ftab[n] = 1 + floor(n * (65536 - A) / Tk).
-__device__ __forceinline__ void build_cdf_row_warp(const uint16_t *counts, int A,
+__device__ __forceinline__ void build_cdf_row_warp(const uint32_t *counts, int cs, int A,
                                                    const uint16_t *ftab, uint32_t *packed,
                                                    uint16_t *out, uint8_t *rec, int lane) {
     unsigned key = 0, sum = 0;
     for (int s = lane; s < A; s += 32) {
-        const unsigned n = counts[s];
+        const unsigned n = counts[s * cs];
         key = max(key, (n << 8) | (255u - (unsigned)s));  // largest n, then smallest s
         sum += ftab[n];
     }
@@ -81,11 +81,11 @@ __device__ __forceinline__ void build_cdf_row_warp(const uint16_t *counts, int A
     const unsigned extra = kM - sum;
     if (rec)  // a count other than the mode's is at most Tk / 2 <= 128
         for (int s = lane; s < A; s += 32)
-            rec[s == best ? 0 : s + (s < best ? 1 : 0)] = (uint8_t)(s == best ? best : counts[s]);
+            rec[s == best ? 0 : s + (s < best ? 1 : 0)] = (uint8_t)(s == best ? best : counts[s * cs]);
     unsigned run = 0;
     for (int base = 0; base < A; base += 32) {
         const int s = base + lane;
-        const unsigned f = (s < A) ? (unsigned)ftab[counts[s]] + (s == best ? extra : 0u) : 0u;
+        const unsigned f = (s < A) ? (unsigned)ftab[counts[s * cs]] + (s == best ? extra : 0u) : 0u;
         unsigned incl = f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(1024, 1) k_code_slices(const uint8_t *__restri
     const int ts = lay.tile_stride;
     uint8_t *tile = smem + lay.tile_off;
     uint32_t *cdfw = reinterpret_cast<uint32_t *>(smem + lay.cdf_off);
-    uint16_t *total = reinterpret_cast<uint16_t *>(smem + lay.total_off);
+    uint32_t *total = reinterpret_cast<uint32_t *>(smem + lay.total_off);
+    const int cs = W + 1;  // counter row stride: channel c of symbol q at q * cs + c
     uint16_t *ftab = reinterpret_cast<uint16_t *>(smem + lay.ftab_off);
 
     const int tid = threadIdx.x;
@@ -172,33 +173,30 @@ __global__ void __launch_bounds__(1024, 1) k_code_slices(const uint8_t *__restri
                 for (int j = lane; j < Wc; j += 32) tile[r * ts + j] = rows[(long long)r * d.C + c0 + j];
         }
         if (do_count)
-            for (int i = tid; i < Wc * A; i += NT) total[i] = 0;
+            for (int i = tid; i < cs * A; i += NT) total[i] = 0;
         __syncthreads();
 
         // 2. per-channel CDF rows for this window
         if (do_count) {
-            // warp w owns channels w, w + nwarps, ...; lanes take 32 tokens at a
-            // time and equal symbols are merged with a match, so each counter has
-            // one writer per step
-            for (int c = warp; c < Wc; c += nwarps) {
-                uint16_t *cc = total + c * A;
-                for (int tb = 0; tb < Tk; tb += 32) {
-                    const int t = tb + lane;
-                    unsigned q = 0xFFFFu;
-                    if (t < Tk) {
-                        q = tile[t * ts + c];
-                        if (q >= (unsigned)A) {
-                            bad = 1;
-                            q = A - 1;
-                        }
+            // each thread counts its token's Wc symbols by shared adds, lane l
+            // starting at channel l mod Wc so that the lanes of a warp add to
+            // different channels (the padded stride puts them in different banks)
+            if (tid < Tk) {
+                const uint8_t *my = tile + tid * ts;
+                int c = lane % Wc;
+                for (int j = 0; j < Wc; j++) {
+                    unsigned q = my[c];
+                    if (q >= (unsigned)A) {
+                        bad = 1;
+                        q = A - 1;
                     }
-                    const unsigned peers = __match_any_sync(0xFFFFFFFFu, q);
-                    if (t < Tk && lane == __ffs(peers) - 1) cc[q] += (uint16_t)__popc(peers);
+                    atomicAdd(total + q * cs + c, 1u);
+                    c = c + 1 == Wc ? 0 : c + 1;
                 }
             }
             __syncthreads();
             for (int c = warp; c < Wc; c += nwarps)
-                build_cdf_row_warp(total + c * A, A, ftab, cdfw + c * A,
+                build_cdf_row_warp(total + c, cs, A, ftab, cdfw + c * A,
                                    cdf_out && !rec_out ? cdf_out + cdf_base + (long long)(c0 + c) * A : nullptr,
                                    rec_out ? rec_out + rec_base + (long long)(c0 + c) * A : nullptr, lane);
         } else {
