@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--piece-chunks", type=int, default=2,
                     help="chunks per piece of the streamed end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-call figures of the other seeded workloads")
     ap.add_argument("--no-chunk-parallel", action="store_true",
                     help="skip the oracle's chunk-parallel timing on all host cores")
     ap.add_argument("--group", type=int, default=1,
@@ -165,6 +167,74 @@ def workload_config(w, extra=None):
     if extra:
         cfg.update(extra)
     return cfg
+
+
+def side_bytes(cd, out, w, fmt):
+    """Side information that travels with the streams: CDF entries, count
+    records or the format 3 side buffer; max1; lengths; offsets (format 3
+    rebuilds them from the lengths)."""
+    side_info = {1: 2 * cd.cdf_elems, 2: cd.rec_bytes}.get(fmt) or out.side3_bytes()
+    return side_info + 2 * 2 * w.L * w.T + 4 * cd.nstreams + (8 * (cd.nstreams + 1) if fmt < 3 else 0)
+
+
+WORKLOAD_SET = ("tiny", "mistral_chunk", "uniform", "ctx32k", "stress80k")
+
+
+def other_workloads(args, hbm, flush, skip):
+    """Per-call compress and decompress figures of the other seeded workloads
+    (inputs from the device generator, resident in HBM; each call timed alone
+    with CUDA events on the launching stream, an L2-sized buffer written
+    before each; mean of 5 after 3 warm-ups)."""
+    import torch
+    from kv_cache_compression_cg_gb300 import codec, synth
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in WORKLOAD_SET:
+        if name == skip:
+            continue
+        w = synth.WORKLOADS[name]
+        k, v = synth.generate_device(w)
+        cd = codec.Codec(w.L, w.T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens, fmt=args.format,
+                         group=args.group)
+        for _ in range(3):
+            cd.compress(k, v)
+            cd.decompress()
+        torch.cuda.synchronize()
+
+        def timed(fn):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+            for a, b in evs:
+                flush.zero_()
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+        cms = timed(lambda: cd.compress(k, v))
+        dms = timed(cd.decompress)
+        out = cd.out
+        total = out.total_bytes()
+        status = int(out.status.item()) | int(cd.dstatus.item())
+        n_el = 2 * w.L * w.T * w.C
+        fp16 = 2 * n_el
+        side = side_bytes(cd, out, w, args.format)
+        c_alg, d_alg = fp16 + total + side, total + side + 4 * n_el
+        res[name] = {
+            "shape_per_kv": [w.L, w.T, w.C], "chunks": w.n_chunks, "slices": 2 * w.L * w.n_chunks,
+            "compress_ms": cms, "decompress_ms": dms,
+            "compress_gbs": fp16 / (cms * 1e-3) / 1e9, "decompress_gbs": fp16 / (dms * 1e-3) / 1e9,
+            "compress_frac_of_hbm": {"fp16_in": fp16 / (cms * 1e-3) / 1e9 / hbm,
+                                     "algorithmic": c_alg / (cms * 1e-3) / 1e9 / hbm},
+            "decompress_frac_of_hbm": {"fp16_in": fp16 / (dms * 1e-3) / 1e9 / hbm,
+                                       "algorithmic": d_alg / (dms * 1e-3) / 1e9 / hbm},
+            "compression_ratio": {"total": fp16 / (total + side), "payload": fp16 / total,
+                                  "bits_per_symbol": 8 * total / n_el},
+            "status_word": status,
+        }
+        del cd, k, v, out
+        torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -375,10 +445,7 @@ def run_ours(args):
     comp_kernel_ms = time_call(lambda: cd.compress(k, v))
     dec_kernel_ms = time_call(cd.decompress)
     n_el = 2 * w.L * w.T * w.C
-    # side information that travels with the streams: CDF entries, count records or the
-    # format 3 side buffer; max1; lengths; offsets (format 3 rebuilds them from the lengths)
-    side_info = {1: 2 * cd.cdf_elems, 2: cd.rec_bytes}.get(args.format) or out.side3_bytes()
-    side = side_info + 2 * 2 * w.L * w.T + 4 * cd.nstreams + (8 * (cd.nstreams + 1) if args.format < 3 else 0)
+    side = side_bytes(cd, out, w, args.format)
     dec_alg_bytes = total + side + 4 * n_el
     comp_alg_bytes = fp16_bytes + total + side
     A = max(max(w.bins_k), max(w.bins_v))
@@ -395,19 +462,24 @@ def run_ours(args):
         "decompress": ("k_decode_pipe (decode + dequantise)", dec_kernel_ms,
                        alg_ops_decode(P), dec_alg_bytes, ["decode_pipe.cuh", "decode.cu", "cg_internal.cuh"]),
     }
+    def roof(which):
+        kname, kms, ops, kbytes, srcs = kern[which]
+        achieved = kbytes / (kms * 1e-3) / 1e9
+        alu = n_el * ops / (kms * 1e-3) / 1e12
+        return {
+            "kernel": kname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+            "measured" else "fallback", "algorithmic_bytes": kbytes, "ms": kms,
+            "traffic": kernel_traffic(f"{kname.split()[0]}_{args.workload}_f{args.format}_g{args.group}", srcs),
+            "alu": {"achieved": alu, "peak": peak_tops, "unit": "Tops/s", "frac": alu / peak_tops,
+                    "ops_per_symbol": ops,
+                    "peak_kind": f"derived: {props.multi_processor_count} SMs x 4 schedulers x 32 lanes x "
+                                 f"{max_mhz:g} MHz"},
+        }
+
     dom = "compress" if comp_kernel_ms >= dec_kernel_ms else "decompress"
-    kname, kms, ops, kbytes, srcs = kern[dom]
-    achieved = n_el * ops / (kms * 1e-3) / 1e12
-    hbm_achieved = kbytes / (kms * 1e-3) / 1e9
-    roofline = {
-        "kernel": kname, "bound": "alu", "achieved": achieved, "peak": peak_tops, "unit": "Tops/s",
-        "frac": achieved / peak_tops,
-        "traffic": kernel_traffic(f"{kname.split()[0]}_{args.workload}_f{args.format}_g{args.group}", srcs),
-        "peak_kind": f"derived: {props.multi_processor_count} SMs x 4 schedulers x 32 lanes x {max_mhz:g} MHz",
-        "ops_per_symbol": ops, "algorithmic_bytes": kbytes, "ms": kms,
-        "hbm": {"achieved": hbm_achieved, "peak": hbm, "unit": "GB/s", "frac": hbm_achieved / hbm,
-                "peak_kind": peak_kind},
-    }
+    roofline = roof(dom)
+    rooflines = {"compress": roof("compress"), "decompress": roof("decompress")}
 
     comp_gbs = fp16_bytes / (statistics.mean(comp_ms) * 1e-3) / 1e9
     dec_gbs = fp16_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9
@@ -416,7 +488,10 @@ def run_ours(args):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "dtype_detail": "fp16 K/V in; binary32 quantise and dequantise; 32-bit integer range coder; "
+                        "binary32 K/V out",
+        "data": "synthetic",
         "config": workload_config(w, {"parallelism": f"chunk-sharded x{world}" if world > 1 else "1 GPU",
                                       "format": args.format, "delta_group": args.group}),
         "compress_gbs": comp_gbs, "decompress_gbs": dec_gbs,
@@ -427,7 +502,7 @@ def run_ours(args):
                                    "algorithmic": dec_alg_bytes / (statistics.mean(dec_ms) * 1e-3) / 1e9 / hbm},
         "compression_ratio": {"total": fp16_bytes / (total + side), "payload": fp16_bytes / total,
                               "bits_per_symbol": 8 * total / n_el},
-        "roofline": roofline,
+        "roofline": roofline, "rooflines": rooflines,
         "reconstruction_rel_rmse": rel_rmse,
         "status_word": status, "clocks": clocks, "wall_s_timed_region": wall,
         "gpu_launches": (KERNELS_PER_STEP + (7 if args.format == 3 else 0)) * args.steps,
@@ -435,6 +510,8 @@ def run_ours(args):
 
     if not args.no_e2e:
         result["e2e"] = e2e(args, w, cd, k_pin, v_pin, fp16_bytes)
+    if rank == 0 and world == 1 and not args.no_workloads:
+        result["workloads"] = other_workloads(args, hbm, flush, args.workload)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_dt, cpu_bytes = oracle_step_time(k_h, v_h, w, min(w.T, 2 * w.chunk_tokens), args.format, args.group)
         reps = max(1, int(10.0 / max(cpu_dt, 1e-3)))

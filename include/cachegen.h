@@ -208,6 +208,9 @@ cg_status cg_decompress_chunk(const uint8_t *packed, uint64_t packed_bytes,
  *  - Calls no allocating routine. The first call on each device looks the
  *    array's device address up (cudaGetSymbolAddress, with that device
  *    current) and caches it; make that first call before any stream capture.
+ *    The cached address belongs to the device's primary context: after a
+ *    cudaDeviceReset of that device it is stale, so do not call this entry
+ *    point on a device that has been reset in the same process.
  *  - All calls on a device share the one array and it keeps the last call's
  *    contents (no byte of it is read before the same call wrote it). Calls
  *    that overlap on the GPU (other streams, other host threads) race on it:

@@ -197,6 +197,7 @@ const char *cg_version(void) { return "cachegen-gb300 formats-1,2,3 delta sm_103
 cg_status cg_quantize(const uint16_t *k, const uint16_t *v, const cg_shape *shape,
                       const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym, uint16_t *max1,
                       int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
@@ -209,6 +210,7 @@ cg_status cg_quantize(const uint16_t *k, const uint16_t *v, const cg_shape *shap
 cg_status cg_calculate_cdf(const uint8_t *sym, const cg_shape *shape, const int32_t *bins_k,
                            const int32_t *bins_v, uint16_t *cdf, int32_t *status,
                            cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     if (!prepare(shape, bins_k, bins_v, d, nullptr)) return CG_ERR_INVALID_ARG;
     if (!sym || !cdf || !aligned(cdf, 2)) return CG_ERR_INVALID_ARG;
@@ -220,6 +222,7 @@ cg_status cg_encode(const uint8_t *sym, const uint16_t *cdf, const cg_shape *sha
                     const int32_t *bins_k, const int32_t *bins_v, uint8_t *packed,
                     uint64_t capacity, uint32_t *len, uint64_t *off, void *workspace,
                     uint64_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     if (!prepare(shape, bins_k, bins_v, d, nullptr)) return CG_ERR_INVALID_ARG;
     if (!off) return CG_ERR_INVALID_ARG;
@@ -239,6 +242,7 @@ cg_status cg_decode(const uint8_t *packed, uint64_t packed_bytes, const uint64_t
                     const uint32_t *len, const uint16_t *cdf, const cg_shape *shape,
                     const int32_t *bins_k, const int32_t *bins_v, uint8_t *sym, int32_t *status,
                     cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
@@ -253,6 +257,7 @@ cg_status cg_decode(const uint8_t *packed, uint64_t packed_bytes, const uint64_t
 cg_status cg_dequantize(const uint8_t *sym, const uint16_t *max1, const cg_shape *shape,
                         const int32_t *bins_k, const int32_t *bins_v, float *out_k, float *out_v,
                         int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     (void)status;
     Dims d;
     MaxTab mt;
@@ -269,6 +274,7 @@ cg_status cg_compress_chunk(const uint16_t *k, const uint16_t *v, const cg_shape
                             uint16_t *cdf, uint8_t *packed, uint64_t capacity, uint32_t *len,
                             uint64_t *off, void *workspace, uint64_t workspace_bytes,
                             int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
@@ -295,6 +301,7 @@ cg_status cg_decompress_chunk(const uint8_t *packed, uint64_t packed_bytes, cons
                               const uint32_t *len, const uint16_t *cdf, const uint16_t *max1,
                               const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v,
                               float *out_k, float *out_v, int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt)) return CG_ERR_INVALID_ARG;
@@ -319,6 +326,7 @@ cg_status cg_compress_chunk_v2(const uint16_t *k, const uint16_t *v, const cg_sh
                                uint8_t *packed, uint64_t capacity, uint32_t *len, uint64_t *off,
                                void *workspace, uint64_t workspace_bytes, int32_t *status,
                                cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return CG_ERR_INVALID_ARG;
@@ -348,6 +356,7 @@ cg_status cg_decompress_chunk_v2(const uint8_t *packed, uint64_t packed_bytes, c
                                  const uint32_t *len, const uint8_t *rec, const uint16_t *max1,
                                  const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v,
                                  float *out_k, float *out_v, int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return CG_ERR_INVALID_ARG;
@@ -365,6 +374,7 @@ cg_status cg_decompress_chunk_ex(const uint8_t *packed, uint64_t packed_bytes, c
                                  const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v, int format,
                                  int32_t group, int out_dtype, void *out_k, void *out_v,
                                  int64_t out_layer_stride, int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || d.Tc > 256) return CG_ERR_INVALID_ARG;
@@ -388,6 +398,7 @@ cg_status cg_decompress_chunk_ex(const uint8_t *packed, uint64_t packed_bytes, c
 cg_status cg_quantize_delta(const uint16_t *k, const uint16_t *v, const cg_shape *shape, const int32_t *bins_k,
                             const int32_t *bins_v, int32_t group, uint8_t *sym, uint16_t *max1, int32_t *status,
                             cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || !group_ok(group)) return CG_ERR_INVALID_ARG;
@@ -402,6 +413,7 @@ cg_status cg_quantize_delta(const uint16_t *k, const uint16_t *v, const cg_shape
 cg_status cg_dequantize_delta(const uint8_t *sym, const uint16_t *max1, const cg_shape *shape,
                               const int32_t *bins_k, const int32_t *bins_v, int32_t group, float *out_k,
                               float *out_v, int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     (void)status;
     Dims d;
     MaxTab mt;
@@ -419,6 +431,7 @@ cg_status cg_compress_chunk_ex(const uint16_t *k, const uint16_t *v, const cg_sh
                                const int32_t *bins_v, int format, int32_t group, uint16_t *max1, void *side,
                                uint8_t *packed, uint64_t capacity, uint32_t *len, uint64_t *off, void *workspace,
                                uint64_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || !group_ok(group) || (format != 1 && format != 2))
@@ -476,6 +489,7 @@ cg_status cg_compress_chunk_v3(const uint16_t *k, const uint16_t *v, const cg_sh
                                uint64_t side_capacity, uint8_t *packed, uint64_t capacity, uint32_t *len,
                                uint64_t *off, void *workspace, uint64_t workspace_bytes, int32_t *status,
                                cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || !v3_ok(d, mt) || !group_ok(group)) return CG_ERR_INVALID_ARG;
@@ -516,6 +530,7 @@ cg_status cg_decompress_chunk_v3(const uint8_t *packed, uint64_t packed_bytes, c
                                  const cg_shape *shape, const int32_t *bins_k, const int32_t *bins_v,
                                  int32_t group, int out_dtype, void *out_k, void *out_v, int64_t out_layer_stride,
                                  void *workspace, uint64_t workspace_bytes, int32_t *status, cudaStream_t stream) {
+    CG_TRACE_RANGE();
     Dims d;
     MaxTab mt;
     if (!prepare(shape, bins_k, bins_v, d, &mt) || !v3_ok(d, mt) || !group_ok(group)) return CG_ERR_INVALID_ARG;

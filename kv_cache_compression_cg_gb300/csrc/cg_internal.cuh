@@ -6,10 +6,22 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/cachegen.h"
 
 namespace cg {
+
+// NVTX range over one ABI call, named after the entry point: a profiler or
+// tracer attached to the process shows each call's launches under its name;
+// with no tool attached the push and pop return at once.
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
+#define CG_TRACE_RANGE() ::cg::TraceRange cg_trace_range_(__func__)
 
 // Per-call geometry, passed by value to every kernel.
 struct Dims {

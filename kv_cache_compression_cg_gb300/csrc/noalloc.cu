@@ -46,6 +46,7 @@ extern "C" cg_status cg_compress_chunk_noalloc(const uint16_t *k, const uint16_t
                                                uint16_t *cdf, uint8_t *packed, uint64_t capacity,
                                                uint32_t *len, uint64_t *off, int32_t *status,
                                                cudaStream_t stream) {
+    CG_TRACE_RANGE();
     const uint64_t need = cg_compress_workspace_bytes(shape);
     if (need == 0) return CG_ERR_INVALID_ARG;
     if (need > CG_NOALLOC_WORKSPACE_BYTES) return CG_ERR_WORKSPACE;

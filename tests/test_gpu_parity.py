@@ -72,7 +72,7 @@ def _synth(synth_mod, name, T=None):
 
 
 CASES = ["tiny", "ragged", "c48_tc32_bins256", "c24_tc70", "c8_t1", "c16_tc1", "mistral_chunk",
-         "uniform"]
+         "uniform", "c24_tc600_bins255"]
 
 
 def make_case(name, synth_mod):
@@ -88,6 +88,8 @@ def make_case(name, synth_mod):
         return _shape_case(3, 1, 8, 256, [16, 16, 16], [4, 4, 4], 3)
     if name == "c16_tc1":
         return _shape_case(1, 5, 16, 1, [32], [32], 4)
+    if name == "c24_tc600_bins255":  # chunks longer than 256 tokens (600, 600, then a ragged 100)
+        return _shape_case(2, 1300, 24, 600, [255, 16], [32, 8], 5)
     raise KeyError(name)
 
 
@@ -115,7 +117,8 @@ def test_compress_decompress_parity(cg, oracle_mod, synth_mod, case):
     assert_close_f32(ov.cpu().numpy(), rv)
 
 
-@pytest.mark.parametrize("case", ["tiny", "ragged", "c48_tc32_bins256", "c24_tc70", "mistral_chunk"])
+@pytest.mark.parametrize("case", ["tiny", "ragged", "c48_tc32_bins256", "c24_tc70", "mistral_chunk",
+                                  "c24_tc600_bins255"])
 def test_step_functions_parity(cg, oracle_mod, synth_mod, case):
     k, v, Tc, bk, bv = make_case(case, synth_mod)
     L, T, C_ = k.shape

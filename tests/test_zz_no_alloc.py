@@ -55,16 +55,22 @@ def test_noalloc_matches_workspace_entry_point_twice():
     lib = capi.load()
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
 
-    # two different shapes in a row: the second call runs on whatever the first
-    # left in the shared static scratch
-    for name in ("mistral_chunk", "tiny"):
-        w = synth.WORKLOADS[name]
-        k_h, v_h = synth.generate(w)
+    # three different shapes in a row: each call runs on whatever the one before
+    # left in the shared static scratch. The last has 13 channels, so the library
+    # takes its multi-kernel path (quantise, count-and-code, scan and pack), which
+    # carves the symbol tensor and the scan partials out of the same scratch.
+    rng = np.random.default_rng(3)
+    odd = (rng.standard_normal((3, 300, 13)) * rng.lognormal(0, 0.5, (1, 1, 13))).astype(np.float16)
+    cases = [(*synth.generate(synth.WORKLOADS[n]), synth.WORKLOADS[n]) for n in ("mistral_chunk", "tiny")]
+    cases.append((odd, -odd[:, ::-1].copy(), None))
+    for k_h, v_h, w in cases:
         k = torch.from_numpy(k_h).cuda()
         v = torch.from_numpy(v_h).cuda()
-        shp = capi.cg_shape(w.L, w.T, w.C, w.chunk_tokens, w.T * w.C)
-        bk, pk = _bins(w.bins_k)
-        bv, pv = _bins(w.bins_v)
+        L, T, C_ = k_h.shape
+        Tc = w.chunk_tokens if w is not None else 128
+        shp = capi.cg_shape(L, T, C_, Tc, T * C_)
+        bk, pk = _bins(w.bins_k if w is not None else [32, 16, 8])
+        bv, pv = _bins(w.bins_v if w is not None else [16, 16, 32])
         cap = int(lib.cg_max_compressed_bytes(C.byref(shp)))
         need = int(lib.cg_compress_workspace_bytes(C.byref(shp)))
         assert 0 < need <= capi.CG_NOALLOC_WORKSPACE_BYTES
