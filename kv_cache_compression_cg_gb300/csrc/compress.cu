@@ -244,6 +244,113 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
     }
 }
 
+// Step 3 for one window: CDF thread ct (channel ct >> 2, part ct & 3) turns
+// the counts of its eight symbols into (lo, f) entries of the channel's row,
+// clearing the counters it read, and writes the side output (CDF entries, or
+// the format 2 count record).
+template <bool V2>
+__device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const uint16_t *ftab, uint2 *cdfw,
+                                                 void *side_out, long long side_base, int c0, int Wc, int A) {
+    const int c = ct >> 2, p = ct & 3;
+    // a warp covers eight channels and Wc is a multiple of 8, so a warp
+    // is entirely inside or entirely outside the window
+    if (c >= Wc) return;
+    uint32_t fj[kSP], pre[kSP];
+    uint32_t sum = 0, key = 0, nlo = 0, nhi = 0;  // counts, one byte each (capped)
+#pragma unroll
+    for (int j = 0; j < kSP; j++) {
+        const int s = kSP * p + j;
+        uint32_t fv = 0;
+        if (s < A) {
+            uint16_t *cp = cnt16 + s * kCntRow + c;
+            const uint32_t n = *cp;
+            *cp = 0;
+            fv = ftab[n];
+            key = max(key, (n << 8) | (255u - (uint32_t)s));  // largest n, then smallest s
+            if (V2) {
+                if (j < 4)
+                    nlo |= min(n, 255u) << (8 * j);
+                else
+                    nhi |= min(n, 255u) << (8 * (j - 4));
+            }
+        }
+        pre[j] = sum;
+        sum += fv;
+        fj[j] = fv;
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o, 4);
+        if (p >= o) incl += v;
+        key = max(key, __shfl_xor_sync(0xFFFFFFFFu, key, o));
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
+    const uint32_t base = incl - sum;
+    const uint32_t best = 255u - (key & 255u);
+    const uint32_t extra = kTotal - total;
+    uint2 *row = cdfw + c * kAS;
+    if (V2) {
+        // count record: the mode, then the other symbols' counts
+        uint8_t *g = static_cast<uint8_t *>(side_out) + side_base + (long long)(c0 + c) * A;
+        if (p == 0) g[0] = (uint8_t)best;
+#pragma unroll
+        for (int j = 0; j < kSP; j++) {
+            const uint32_t s = (uint32_t)(kSP * p + j);
+            if ((int)s < A) {
+                const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
+                const uint32_t f = fj[j] + (s == best ? extra : 0u);
+                row[s] = make_uint2(lo, f);
+                if (s != best) g[s + (s < best ? 1u : 0u)] = (uint8_t)((j < 4 ? nlo >> (8 * j) : nhi >> (8 * (j - 4))) & 0xFFu);
+            }
+        }
+    } else {
+        uint16_t *g = static_cast<uint16_t *>(side_out) + side_base + (long long)(c0 + c) * A;
+#pragma unroll
+        for (int j = 0; j < kSP; j++) {
+            const uint32_t s = (uint32_t)(kSP * p + j);
+            if ((int)s < A) {
+                const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
+                const uint32_t f = fj[j] + (s == best ? extra : 0u);
+                row[s] = make_uint2(lo, f);
+                g[s] = (uint16_t)lo;
+            }
+        }
+    }
+}
+
+// Step 4 for one window: code this thread's row of the symbol tile (bytes 8q)
+// with the window's (lo, f) rows.
+__device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uint8_t *symrow, const uint2 *cdfw,
+                                              int Wc) {
+    const uint32_t *my = reinterpret_cast<const uint32_t *>(symrow);
+    const unsigned char *rows = reinterpret_cast<const unsigned char *>(cdfw);
+    if (Wc == kW) {
+#pragma unroll
+        for (int g = 0; g < kW / 4; g++) {
+            // every byte is 8q; the mask keeps any tile content 8-byte aligned
+            const uint32_t w4 = my[g] & 0xF8F8F8F8u;
+            const unsigned char *r0 = rows + (4 * g) * kAS * 8;
+            const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + (w4 & 0xFFu));
+            const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + ((w4 >> 8) & 0xFFu));
+            const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + ((w4 >> 16) & 0xFFu));
+            const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + (w4 >> 24));
+            if (e.nbits >= 32) enc_flush_word(e, stream);
+            enc_symbol_lf(e, e0.x, e0.y);
+            enc_symbol_lf(e, e1.x, e1.y);
+            if (e.nbits >= 32) enc_flush_word(e, stream);
+            enc_symbol_lf(e, e2.x, e2.y);
+            enc_symbol_lf(e, e3.x, e3.y);
+        }
+    } else {
+        for (int c = 0; c < Wc; c++) {
+            const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + (symrow[c] & 0xF8u));
+            if (e.nbits >= 32) enc_flush_word(e, stream);
+            enc_symbol_lf(e, en.x, en.y);
+        }
+    }
+}
+
 // The reference max1 of row r with anchor row ra: the anchor's, or 0 for an
 // anchor itself.
 __device__ __forceinline__ float anchor_m1(const uint16_t *m1, int ra, int r) {
@@ -481,106 +588,10 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         __syncthreads();
         if (tid == 0 && w + 1 < nwin) tma_load(buf0, tm, c0 + kW, t0, l, bar0, box_bytes);
         // 3. CDF rows: thread (channel c, part p) owns symbols 8p .. 8p + 7
-        {
-            const int c = tid >> 2, p = tid & 3;
-            // a warp covers eight channels and Wc is a multiple of 8, so a warp
-            // is entirely inside or entirely outside the window
-            if (c < Wc) {
-                uint32_t fj[kSP], pre[kSP];
-                uint32_t sum = 0, key = 0, nlo = 0, nhi = 0;  // counts, one byte each (capped)
-#pragma unroll
-                for (int j = 0; j < kSP; j++) {
-                    const int s = kSP * p + j;
-                    uint32_t fv = 0;
-                    if (s < A) {
-                        uint16_t *cp = cnt16 + s * kCntRow + c;
-                        const uint32_t n = *cp;
-                        *cp = 0;
-                        fv = s_ftab[n];
-                        key = max(key, (n << 8) | (255u - (uint32_t)s));  // largest n, then smallest s
-                        if (V2) {
-                            if (j < 4)
-                                nlo |= min(n, 255u) << (8 * j);
-                            else
-                                nhi |= min(n, 255u) << (8 * (j - 4));
-                        }
-                    }
-                    pre[j] = sum;
-                    sum += fv;
-                    fj[j] = fv;
-                }
-                uint32_t incl = sum;
-#pragma unroll
-                for (int o = 1; o < 4; o <<= 1) {
-                    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o, 4);
-                    if (p >= o) incl += v;
-                    key = max(key, __shfl_xor_sync(0xFFFFFFFFu, key, o));
-                }
-                const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
-                const uint32_t base = incl - sum;
-                const uint32_t best = 255u - (key & 255u);
-                const uint32_t extra = kTotal - total;
-                uint2 *row = cdfw + c * kAS;
-                if (V2) {
-                    // count record: the mode, then the other symbols' counts
-                    uint8_t *g = static_cast<uint8_t *>(side_out) + side_base + (long long)(c0 + c) * A;
-                    if (p == 0) g[0] = (uint8_t)best;
-#pragma unroll
-                    for (int j = 0; j < kSP; j++) {
-                        const uint32_t s = (uint32_t)(kSP * p + j);
-                        if ((int)s < A) {
-                            const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
-                            const uint32_t f = fj[j] + (s == best ? extra : 0u);
-                            row[s] = make_uint2(lo, f);
-                            if (s != best) g[s + (s < best ? 1u : 0u)] = (uint8_t)((j < 4 ? nlo >> (8 * j) : nhi >> (8 * (j - 4))) & 0xFFu);
-                        }
-                    }
-                } else {
-                    uint16_t *g = static_cast<uint16_t *>(side_out) + side_base + (long long)(c0 + c) * A;
-#pragma unroll
-                    for (int j = 0; j < kSP; j++) {
-                        const uint32_t s = (uint32_t)(kSP * p + j);
-                        if ((int)s < A) {
-                            const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
-                            const uint32_t f = fj[j] + (s == best ? extra : 0u);
-                            row[s] = make_uint2(lo, f);
-                            g[s] = (uint16_t)lo;
-                        }
-                    }
-                }
-            }
-        }
+        build_cdf_window<V2>(tid, cnt16, s_ftab, cdfw, side_out, side_base, c0, Wc, A);
         __syncthreads();
         // 4. code my token's symbols of this window
-        if (tid < Tk) {
-            const uint32_t *my = reinterpret_cast<const uint32_t *>(sym + tid * kSymRow);
-            const unsigned char *rows = reinterpret_cast<const unsigned char *>(cdfw);
-            if (Wc == kW) {
-#pragma unroll
-                for (int g = 0; g < kW / 4; g++) {
-                    // every byte is 8q; the mask keeps any tile content 8-byte aligned
-                    const uint32_t w4 = my[g] & 0xF8F8F8F8u;
-                    const unsigned char *r0 = rows + (4 * g) * kAS * 8;
-                    const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + (w4 & 0xFFu));
-                    const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + ((w4 >> 8) & 0xFFu));
-                    const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + ((w4 >> 16) & 0xFFu));
-                    const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + (w4 >> 24));
-                    if (e.nbits >= 32) enc_flush_word(e, stream);
-                    enc_symbol_lf(e, e0.x, e0.y);
-                    enc_symbol_lf(e, e1.x, e1.y);
-                    if (e.nbits >= 32) enc_flush_word(e, stream);
-                    enc_symbol_lf(e, e2.x, e2.y);
-                    enc_symbol_lf(e, e3.x, e3.y);
-                }
-            } else {
-                const uint8_t *mb = sym + tid * kSymRow;
-                for (int c = 0; c < Wc; c++) {
-                    const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + (mb[c] & 0xF8u));
-                    if (e.nbits >= 32) enc_flush_word(e, stream);
-                    enc_symbol_lf(e, en.x, en.y);
-                }
-            }
-        }
+        if (tid < Tk) encode_window(e, stream, sym + tid * kSymRow, cdfw, Wc);
     }
 
     // 5. stream lengths and the slice's total (offsets and packing follow in
@@ -600,6 +611,205 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     }
     if (status && (nonfinite || timed_out) && (tid == 0 || timed_out))
         atomicOr(status, (nonfinite ? CG_FLAG_NONFINITE : 0) | (timed_out ? CG_FLAG_TIMEOUT : 0));
+}
+
+// Latency mode: launches of at most one slice per SM (a single chunk, say),
+// where each slice's CTA has an SM to itself and the coders' time is set by the
+// serial chain of each token stream, not by instruction issue. A CTA of 512
+// threads splits the work by warp: warps 0-7 only code (thread t codes token t),
+// warps 8-15 quantise and count window i + 1 and turn its counts into CDF rows
+// while the coders code window i, so the coders never wait on those steps. The
+// symbol tile and the CDF rows are double-buffered; one 512-thread named
+// barrier per window hands a window over (producers have finished window i,
+// coders have finished window i - 1). The max1 pass uses all 16 warps; the
+// fp16 boxes come by TMA into two buffers, window i + 2's box loading while
+// window i + 1 is quantised.
+constexpr int kLmThreads = 512;
+
+// Dynamic shared memory of the latency-mode kernel, in bytes from the
+// 128-byte aligned base: two fp16 boxes, two (lo, f) row sets, the counters,
+// two symbol tiles.
+struct LmSmem {
+    static constexpr int cdfw = 0;
+    static constexpr int cnt = cdfw + 2 * kCdfwBytes;
+    static constexpr int sym = cnt + kCntBytes;
+    static constexpr int box = (sym + 2 * kSymBytes + 127) & ~127;
+    static int bytes(int box_bytes) { return 128 + box + 2 * box_bytes; }
+};
+
+template <bool V2>
+__global__ void __launch_bounds__(kLmThreads, 1) k_compress_lm(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, Dims d, MaxTab mt,
+    int box_rows, uint16_t *__restrict__ max1_out, void *__restrict__ side_out, uint8_t *__restrict__ stage,
+    uint32_t *__restrict__ len, unsigned long long *state, int32_t *status) {
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ unsigned long long s_bar[2];
+    __shared__ unsigned long long s_scan[kNW];
+    __shared__ float s_fac[kNT];
+    __shared__ uint16_t s_m1[kNT];
+    __shared__ uint16_t s_ftab[kNT + 2];
+
+    const uint32_t dyn = smem_u32(dsm);
+    const uint32_t base = (dyn + 127u) & ~127u;
+    unsigned char *sm = dsm + (base - dyn);
+    uint2 *cdfw2 = reinterpret_cast<uint2 *>(sm + LmSmem::cdfw);
+    uint16_t *cnt16 = reinterpret_cast<uint16_t *>(sm + LmSmem::cnt);
+    uint32_t *cnt32 = reinterpret_cast<uint32_t *>(sm + LmSmem::cnt);
+    uint8_t *sym2 = sm + LmSmem::sym;
+    const uint32_t buf0 = base + LmSmem::box, buf1 = buf0 + (uint32_t)box_rows * (kW * 2);
+    const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int slice = blockIdx.x;
+    int k, kv, l;
+    slice_coords(d, slice, k, kv, l);
+    const int Tk = chunk_tokens(d, k);
+    const int MAX = mt.v[kv][l];
+    const int A = V2 ? 2 * MAX + 1 : d.A[kv];
+    const CUtensorMap *tm = kv ? &tmv : &tmk;
+    const int t0 = k * d.Tc;
+    const int nwin = (d.C + kW - 1) / kW;
+    const uint32_t box_bytes = (uint32_t)box_rows * (kW * 2);
+    const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
+    const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk;
+    bool timed_out = false;
+    if (tid == 0) {
+        mbar_init(bar0);
+        mbar_init(bar1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // the max1 pass reads window m from buffer m & 1; the coding pass reads
+        // window i from buffer (nwin + i) & 1 (with one window, buffer 1 holds it)
+        tma_load(buf0, tm, 0, t0, l, bar0, box_bytes);
+        tma_load(buf1, tm, nwin > 1 ? kW : 0, t0, l, bar1, box_bytes);
+    }
+    __syncthreads();
+
+    // 1. max1 pass, all 16 warps: lane (quad kq) of warp w keeps rows 16 w + (lane >> 4) + 2 i
+    const int kq = lane & 15;
+    uint32_t ph0 = 0u, ph1 = 0u;
+    {
+        const int rb = 16 * warp + (lane >> 4);
+        uint32_t mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) mx[i] = 0;
+        for (int m = 0; m < nwin; m++) {
+            const bool b = (m & 1) != 0;
+            if (!mbar_wait(b ? bar1 : bar0, b ? ph1 : ph0)) timed_out = true;
+            if (b)
+                ph1 ^= 1u;
+            else
+                ph0 ^= 1u;
+            const unsigned char *box = sm + ((b ? buf1 : buf0) - base);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int r = rb + 2 * i;
+                if (r < Tk) {
+                    const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
+                    mx[i] = __vmaxu2(mx[i], x.x & 0x7FFF7FFFu);
+                    mx[i] = __vmaxu2(mx[i], x.y & 0x7FFF7FFFu);
+                }
+            }
+            __syncthreads();  // the buffer is free again
+            if (tid == 0) {
+                const int j = m + 2 < nwin ? m + 2 : m + 2 - nwin;  // the coding pass starts over at 0 and 1
+                if (m + 2 < nwin || (j < 2 && j < nwin))
+                    tma_load(b ? buf1 : buf0, tm, j * kW, t0, l, b ? bar1 : bar0, box_bytes);
+            }
+        }
+        uint32_t mine = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            uint32_t v = max(mx[i] & 0xFFFFu, mx[i] >> 16);
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+            v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 8));
+            if (kq == i) mine = v;
+        }
+        bool nonfinite = false;
+        const int r = rb + 2 * kq;
+        if (kq < 8 && r < Tk) {
+            s_m1[r] = (uint16_t)mine;
+            max1_out[group_index(d, kv, l, t0 + r)] = (uint16_t)mine;
+            nonfinite = mine >= 0x7C00u;
+        }
+        for (int n = tid; n <= Tk; n += kLmThreads)
+            s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kTotal - (uint32_t)A)) / (uint32_t)Tk);
+        for (int i = tid; i < kCntBytes / 4; i += kLmThreads) cnt32[i] = 0;
+        nonfinite = __syncthreads_or(nonfinite) != 0;
+        if (tid < Tk) {
+            const unsigned mb = s_m1[tid];
+            s_fac[tid] = mb ? __fdiv_rn((float)MAX, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
+        }
+        timed_out = __syncthreads_or(timed_out) != 0;
+        if (tid == 0 && status && (nonfinite || timed_out))
+            atomicOr(status, (nonfinite ? CG_FLAG_NONFINITE : 0) | (timed_out ? CG_FLAG_TIMEOUT : 0));
+        timed_out = timed_out || nonfinite;  // either takes the clamping quantiser
+    }
+    const bool safe = timed_out;
+
+    if (warp >= kNW) {
+        // producers: window i's symbols, counts and CDF rows into buffers i & 1
+        const int pt = tid - kNT;
+        const int pw = warp - kNW;
+        const int rbase = 32 * pw + (lane >> 4);
+        const unsigned long long fm = pair((float)MAX, (float)MAX);
+        const unsigned long long mg = pair(12582912.0f, 12582912.0f);
+        const uint32_t qmax = 2u * (uint32_t)MAX;
+        const uint32_t cnt_lane = smem_u32(cnt32) + 8u * (uint32_t)kq - (uint32_t)(kCntRow * 2) * kMagic;
+        bool late = false;
+        for (int i = 0; i < nwin; i++) {
+            const int c0 = i * kW;
+            const int Wc = min(kW, d.C - c0);
+            const bool b = ((nwin + i) & 1) != 0;  // box buffer of window i in the coding pass
+            if (!mbar_wait(b ? bar1 : bar0, b ? ph1 : ph0)) late = true;
+            if (b)
+                ph1 ^= 1u;
+            else
+                ph0 ^= 1u;
+            uint8_t *sym = sym2 + (i & 1) * kSymBytes;
+            const unsigned char *box = sm + ((b ? buf1 : buf0) - base);
+            if (4 * kq < Wc) {
+                if (safe || late)
+                    quantise_window<true>(box, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                else
+                    quantise_window<false>(box, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kNT) : "memory");  // counts in, box read
+            if (pt == 0 && i + 2 < nwin) tma_load(b ? buf1 : buf0, tm, (i + 2) * kW, t0, l, b ? bar1 : bar0, box_bytes);
+            build_cdf_window<V2>(pt, cnt16, s_ftab, cdfw2 + (i & 1) * (kCdfwBytes / 8), side_out, side_base, c0,
+                                 Wc, A);
+            asm volatile("bar.sync 2, %0;" ::"n"(kLmThreads) : "memory");  // window i handed over
+        }
+        if (late && lane == 0 && status) atomicOr(status, CG_FLAG_TIMEOUT);
+    } else {
+        // coders: window i from buffers i & 1
+        Enc e;
+        enc_init(e);
+        uint8_t *stream = stage_stream(stage, sid0 + (tid < Tk ? tid : 0), d);
+        asm volatile("bar.sync 2, %0;" ::"n"(kLmThreads) : "memory");  // window 0 is ready
+        for (int i = 0; i < nwin; i++) {
+            const int Wc = min(kW, d.C - i * kW);
+            if (tid < Tk)
+                encode_window(e, stream, sym2 + (i & 1) * kSymBytes + tid * kSymRow,
+                              cdfw2 + (i & 1) * (kCdfwBytes / 8), Wc);
+            if (i + 1 < nwin) asm volatile("bar.sync 2, %0;" ::"n"(kLmThreads) : "memory");
+        }
+        const uint32_t mylen = tid < Tk ? enc_finish(e, stream) : 0u;
+        if (tid < Tk) len[sid0 + tid] = mylen;
+        uint32_t tot = mylen;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+        if (lane == 0) s_scan[warp] = tot;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long run = 0;
+#pragma unroll
+        for (int w = 0; w < kNW; w++) run += s_scan[w];
+        state[2 + 2LL * d.L * d.nch + slice] = run;
+    }
 }
 
 // Offsets and packing: CTA per slice in stream order (by ticket). Every
@@ -763,6 +973,19 @@ bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v)
     return d.T > 0 && tmax <= kNT && A <= kAmax && d.C % 8 == 0 && aligned;
 }
 
+// SMs of the current device, looked up once per device.
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d, const MaxTab &mt,
                                   uint16_t *max1, uint16_t *cdf, uint8_t *rec, uint8_t *stage, uint32_t *len,
                                   uint64_t *off, uint8_t *packed, uint64_t capacity,
@@ -770,19 +993,32 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
     const int box_rows = d.Tc < d.T ? d.Tc : d.T;
     CUtensorMap tmk, tmv;
     if (!make_map(&tmk, k, d, box_rows) || !make_map(&tmv, v, d, box_rows)) return cudaErrorNotSupported;
-    const int dyn = 128 + box_rows * kW * 2;
     const bool v2 = cdf == nullptr;
-    auto kern = d.G > 1 ? (v2 ? k_compress_tma<true, true> : k_compress_tma<false, true>)
-                        : (v2 ? k_compress_tma<true, false> : k_compress_tma<false, false>);
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    if (err != cudaSuccess) return err;
+    void *side = v2 ? static_cast<void *>(rec) : static_cast<void *>(cdf);
     const long long nslices = 2LL * d.L * d.nch;
     k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
-    kern<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, k, v, d, mt, box_rows, max1,
-                                              v2 ? static_cast<void *>(rec) : static_cast<void *>(cdf), stage, len,
-                                              state, status);
+    cudaError_t err;
+    const int sms = sm_count();
+    if (d.G == 1 && sms > 0 && nslices <= sms) {
+        // latency mode: one CTA of coders and producers per slice, one slice per SM
+        const int dyn = LmSmem::bytes(box_rows * kW * 2);
+        auto kern = v2 ? k_compress_lm<true> : k_compress_lm<false>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+        if (err != cudaSuccess) return err;
+        kern<<<(unsigned)nslices, kLmThreads, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, side, stage, len, state,
+                                                        status);
+    } else {
+        const int dyn = 128 + box_rows * kW * 2;
+        auto kern = d.G > 1 ? (v2 ? k_compress_tma<true, true> : k_compress_tma<false, true>)
+                            : (v2 ? k_compress_tma<true, false> : k_compress_tma<false, false>);
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared);
+        if (err != cudaSuccess) return err;
+        kern<<<(unsigned)nslices, kNT, dyn, s>>>(tmk, tmv, k, v, d, mt, box_rows, max1, side, stage, len, state,
+                                                  status);
+    }
     k_pack<<<(unsigned)nslices, kNT, 0, s>>>(d, stage, len, off, packed, capacity, state, status);
     return cudaGetLastError();
 }
