@@ -23,6 +23,19 @@ struct TraceRange {
 };
 #define CG_TRACE_RANGE() ::cg::TraceRange cg_trace_range_(__func__)
 
+// SMs of the current device, looked up once per device (per translation unit).
+inline int device_sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 // Per-call geometry, passed by value to every kernel.
 struct Dims {
     int L, T, C, Tc;       // layers, tokens, channels, tokens per chunk

@@ -931,6 +931,91 @@ __global__ void __launch_bounds__(kNT) k_pack(Dims d, const uint8_t *__restrict_
     if (timed_out && status && lane == 0) atomicOr(status, CG_FLAG_TIMEOUT);
 }
 
+// Packing after the latency-mode kernel (at most one slice per SM): four
+// CTAs per slice, each placing a quarter of its streams. A slice's offset is
+// the sum of the byte totals of the slices before it, read directly (at most
+// one slice per SM precedes it): no look-back and no wait on another CTA.
+constexpr int kPackParts = 4;
+
+__global__ void __launch_bounds__(kNT, 4) k_pack_lm(Dims d, const uint8_t *__restrict__ stage,
+                                                 const uint32_t *__restrict__ len, uint64_t *__restrict__ off,
+                                                 uint8_t *__restrict__ packed, unsigned long long capacity,
+                                                 const unsigned long long *__restrict__ totals, int32_t *status) {
+    __shared__ unsigned long long s_red[kNW];
+    __shared__ uint32_t s_len[kNT], s_loc[kNT], s_wtot[kNW];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int slice = blockIdx.x / kPackParts, part = blockIdx.x % kPackParts;
+    const long long nslices = 2LL * d.L * d.nch;
+    int k, kv, l;
+    slice_coords(d, slice, k, kv, l);
+    const int Tk = chunk_tokens(d, k);
+    const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk;
+    // the slice's offset and the places of its streams
+    unsigned long long b = 0;
+    for (int j = tid; j < slice; j += kNT) b += totals[j];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+    const uint32_t mylen = tid < Tk ? len[sid0 + tid] : 0u;
+    uint32_t incl = mylen;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 0) s_red[warp] = b;
+    if (lane == 31) s_wtot[warp] = incl;
+    s_len[tid] = mylen;
+    __syncthreads();
+    unsigned long long sbase = 0;
+    uint32_t wbase = 0;
+#pragma unroll
+    for (int w = 0; w < kNW; w++) {
+        sbase += s_red[w];
+        wbase += w < warp ? s_wtot[w] : 0u;
+    }
+    s_loc[tid] = wbase + incl - mylen;
+    __syncthreads();
+    const int q0 = (int)((long long)Tk * part / kPackParts), q1 = (int)((long long)Tk * (part + 1) / kPackParts);
+    if (tid >= q0 && tid < q1) off[sid0 + tid] = sbase + s_loc[tid];
+    if (slice == nslices - 1 && part == kPackParts - 1 && tid == 0) {
+        unsigned long long run = 0;
+#pragma unroll
+        for (int w = 0; w < kNW; w++) run += s_wtot[w];
+        off[d.nstreams] = sbase + run;
+        if (sbase + run > capacity && status) atomicOr(status, CG_FLAG_CAPACITY);
+    }
+    // warps take this part's streams in turn, lane i word i; all first words in flight at once
+    constexpr int kBatch = 8;
+    for (int t0 = q0; t0 < q1; t0 += kNW * kBatch) {
+        uint32_t held[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; u++) {
+            const int t = t0 + warp + kNW * u;
+            held[u] = 0;
+            if (t < q1 && 4u * lane < s_len[t])
+                held[u] = *reinterpret_cast<const uint32_t *>(stage_stream(const_cast<uint8_t *>(stage), sid0 + t, d) +
+                                                              4 * lane);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; u++) {
+            const int t = t0 + warp + kNW * u;
+            if (t >= q1) continue;
+            const uint32_t n = s_len[t];
+            const unsigned long long dst = sbase + s_loc[t];
+            const uint8_t *src = stage_stream(const_cast<uint8_t *>(stage), sid0 + t, d);
+            for (uint32_t bb = 4u * lane; bb < n; bb += 128u) {
+                const uint32_t wv = bb < 128u ? held[u] : *reinterpret_cast<const uint32_t *>(src + bb);
+                const uint32_t nb = min(4u, n - bb);
+#pragma unroll
+                for (uint32_t q = 0; q < 4; q++) {
+                    const unsigned long long pos = dst + bb + q;
+                    if (q < nb && pos < capacity) packed[pos] = (uint8_t)(wv >> (8 * q));
+                }
+            }
+        }
+    }
+}
+
 // cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -973,19 +1058,6 @@ bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v)
     return d.T > 0 && tmax <= kNT && A <= kAmax && d.C % 8 == 0 && aligned;
 }
 
-// SMs of the current device, looked up once per device.
-int sm_count() {
-    static int counts[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
-}
-
 cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d, const MaxTab &mt,
                                   uint16_t *max1, uint16_t *cdf, uint8_t *rec, uint8_t *stage, uint32_t *len,
                                   uint64_t *off, uint8_t *packed, uint64_t capacity,
@@ -996,18 +1068,24 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
     const bool v2 = cdf == nullptr;
     void *side = v2 ? static_cast<void *>(rec) : static_cast<void *>(cdf);
     const long long nslices = 2LL * d.L * d.nch;
-    k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
     cudaError_t err;
-    const int sms = sm_count();
+    const int sms = device_sm_count();
     if (d.G == 1 && sms > 0 && nslices <= sms) {
-        // latency mode: one CTA of coders and producers per slice, one slice per SM
+        // latency mode: one CTA of coders and producers per slice, one slice per
+        // SM; the slice totals go to state[2 + nslices ..], which the packing
+        // reads directly (no tickets, no look-back)
         const int dyn = LmSmem::bytes(box_rows * kW * 2);
         auto kern = v2 ? k_compress_lm<true> : k_compress_lm<false>;
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
         if (err != cudaSuccess) return err;
         kern<<<(unsigned)nslices, kLmThreads, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, side, stage, len, state,
                                                         status);
-    } else {
+        k_pack_lm<<<(unsigned)(kPackParts * nslices), kNT, 0, s>>>(d, stage, len, off, packed, capacity,
+                                                                   state + 2 + nslices, status);
+        return cudaGetLastError();
+    }
+    k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
+    {
         const int dyn = 128 + box_rows * kW * 2;
         auto kern = d.G > 1 ? (v2 ? k_compress_tma<true, true> : k_compress_tma<false, true>)
                             : (v2 ? k_compress_tma<true, false> : k_compress_tma<false, false>);
