@@ -144,6 +144,26 @@ __device__ __forceinline__ void search_from(uint32_t &addr, uint32_t r, uint32_t
     if constexpr (STEP > 1) search_from<STEP / 2>(addr, r, code);
 }
 
+// The same search over SPAN entries four ways per level: the entries at
+// SPAN / 4, SPAN / 2 and 3 SPAN / 4 are loaded and compared at once, which
+// halves the dependent loads of the search (a shorter chain per symbol, for
+// more instructions: the decoder of launches whose time is set by that chain).
+template <int SPAN>
+__device__ __forceinline__ void search4(uint32_t &addr, uint32_t r, uint32_t code) {
+    if constexpr (SPAN >= 4) {
+        constexpr int Q = SPAN / 4;
+        uint32_t c1, c2, c3;
+        asm("ld.shared.u16 %0, [%1 + %2];" : "=r"(c1) : "r"(addr), "n"(2 * Q));
+        asm("ld.shared.u16 %0, [%1 + %2];" : "=r"(c2) : "r"(addr), "n"(4 * Q));
+        asm("ld.shared.u16 %0, [%1 + %2];" : "=r"(c3) : "r"(addr), "n"(6 * Q));
+        const uint32_t n = (r * c1 <= code ? 1u : 0u) + (r * c2 <= code ? 1u : 0u) + (r * c3 <= code ? 1u : 0u);
+        addr += 2u * Q * n;
+        search4<Q>(addr, r, code);
+    } else if constexpr (SPAN == 2) {
+        search_step<1>(addr, r, code);
+    }
+}
+
 // One symbol from the row of its channel: `cum` is the shared address of the
 // uint16 cumulative row, its frequencies sit frq_off bytes further; needs
 // nb >= 16. Searches the first PS entries of the row (PS >= A). Returns the
@@ -153,11 +173,14 @@ __device__ __forceinline__ void search_from(uint32_t &addr, uint32_t r, uint32_t
 // stream whose code reaches r * 65535 and a corrupt stream the decoder rule's
 // answer (largest s < A with r*cum[s] <= code). With A == P no entry is
 // padding and the search cannot pass A - 1.
-template <int PS, bool CLAMP>
+template <int PS, bool CLAMP, bool WIDE = false>
 __device__ __forceinline__ uint32_t decode_symbol(Stream &s, uint32_t cum, uint32_t frq_off, uint32_t amax2) {
     const uint32_t r = s.range >> 16;
     uint32_t addr = cum;
-    search_from<PS / 2>(addr, r, s.code);
+    if (WIDE)
+        search4<PS>(addr, r, s.code);
+    else
+        search_from<PS / 2>(addr, r, s.code);
     if (CLAMP) addr = min(addr, cum + amax2);
     uint32_t lo, f;
     asm("ld.shared.u16 %0, [%1];" : "=r"(lo) : "r"(addr));
@@ -486,7 +509,7 @@ __device__ __forceinline__ void write_window_delta(const uint8_t *tile, const fl
 
 // Decode this thread's Wc symbols of one window into its tile row: rows are P
 // entries apart, the search covers the first PS (the alphabet fits in PS).
-template <int P, int PS, bool CLAMP, bool TAIL>
+template <int P, int PS, bool CLAMP, bool TAIL, bool WIDE = false>
 __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t fo, uint32_t amax2, uint8_t *my,
                                               int Wc) {
     constexpr int W = DecodeCfg<P>::W;
@@ -496,11 +519,11 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
         for (int c = 0; c < W; c += 4) {
             const uint32_t rc = cb + 2 * P * c;
             refill<TAIL>(s);
-            const uint32_t e0 = decode_symbol<PS, CLAMP>(s, rc, fo, amax2);
-            const uint32_t e1 = decode_symbol<PS, CLAMP>(s, rc + 2 * P, fo, amax2);
+            const uint32_t e0 = decode_symbol<PS, CLAMP, WIDE>(s, rc, fo, amax2);
+            const uint32_t e1 = decode_symbol<PS, CLAMP, WIDE>(s, rc + 2 * P, fo, amax2);
             refill<TAIL>(s);
-            const uint32_t e2 = decode_symbol<PS, CLAMP>(s, rc + 4 * P, fo, amax2);
-            const uint32_t e3 = decode_symbol<PS, CLAMP>(s, rc + 6 * P, fo, amax2);
+            const uint32_t e2 = decode_symbol<PS, CLAMP, WIDE>(s, rc + 4 * P, fo, amax2);
+            const uint32_t e3 = decode_symbol<PS, CLAMP, WIDE>(s, rc + 6 * P, fo, amax2);
             // e = 2s: store 4s (SH == 2) or s
             const uint32_t w = SH == 2 ? 2u * (e0 | (e1 << 8) | (e2 << 16) | (e3 << 24))
                                        : (e0 >> 1) | ((e1 >> 1) << 8) | ((e2 >> 1) << 16) | ((e3 >> 1) << 24);
@@ -510,7 +533,7 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
 #pragma unroll 1
         for (int c = 0; c < Wc; c++) {
             refill<TAIL>(s);
-            const uint32_t e = decode_symbol<PS, CLAMP>(s, cb + 2 * P * c, fo, amax2);
+            const uint32_t e = decode_symbol<PS, CLAMP, WIDE>(s, cb + 2 * P * c, fo, amax2);
             my[c] = (uint8_t)(SH == 2 ? 2u * e : e >> 1);
         }
     }
@@ -701,11 +724,178 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
     if (bad_rec && status) atomicOr(status, CG_FLAG_CORRUPT);
 }
 
+// Latency mode: launches of at most one slice per SM, where a slice's time is
+// set by the serial chain of each token stream. A CTA of 512 threads splits the
+// work by warp: warps 0-7 only decode (thread t decodes token t, searching four
+// ways per level: fewer dependent loads per symbol), warps 8-15 build window
+// i + 1's CDF rows and write window i - 1's dequantised rows out while window i
+// is decoded, from double-buffered rows and symbol tiles; one 512-thread named
+// barrier per window hands them over.
+constexpr int kLmDecThreads = 512;
+
+template <int P>
+struct LmDecSmem {
+    static constexpr int W = DecodeCfg<P>::W;
+    static constexpr int TS = DecodeCfg<P>::TS;
+    static constexpr size_t cum = 0;                                        // [2][W][P] uint16
+    static constexpr size_t frq = cum + 2ull * W * P * 2;                   // [2][W][P] uint16
+    static constexpr size_t tile = (frq + 2ull * W * P * 2 + 15) & ~15ull;  // [2][kThreads * TS]
+    static constexpr size_t m1 = tile + 2ull * kThreads * TS;               // float[kThreads]
+    static constexpr size_t recs = m1 + kThreads * 4;                       // format 2: [W * P] records
+    static constexpr size_t bytes = recs + 1ull * W * P;
+};
+
+template <int P, int MODE, bool V2, bool DELTA>
+__global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
+    const uint8_t *__restrict__ packed, long long packed_bytes, const uint64_t *__restrict__ off,
+    const uint32_t *__restrict__ len, const uint16_t *__restrict__ cdf, const uint8_t *__restrict__ rec,
+    const uint16_t *__restrict__ max1, Dims d, MaxTab mt, void *__restrict__ out_k, void *__restrict__ out_v,
+    long long ols, int32_t *status) {
+    using L = LmDecSmem<P>;
+    constexpr int W = L::W;
+    constexpr int TS = L::TS;
+    __shared__ __align__(256) float s_unit[256];  // (s - MAX) / MAX
+    __shared__ uint16_t s_ftab[kThreads + 2];
+    __shared__ float s_m1a[DELTA ? kThreads : 1];
+    __shared__ uint8_t s_anchor[DELTA ? kThreads : 1];
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint16_t *cum = reinterpret_cast<uint16_t *>(smem + L::cum);
+    uint16_t *frq = reinterpret_cast<uint16_t *>(smem + L::frq);
+    uint8_t *tile = smem + L::tile;
+    float *m1s = reinterpret_cast<float *>(smem + L::m1);
+    uint8_t *srec = smem + L::recs;
+
+    int k, kv, l;
+    slice_coords(d, blockIdx.x, k, kv, l);
+    const int A = V2 ? 2 * mt.v[kv][l] + 1 : d.A[kv];
+    const uint32_t amax2 = 2u * ((uint32_t)A - 1);
+    const int Tk = chunk_tokens(d, k);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool dec = tid < kThreads;
+    const int st = tid - kThreads;  // support thread 0..255
+    const long long t0 = (long long)k * d.Tc;
+    const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
+    const long long sid = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk + tid;
+    const int nwin = (d.C + W - 1) / W;
+
+    if (V2 && tid <= Tk) s_ftab[tid] = (uint16_t)(1u + ((uint32_t)tid * (kM - (uint32_t)A)) / (uint32_t)Tk);
+    if (dec) {
+        const int MAX = mt.v[kv][l];
+        s_unit[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
+        if (tid < Tk) m1s[tid] = __half2float(__ushort_as_half(max1[group_index(d, kv, l, t0 + tid)]));
+        if (DELTA) {
+            const int ra = tid - tid % d.G;
+            s_anchor[tid] = (uint8_t)ra;
+            s_m1a[tid] = (tid < Tk && ra != tid)
+                             ? __half2float(__ushort_as_half(max1[group_index(d, kv, l, t0 + ra)]))
+                             : 0.0f;
+        }
+    }
+    Stream s;
+    bool corrupt = false, tail = false;
+    if (dec && tid < Tk) {
+        long long start = (long long)off[sid];
+        long long end = start + (long long)len[sid];
+        if (start > packed_bytes || end > packed_bytes) {
+            corrupt = true;
+            start = min(start, packed_bytes);
+            end = min(end, packed_bytes);
+        }
+        stream_init(s, packed, start, end);
+        const long long p4 = packed_bytes & ~3LL;
+        tail = end > p4 || (start & ~3LL) >= p4;
+    }
+    if (dec) tail = __any_sync(0xFFFFFFFFu, tail);
+    const bool vec = ((reinterpret_cast<uintptr_t>(cdf) & 15) == 0) && (d.A[0] % 8 == 0) && (d.A[1] % 8 == 0);
+    const uintptr_t galign = MODE == 2 ? 8 : 16;
+    const bool ovec = (d.C & 3) == 0 && (ols & 3) == 0 &&
+                      ((reinterpret_cast<uintptr_t>(out_k) | reinterpret_cast<uintptr_t>(out_v)) & (galign - 1)) == 0;
+    bool bad_rec = false;
+    __syncthreads();  // tables and max1
+
+    // support: the rows of window j into buffer j & 1
+    auto build = [&](int j) {
+        const int c0 = j * W, Wc = min(W, d.C - c0);
+        uint16_t *cb = cum + (j & 1) * W * P, *fb = frq + (j & 1) * W * P;
+        if (V2) {
+            if (warp == kThreads / 32) copy_records(srec, rec + side_base + (long long)c0 * A, Wc * A, lane);
+            asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");  // the records are in
+            bad_rec |= build_rows_v2<P>(cb, fb, srec, A, (uint32_t)Tk, W, Wc, st, s_ftab);
+        } else if (warp == kThreads / 32) {
+            stage_rows<P>(cb, fb, cdf + side_base + (long long)c0 * A, A, Wc, lane, vec);
+        }
+    };
+    // support: window j's decoded tile out
+    auto write = [&](int j) {
+        const int c0 = j * W, Wc = min(W, d.C - c0);
+        const uint8_t *tb = tile + (j & 1) * kThreads * TS;
+        if (DELTA) {
+            const int sw = warp - kThreads / 32;
+            const int rows = min(32, Tk - 32 * sw);
+            if (rows > 0)
+                write_window_delta<P, MODE>(tb, s_unit, m1s, s_m1a, s_anchor, d, kv, l, t0, 32 * sw, rows, c0, Wc,
+                                            out_k, out_v, ols, ovec, lane);
+        } else {
+            write_window<P, MODE, kThreads>(tb, s_unit, m1s, d, kv, l, t0, Tk, c0, Wc, out_k, out_v, ols, ovec, st);
+        }
+    };
+    if (!dec) build(0);
+    asm volatile("bar.sync 2, %0;" ::"n"(kLmDecThreads) : "memory");  // window 0's rows
+    const uint32_t fo = (uint32_t)(L::frq - L::cum);
+    for (int i = 0; i < nwin; i++) {
+        const int b = i & 1;
+        const int Wc = min(W, d.C - i * W);
+        if (dec) {
+            if (tid < Tk) {
+                const uint32_t cb = (uint32_t)__cvta_generic_to_shared(cum + b * W * P);
+                uint8_t *my = tile + b * kThreads * TS + tid * TS;
+                constexpr int PH = P > 4 ? P / 2 : P;
+                if (!V2 && A == P) {
+                    if (tail)
+                        decode_window<P, P, false, true, true>(s, cb, fo, amax2, my, Wc);
+                    else
+                        decode_window<P, P, false, false, true>(s, cb, fo, amax2, my, Wc);
+                } else if (A <= PH) {
+                    if (tail)
+                        decode_window<P, PH, true, true, true>(s, cb, fo, amax2, my, Wc);
+                    else
+                        decode_window<P, PH, true, false, true>(s, cb, fo, amax2, my, Wc);
+                } else {
+                    if (tail)
+                        decode_window<P, P, true, true, true>(s, cb, fo, amax2, my, Wc);
+                    else
+                        decode_window<P, P, true, false, true>(s, cb, fo, amax2, my, Wc);
+                }
+            }
+        } else {
+            if (i + 1 < nwin) build(i + 1);
+            if (i >= 1) write(i - 1);
+        }
+        asm volatile("bar.sync 2, %0;" ::"n"(kLmDecThreads) : "memory");  // window i handed over
+    }
+    if (!dec) write(nwin - 1);
+    if (dec && tid < Tk) {
+        const long long consumed = (long long)len[sid] - s.rem - s.nb / 8;
+        if ((corrupt || consumed != (long long)len[sid] + 3) && status) atomicOr(status, CG_FLAG_CORRUPT);
+    }
+    if (bad_rec && status) atomicOr(status, CG_FLAG_CORRUPT);
+}
+
 template <int P, int MODE, bool V2, bool DELTA>
 cudaError_t launch_pm(const uint8_t *packed, uint64_t packed_bytes, const uint64_t *off, const uint32_t *len,
                       const uint16_t *cdf, const uint8_t *rec, const uint16_t *max1, const Dims &d, const MaxTab &mt,
                       void *out_k, void *out_v, long long ols, int32_t *status, cudaStream_t s) {
     const unsigned nslices = (unsigned)(2LL * d.L * d.nch);
+    const int sms = device_sm_count();
+    if (sms > 0 && nslices <= (unsigned)sms) {  // latency mode: one slice per SM
+        const int lsmem = (int)LmDecSmem<P>::bytes;
+        cudaError_t err = cudaFuncSetAttribute(k_decode_lm<P, MODE, V2, DELTA>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, lsmem);
+        if (err != cudaSuccess) return err;
+        k_decode_lm<P, MODE, V2, DELTA><<<nslices, kLmDecThreads, lsmem, s>>>(
+            packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols, status);
+        return cudaGetLastError();
+    }
     const int smem = (int)PipeSmem<P>::bytes;
     cudaError_t err = cudaFuncSetAttribute(k_decode_pipe<P, MODE, V2, DELTA>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
