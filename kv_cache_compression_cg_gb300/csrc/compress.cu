@@ -323,18 +323,18 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
 // with the window's (lo, f) rows.
 __device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uint8_t *symrow, const uint2 *cdfw,
                                               int Wc) {
-    const uint32_t *my = reinterpret_cast<const uint32_t *>(symrow);
     const unsigned char *rows = reinterpret_cast<const unsigned char *>(cdfw);
     if (Wc == kW) {
 #pragma unroll
         for (int g = 0; g < kW / 4; g++) {
-            // every byte is 8q; the mask keeps any tile content 8-byte aligned
-            const uint32_t w4 = my[g] & 0xF8F8F8F8u;
+            // every tile byte is 8q (q <= 30, written by the quantiser), an aligned
+            // (lo, f) offset in its row: byte loads, no unpacking
+            const unsigned char *m4 = symrow + 4 * g;
             const unsigned char *r0 = rows + (4 * g) * kAS * 8;
-            const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + (w4 & 0xFFu));
-            const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + ((w4 >> 8) & 0xFFu));
-            const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + ((w4 >> 16) & 0xFFu));
-            const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + (w4 >> 24));
+            const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + m4[0]);
+            const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + m4[1]);
+            const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + m4[2]);
+            const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + m4[3]);
             if (e.nbits >= 32) enc_flush_word(e, stream);
             enc_symbol_lf(e, e0.x, e0.y);
             enc_symbol_lf(e, e1.x, e1.y);

@@ -818,7 +818,23 @@ __global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
         const int c0 = j * W, Wc = min(W, d.C - c0);
         uint16_t *cb = cum + (j & 1) * W * P, *fb = frq + (j & 1) * W * P;
         if (V2) {
-            if (warp == kThreads / 32) copy_records(srec, rec + side_base + (long long)c0 * A, Wc * A, lane);
+            // the window's records (contiguous) into shared memory, all support threads at once
+            const uint8_t *rw = rec + side_base + (long long)c0 * A;
+            const int nb = Wc * A;
+            const int lead = (int)((16 - (reinterpret_cast<uintptr_t>(rw) & 15)) & 15);  // bytes before a 16-byte boundary
+            const int head = min(lead, nb), nvec = (nb - head) >> 4;
+            for (int i = st; i < head; i += kThreads) srec[i] = __ldg(rw + i);
+            for (int i = st; i < nvec; i += kThreads) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4 *>(rw + head) + i);
+                uint8_t *dst = srec + head + 16 * i;
+#pragma unroll
+                for (int b = 0; b < 4; b++) {
+                    const uint32_t w = b == 0 ? q.x : b == 1 ? q.y : b == 2 ? q.z : q.w;
+#pragma unroll
+                    for (int y = 0; y < 4; y++) dst[4 * b + y] = (uint8_t)(w >> (8 * y));
+                }
+            }
+            for (int i = head + 16 * nvec + st; i < nb; i += kThreads) srec[i] = __ldg(rw + i);
             asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");  // the records are in
             bad_rec |= build_rows_v2<P>(cb, fb, srec, A, (uint32_t)Tk, W, Wc, st, s_ftab);
         } else if (warp == kThreads / 32) {
