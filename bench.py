@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-call figures of the other seeded workloads")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="code only the first N tokens of the workload (same bytes; for profiling a smaller case)")
     ap.add_argument("--no-chunk-parallel", action="store_true",
                     help="skip the oracle's chunk-parallel timing on all host cores")
     ap.add_argument("--group", type=int, default=1,
@@ -371,6 +373,8 @@ def run_ours(args):
     import dataclasses
 
     base = synth.WORKLOADS[args.workload]
+    if args.tokens:
+        base = dataclasses.replace(base, T=min(args.tokens, base.T))
     w = dataclasses.replace(base, seed=base.seed + 1000 * rank) if rank else base
     k, v = synth.generate_device(w)  # same bytes as the host generator
     fp16_bytes = 2 * k.numel() * k.element_size()

@@ -725,35 +725,40 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
 }
 
 // Latency mode: launches of at most one slice per SM, where a slice's time is
-// set by the serial chain of each token stream. A CTA of 512 threads splits the
-// work by warp: warps 0-7 only decode (thread t decodes token t, searching four
-// ways per level: fewer dependent loads per symbol), warps 8-15 build window
-// i + 1's CDF rows and write window i - 1's dequantised rows out while window i
-// is decoded, from double-buffered rows and symbol tiles; one 512-thread named
-// barrier per window hands them over.
-constexpr int kLmDecThreads = 512;
-
-template <int P>
+// set by the serial chain of each token stream. A CTA of 2 DEC threads splits
+// the work by warp: the first DEC threads only decode (thread t decodes token
+// R0 + t, searching four ways per level: fewer dependent loads per symbol), the
+// other DEC build window i + 1's CDF rows and write window i - 1's dequantised
+// rows out while window i is decoded, from double-buffered rows and symbol
+// tiles; one named barrier of all 2 DEC threads per window hands them over.
+// DEC = 256: a CTA per slice (at most one slice per SM). DEC = 128 (at most
+// one slice per two SMs, no delta): two CTAs per slice, each decoding half of
+// its token streams (rows [R0, R0 + h), h = ceil(Tc_k / 2)) with its own copy
+// of the CDF rows, which halves the instructions each SM issues per symbol.
+template <int P, int DEC>
 struct LmDecSmem {
     static constexpr int W = DecodeCfg<P>::W;
     static constexpr int TS = DecodeCfg<P>::TS;
     static constexpr size_t cum = 0;                                        // [2][W][P] uint16
     static constexpr size_t frq = cum + 2ull * W * P * 2;                   // [2][W][P] uint16
-    static constexpr size_t tile = (frq + 2ull * W * P * 2 + 15) & ~15ull;  // [2][kThreads * TS]
-    static constexpr size_t m1 = tile + 2ull * kThreads * TS;               // float[kThreads]
-    static constexpr size_t recs = m1 + kThreads * 4;                       // format 2: [W * P] records
+    static constexpr size_t tile = (frq + 2ull * W * P * 2 + 15) & ~15ull;  // [2][DEC * TS]
+    static constexpr size_t m1 = tile + 2ull * DEC * TS;                    // float[DEC]
+    static constexpr size_t recs = m1 + DEC * 4;                            // format 2: [W * P] records
     static constexpr size_t bytes = recs + 1ull * W * P;
 };
 
-template <int P, int MODE, bool V2, bool DELTA>
-__global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
+template <int P, int MODE, bool V2, bool DELTA, int DEC>
+__global__ void __launch_bounds__(2 * DEC, 1) k_decode_lm(
     const uint8_t *__restrict__ packed, long long packed_bytes, const uint64_t *__restrict__ off,
     const uint32_t *__restrict__ len, const uint16_t *__restrict__ cdf, const uint8_t *__restrict__ rec,
     const uint16_t *__restrict__ max1, Dims d, MaxTab mt, void *__restrict__ out_k, void *__restrict__ out_v,
     long long ols, int32_t *status) {
-    using L = LmDecSmem<P>;
+    using L = LmDecSmem<P, DEC>;
     constexpr int W = L::W;
     constexpr int TS = L::TS;
+    constexpr int NT = 2 * DEC;            // threads
+    constexpr int NP = kThreads / DEC;     // CTAs per slice
+    static_assert(!DELTA || NP == 1, "a token's anchor row must be in the same CTA");
     __shared__ __align__(256) float s_unit[256];  // (s - MAX) / MAX
     __shared__ uint16_t s_ftab[kThreads + 2];
     __shared__ float s_m1a[DELTA ? kThreads : 1];
@@ -766,23 +771,29 @@ __global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
     uint8_t *srec = smem + L::recs;
 
     int k, kv, l;
-    slice_coords(d, blockIdx.x, k, kv, l);
+    slice_coords(d, blockIdx.x / NP, k, kv, l);
     const int A = V2 ? 2 * mt.v[kv][l] + 1 : d.A[kv];
     const uint32_t amax2 = 2u * ((uint32_t)A - 1);
     const int Tk = chunk_tokens(d, k);
+    const int hrows = (Tk + NP - 1) / NP;
+    const int R0 = (int)(blockIdx.x % NP) * hrows;
+    const int nr = min(hrows, Tk - R0);  // this CTA's rows of the slice
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool dec = tid < kThreads;
-    const int st = tid - kThreads;  // support thread 0..255
-    const long long t0 = (long long)k * d.Tc;
+    const bool dec = tid < DEC;
+    const int st = tid - DEC;  // support thread 0 .. DEC - 1
+    const long long t0 = (long long)k * d.Tc + R0;  // first row of this CTA
     const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
-    const long long sid = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk + tid;
+    const long long sid = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk + R0 + tid;
     const int nwin = (d.C + W - 1) / W;
 
-    if (V2 && tid <= Tk) s_ftab[tid] = (uint16_t)(1u + ((uint32_t)tid * (kM - (uint32_t)A)) / (uint32_t)Tk);
-    if (dec) {
+    for (int n = tid; n <= Tk; n += NT)
+        if (V2) s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kM - (uint32_t)A)) / (uint32_t)Tk);
+    for (int q = tid; q < 256; q += NT) {
         const int MAX = mt.v[kv][l];
-        s_unit[tid] = __fdiv_rn((float)(tid - MAX), (float)MAX);
-        if (tid < Tk) m1s[tid] = __half2float(__ushort_as_half(max1[group_index(d, kv, l, t0 + tid)]));
+        s_unit[q] = __fdiv_rn((float)(q - MAX), (float)MAX);
+    }
+    if (dec) {
+        if (tid < nr) m1s[tid] = __half2float(__ushort_as_half(max1[group_index(d, kv, l, t0 + tid)]));
         if (DELTA) {
             const int ra = tid - tid % d.G;
             s_anchor[tid] = (uint8_t)ra;
@@ -793,7 +804,7 @@ __global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
     }
     Stream s;
     bool corrupt = false, tail = false;
-    if (dec && tid < Tk) {
+    if (dec && tid < nr) {
         long long start = (long long)off[sid];
         long long end = start + (long long)len[sid];
         if (start > packed_bytes || end > packed_bytes) {
@@ -823,8 +834,8 @@ __global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
             const int nb = Wc * A;
             const int lead = (int)((16 - (reinterpret_cast<uintptr_t>(rw) & 15)) & 15);  // bytes before a 16-byte boundary
             const int head = min(lead, nb), nvec = (nb - head) >> 4;
-            for (int i = st; i < head; i += kThreads) srec[i] = __ldg(rw + i);
-            for (int i = st; i < nvec; i += kThreads) {
+            for (int i = st; i < head; i += DEC) srec[i] = __ldg(rw + i);
+            for (int i = st; i < nvec; i += DEC) {
                 const uint4 q = __ldg(reinterpret_cast<const uint4 *>(rw + head) + i);
                 uint8_t *dst = srec + head + 16 * i;
 #pragma unroll
@@ -834,37 +845,39 @@ __global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
                     for (int y = 0; y < 4; y++) dst[4 * b + y] = (uint8_t)(w >> (8 * y));
                 }
             }
-            for (int i = head + 16 * nvec + st; i < nb; i += kThreads) srec[i] = __ldg(rw + i);
-            asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");  // the records are in
-            bad_rec |= build_rows_v2<P>(cb, fb, srec, A, (uint32_t)Tk, W, Wc, st, s_ftab);
-        } else if (warp == kThreads / 32) {
+            for (int i = head + 16 * nvec + st; i < nb; i += DEC) srec[i] = __ldg(rw + i);
+            asm volatile("bar.sync 1, %0;" ::"n"(DEC) : "memory");  // the records are in
+#pragma unroll
+            for (int t = st; t < kThreads; t += DEC)  // the row builder's 256 parts
+                bad_rec |= build_rows_v2<P>(cb, fb, srec, A, (uint32_t)Tk, W, Wc, t, s_ftab);
+        } else if (warp == DEC / 32) {
             stage_rows<P>(cb, fb, cdf + side_base + (long long)c0 * A, A, Wc, lane, vec);
         }
     };
     // support: window j's decoded tile out
     auto write = [&](int j) {
         const int c0 = j * W, Wc = min(W, d.C - c0);
-        const uint8_t *tb = tile + (j & 1) * kThreads * TS;
+        const uint8_t *tb = tile + (j & 1) * DEC * TS;
         if (DELTA) {
-            const int sw = warp - kThreads / 32;
-            const int rows = min(32, Tk - 32 * sw);
+            const int sw = warp - DEC / 32;
+            const int rows = min(32, nr - 32 * sw);
             if (rows > 0)
                 write_window_delta<P, MODE>(tb, s_unit, m1s, s_m1a, s_anchor, d, kv, l, t0, 32 * sw, rows, c0, Wc,
                                             out_k, out_v, ols, ovec, lane);
         } else {
-            write_window<P, MODE, kThreads>(tb, s_unit, m1s, d, kv, l, t0, Tk, c0, Wc, out_k, out_v, ols, ovec, st);
+            write_window<P, MODE, DEC>(tb, s_unit, m1s, d, kv, l, t0, nr, c0, Wc, out_k, out_v, ols, ovec, st);
         }
     };
     if (!dec) build(0);
-    asm volatile("bar.sync 2, %0;" ::"n"(kLmDecThreads) : "memory");  // window 0's rows
+    asm volatile("bar.sync 2, %0;" ::"n"(NT) : "memory");  // window 0's rows
     const uint32_t fo = (uint32_t)(L::frq - L::cum);
     for (int i = 0; i < nwin; i++) {
         const int b = i & 1;
         const int Wc = min(W, d.C - i * W);
         if (dec) {
-            if (tid < Tk) {
+            if (tid < nr) {
                 const uint32_t cb = (uint32_t)__cvta_generic_to_shared(cum + b * W * P);
-                uint8_t *my = tile + b * kThreads * TS + tid * TS;
+                uint8_t *my = tile + b * DEC * TS + tid * TS;
                 constexpr int PH = P > 4 ? P / 2 : P;
                 if (!V2 && A == P) {
                     if (tail)
@@ -887,10 +900,10 @@ __global__ void __launch_bounds__(kLmDecThreads, 1) k_decode_lm(
             if (i + 1 < nwin) build(i + 1);
             if (i >= 1) write(i - 1);
         }
-        asm volatile("bar.sync 2, %0;" ::"n"(kLmDecThreads) : "memory");  // window i handed over
+        asm volatile("bar.sync 2, %0;" ::"n"(NT) : "memory");  // window i handed over
     }
     if (!dec) write(nwin - 1);
-    if (dec && tid < Tk) {
+    if (dec && tid < nr) {
         const long long consumed = (long long)len[sid] - s.rem - s.nb / 8;
         if ((corrupt || consumed != (long long)len[sid] + 3) && status) atomicOr(status, CG_FLAG_CORRUPT);
     }
@@ -903,12 +916,23 @@ cudaError_t launch_pm(const uint8_t *packed, uint64_t packed_bytes, const uint64
                       void *out_k, void *out_v, long long ols, int32_t *status, cudaStream_t s) {
     const unsigned nslices = (unsigned)(2LL * d.L * d.nch);
     const int sms = device_sm_count();
-    if (sms > 0 && nslices <= (unsigned)sms) {  // latency mode: one slice per SM
-        const int lsmem = (int)LmDecSmem<P>::bytes;
-        cudaError_t err = cudaFuncSetAttribute(k_decode_lm<P, MODE, V2, DELTA>,
+    if constexpr (!DELTA) {
+        if (sms > 0 && 2 * nslices <= (unsigned)sms) {  // latency mode: a slice per two SMs
+            const int lsmem = (int)LmDecSmem<P, 128>::bytes;
+            cudaError_t err = cudaFuncSetAttribute(k_decode_lm<P, MODE, V2, false, 128>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, lsmem);
+            if (err != cudaSuccess) return err;
+            k_decode_lm<P, MODE, V2, false, 128><<<2 * nslices, 256, lsmem, s>>>(
+                packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols, status);
+            return cudaGetLastError();
+        }
+    }
+    if (sms > 0 && nslices <= (unsigned)sms) {  // latency mode: a slice per SM
+        const int lsmem = (int)LmDecSmem<P, 256>::bytes;
+        cudaError_t err = cudaFuncSetAttribute(k_decode_lm<P, MODE, V2, DELTA, 256>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, lsmem);
         if (err != cudaSuccess) return err;
-        k_decode_lm<P, MODE, V2, DELTA><<<nslices, kLmDecThreads, lsmem, s>>>(
+        k_decode_lm<P, MODE, V2, DELTA, 256><<<nslices, 512, lsmem, s>>>(
             packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols, status);
         return cudaGetLastError();
     }
