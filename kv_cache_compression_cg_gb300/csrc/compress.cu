@@ -410,6 +410,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     // the delta: each row's anchor row and the table (q - MAX) / MAX (an
     // anchor row keeps its max1 in s_m1 from the pre-pass on)
     __shared__ uint8_t s_anchor[DELTA ? kNT : 1];
+    __shared__ uint8_t s_aidx[DELTA ? kNT : 1];  // the delta: each row's anchor index (row / G)
     __shared__ float s_unitc[DELTA ? 64 : 1];
     extern __shared__ __align__(128) unsigned char dsm[];
 
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         __syncthreads();
         const int ra = tid - tid % d.G;
         s_anchor[tid] = (uint8_t)ra;
+        s_aidx[tid] = (uint8_t)(tid / d.G);
         if (tid < Tk && ra == tid) {
             const unsigned mb = s_m1[tid];
             s_fac[tid] = mb ? __fdiv_rn(fmax, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
@@ -492,7 +494,15 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     }
 
     // 1. max1 pass over the slice's boxes (buffers alternate); with the delta,
-    // max |x - a^| as binary32 bits (non-negative floats order like their bits)
+    // max |x - a^| as binary32 bits (non-negative floats order like their bits).
+    // When the anchor rows' reconstructions of a box (binary32, 256 bytes per
+    // anchor row) fit in the shared union beside the second box buffer (groups
+    // of 10 or more for 256-token chunks), each is computed once per box and
+    // read back by the rows of its group; otherwise each row recomputes its
+    // anchor's quad.
+    const int na = DELTA ? (Tk + d.G - 1) / d.G : 0;
+    const bool ahat_shared = DELTA && na * (kW * 4) <= kUnionBytes - (int)box_bytes;
+    float4 *ahat = reinterpret_cast<float4 *>(s_union + box_bytes);
     uint32_t ph0 = 0, ph1 = 0;
     uint32_t mx[16];
 #pragma unroll
@@ -505,6 +515,37 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         else
             ph0 ^= 1u;
         const unsigned char *box = odd ? s_union : box0;
+        if (DELTA && ahat_shared) {
+            for (int idx = tid; idx < na * 16; idx += kNT) {
+                const int ra = (idx >> 4) * d.G, q = idx & 15;
+                const uint2 xa = *reinterpret_cast<const uint2 *>(box + ra * (kW * 2) + 8 * q);
+                const float fa = s_fac[ra], ma = __half2float(__ushort_as_half(s_m1[ra]));
+                uint32_t c0, c1, c2, c3;
+                quant_pair(xa.x, fa, fm, mg, c0, c1);
+                quant_pair(xa.y, fa, fm, mg, c2, c3);
+                ahat[idx] = make_float4(__fmul_rn(lds_f32(us + 4u * min(c0 - kMagic, qmax)), ma),
+                                        __fmul_rn(lds_f32(us + 4u * min(c1 - kMagic, qmax)), ma),
+                                        __fmul_rn(lds_f32(us + 4u * min(c2 - kMagic, qmax)), ma),
+                                        __fmul_rn(lds_f32(us + 4u * min(c3 - kMagic, qmax)), ma));
+            }
+            __syncthreads();  // the box's anchor reconstructions are in
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const int r = rbase + 2 * i;
+                if (r < Tk) {
+                    const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
+                    // an anchor is its own zero reference: |x - (+-0)| = |x|
+                    const float4 a4 = s_anchor[r] == r ? make_float4(0.f, 0.f, 0.f, 0.f) : ahat[16 * s_aidx[r] + kq];
+                    const float2 x01 = __half22float2(*reinterpret_cast<const __half2 *>(&x.x));
+                    const float2 x23 = __half22float2(*reinterpret_cast<const __half2 *>(&x.y));
+                    const uint32_t m01 = max(__float_as_uint(__fsub_rn(x01.x, a4.x)) & 0x7FFFFFFFu,
+                                             __float_as_uint(__fsub_rn(x01.y, a4.y)) & 0x7FFFFFFFu);
+                    const uint32_t m23 = max(__float_as_uint(__fsub_rn(x23.x, a4.z)) & 0x7FFFFFFFu,
+                                             __float_as_uint(__fsub_rn(x23.y, a4.w)) & 0x7FFFFFFFu);
+                    mx[i] = max(mx[i], max(m01, m23));
+                }
+            }
+        } else {
 #pragma unroll
         for (int i = 0; i < 16; i++) {
             const int r = rbase + 2 * i;
@@ -523,6 +564,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
                     mx[i] = __vmaxu2(mx[i], x.y & 0x7FFF7FFFu);
                 }
             }
+        }
         }
         __syncthreads();  // the buffer is free again
         if (tid == 0) {
