@@ -122,6 +122,58 @@ __device__ __forceinline__ void red_add(uint32_t addr, uint32_t v) {
     asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// Thread-block cluster helpers (two CTAs sharing a slice in latency mode).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared address `addr` of this CTA, as the same location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_peer_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_peer_u64(uint32_t addr) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Every thread of both CTAs of the cluster arrives, then waits.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive (release, cluster scope) on the mbarrier at shared::cluster address `remote`.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Bounded wait (acquire, cluster scope) for the phase with the given parity.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+    for (int i = 0; i < kWaitLimit; i++) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
 __device__ __forceinline__ unsigned long long pair(float a, float b) {
     unsigned long long r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
@@ -248,9 +300,14 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
 // the counts of its eight symbols into (lo, f) entries of the channel's row,
 // clearing the counters it read, and writes the side output (CDF entries, or
 // the format 2 count record).
-template <bool V2>
+// NC == 2 (two CTAs per slice): the counts are this CTA's table `tb` (in
+// elements) plus the same table of the peer CTA (rank ^ 1), read through
+// distributed shared memory; the other table (the last window's, which both
+// CTAs have read) is cleared instead; only rank 0 writes the side output.
+template <bool V2, int NC = 1>
 __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const uint16_t *ftab, uint2 *cdfw,
-                                                 void *side_out, long long side_base, int c0, int Wc, int A) {
+                                                 void *side_out, long long side_base, int c0, int Wc, int A,
+                                                 int tb = 0, uint32_t rank = 0) {
     const int c = ct >> 2, p = ct & 3;
     // a warp covers eight channels and Wc is a multiple of 8, so a warp
     // is entirely inside or entirely outside the window
@@ -263,8 +320,14 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
         uint32_t fv = 0;
         if (s < A) {
             uint16_t *cp = cnt16 + s * kCntRow + c;
-            const uint32_t n = *cp;
-            *cp = 0;
+            uint32_t n;
+            if constexpr (NC == 2) {
+                n = (uint32_t)cp[tb] + ld_peer_u16(peer_addr(smem_u32(cp + tb), rank ^ 1u));
+                cp[(kCntBytes / 2) - tb] = 0;
+            } else {
+                n = *cp;
+                *cp = 0;
+            }
             fv = ftab[n];
             key = max(key, (n << 8) | (255u - (uint32_t)s));  // largest n, then smallest s
             if (V2) {
@@ -290,10 +353,11 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
     const uint32_t best = 255u - (key & 255u);
     const uint32_t extra = kTotal - total;
     uint2 *row = cdfw + c * kAS;
+    const bool out = NC == 1 || rank == 0;
     if (V2) {
         // count record: the mode, then the other symbols' counts
         uint8_t *g = static_cast<uint8_t *>(side_out) + side_base + (long long)(c0 + c) * A;
-        if (p == 0) g[0] = (uint8_t)best;
+        if (p == 0 && out) g[0] = (uint8_t)best;
 #pragma unroll
         for (int j = 0; j < kSP; j++) {
             const uint32_t s = (uint32_t)(kSP * p + j);
@@ -301,7 +365,8 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
                 const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
                 const uint32_t f = fj[j] + (s == best ? extra : 0u);
                 row[s] = make_uint2(lo, f);
-                if (s != best) g[s + (s < best ? 1u : 0u)] = (uint8_t)((j < 4 ? nlo >> (8 * j) : nhi >> (8 * (j - 4))) & 0xFFu);
+                if (s != best && out)
+                    g[s + (s < best ? 1u : 0u)] = (uint8_t)((j < 4 ? nlo >> (8 * j) : nhi >> (8 * (j - 4))) & 0xFFu);
             }
         }
     } else {
@@ -313,7 +378,7 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
                 const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
                 const uint32_t f = fj[j] + (s == best ? extra : 0u);
                 row[s] = make_uint2(lo, f);
-                g[s] = (uint16_t)lo;
+                if (out) g[s] = (uint16_t)lo;
             }
         }
     }
@@ -657,77 +722,99 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
 
 // Latency mode: launches of at most one slice per SM (a single chunk, say),
 // where each slice's CTA has an SM to itself and the coders' time is set by the
-// serial chain of each token stream, not by instruction issue. A CTA of 512
-// threads splits the work by warp: warps 0-7 only code (thread t codes token t),
-// warps 8-15 quantise and count window i + 1 and turn its counts into CDF rows
-// while the coders code window i, so the coders never wait on those steps. The
-// symbol tile and the CDF rows are double-buffered; one 512-thread named
-// barrier per window hands a window over (producers have finished window i,
-// coders have finished window i - 1). The max1 pass uses all 16 warps; the
-// fp16 boxes come by TMA into two buffers, window i + 2's box loading while
-// window i + 1 is quantised.
-constexpr int kLmThreads = 512;
-
-// Dynamic shared memory of the latency-mode kernel, in bytes from the
-// 128-byte aligned base: two fp16 boxes, two (lo, f) row sets, the counters,
-// two symbol tiles.
+// serial chain of each token stream, not by instruction issue. A CTA splits the
+// work by warp: the first 256 / NC threads only code (thread t codes token
+// R0 + t), the next 256 quantise and count window i + 1 and turn its counts into
+// CDF rows while the coders code window i, so the coders never wait on those
+// steps. The symbol tile and the CDF rows are double-buffered; one named
+// barrier of all threads per window hands a window over (producers have
+// finished window i, coders have finished window i - 1). The max1 pass uses all
+// warps; the fp16 boxes come by TMA into two buffers, window i + 2's box
+// loading while window i + 1 is quantised.
+// NC = 2 (at most one slice per two SMs): a cluster of two CTAs shares a slice,
+// CTA rank r taking rows [r h, r h + h), h = ceil(Tc_k / 2), so each SM codes
+// half the streams and quantises half the rows. Each CTA counts its rows into
+// one of two counter tables (alternating per window); its producers then tell
+// the peer's producers (a remote arrive on the peer's mbarrier, release at
+// cluster scope) and wait for the peer's word before both build the same CDF
+// rows from both tables (the peer's through distributed shared memory). A
+// CTA clears a table only after the peer has announced the next window's
+// counts, by which time the peer has read it. Rank 0 writes the side output
+// and the slice's byte total.
+template <int NC>
 struct LmSmem {
+    static constexpr int rows = kNT / NC;
+    static constexpr int sym_bytes = rows * kSymRow;
     static constexpr int cdfw = 0;
     static constexpr int cnt = cdfw + 2 * kCdfwBytes;
-    static constexpr int sym = cnt + kCntBytes;
-    static constexpr int box = (sym + 2 * kSymBytes + 127) & ~127;
+    static constexpr int sym = cnt + NC * kCntBytes;
+    static constexpr int box = (sym + 2 * sym_bytes + 127) & ~127;
     static int bytes(int box_bytes) { return 128 + box + 2 * box_bytes; }
 };
 
-template <bool V2>
-__global__ void __launch_bounds__(kLmThreads, 1) k_compress_lm(
+template <bool V2, int NC>
+__global__ void __launch_bounds__(kNT / NC + kNT, 1) k_compress_lm(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, Dims d, MaxTab mt,
     int box_rows, uint16_t *__restrict__ max1_out, void *__restrict__ side_out, uint8_t *__restrict__ stage,
     uint32_t *__restrict__ len, unsigned long long *state, int32_t *status) {
+    using S = LmSmem<NC>;
+    constexpr int NCOD = kNT / NC;   // coder threads
+    constexpr int NCW = NCOD / 32;   // coder warps
+    constexpr int NTH = NCOD + kNT;  // threads
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ unsigned long long s_bar[2];
-    __shared__ unsigned long long s_scan[kNW];
-    __shared__ float s_fac[kNT];
-    __shared__ uint16_t s_m1[kNT];
+    __shared__ unsigned long long s_bar[4];  // box buffers 0 and 1; the peer's word on even / odd windows
+    __shared__ unsigned long long s_scan[NCW + 1];
+    __shared__ float s_fac[NCOD];
+    __shared__ uint16_t s_m1[NCOD];
     __shared__ uint16_t s_ftab[kNT + 2];
 
     const uint32_t dyn = smem_u32(dsm);
     const uint32_t base = (dyn + 127u) & ~127u;
     unsigned char *sm = dsm + (base - dyn);
-    uint2 *cdfw2 = reinterpret_cast<uint2 *>(sm + LmSmem::cdfw);
-    uint16_t *cnt16 = reinterpret_cast<uint16_t *>(sm + LmSmem::cnt);
-    uint32_t *cnt32 = reinterpret_cast<uint32_t *>(sm + LmSmem::cnt);
-    uint8_t *sym2 = sm + LmSmem::sym;
-    const uint32_t buf0 = base + LmSmem::box, buf1 = buf0 + (uint32_t)box_rows * (kW * 2);
+    uint2 *cdfw2 = reinterpret_cast<uint2 *>(sm + S::cdfw);
+    uint16_t *cnt16 = reinterpret_cast<uint16_t *>(sm + S::cnt);
+    uint32_t *cnt32 = reinterpret_cast<uint32_t *>(sm + S::cnt);
+    uint8_t *sym2 = sm + S::sym;
+    const uint32_t buf0 = base + S::box, buf1 = buf0 + (uint32_t)box_rows * (kW * 2);
     const uint32_t bar0 = smem_u32(&s_bar[0]), bar1 = smem_u32(&s_bar[1]);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int slice = blockIdx.x;
+    const uint32_t rank = NC == 2 ? cluster_rank() : 0u;
+    const int slice = blockIdx.x / NC;
     int k, kv, l;
     slice_coords(d, slice, k, kv, l);
     const int Tk = chunk_tokens(d, k);
+    const int h = (Tk + NC - 1) / NC;
+    const int R0 = (int)rank * h;
+    const int nr = min(h, Tk - R0);  // this CTA's rows of the slice: [R0, R0 + nr)
     const int MAX = mt.v[kv][l];
     const int A = V2 ? 2 * MAX + 1 : d.A[kv];
     const CUtensorMap *tm = kv ? &tmv : &tmk;
     const int t0 = k * d.Tc;
+    const int ty = t0 + R0;  // first row of this CTA's boxes
     const int nwin = (d.C + kW - 1) / kW;
     const uint32_t box_bytes = (uint32_t)box_rows * (kW * 2);
     const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
-    const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk;
+    const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk + R0;
     bool timed_out = false;
     if (tid == 0) {
         mbar_init(bar0);
         mbar_init(bar1);
+        mbar_init(smem_u32(&s_bar[2]));
+        mbar_init(smem_u32(&s_bar[3]));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         // the max1 pass reads window m from buffer m & 1; the coding pass reads
         // window i from buffer (nwin + i) & 1 (with one window, buffer 1 holds it)
-        tma_load(buf0, tm, 0, t0, l, bar0, box_bytes);
-        tma_load(buf1, tm, nwin > 1 ? kW : 0, t0, l, bar1, box_bytes);
+        tma_load(buf0, tm, 0, ty, l, bar0, box_bytes);
+        tma_load(buf1, tm, nwin > 1 ? kW : 0, ty, l, bar1, box_bytes);
     }
-    __syncthreads();
+    if (NC == 2)
+        cluster_sync();  // both CTAs' mbarriers exist before either arrives on the other's
+    else
+        __syncthreads();
 
-    // 1. max1 pass, all 16 warps: lane (quad kq) of warp w keeps rows 16 w + (lane >> 4) + 2 i
+    // 1. max1 pass, all warps: lane (quad kq) of warp w keeps rows 16 w + (lane >> 4) + 2 i
     const int kq = lane & 15;
     uint32_t ph0 = 0u, ph1 = 0u;
     {
@@ -746,7 +833,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) k_compress_lm(
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 const int r = rb + 2 * i;
-                if (r < Tk) {
+                if (r < nr) {
                     const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
                     mx[i] = __vmaxu2(mx[i], x.x & 0x7FFF7FFFu);
                     mx[i] = __vmaxu2(mx[i], x.y & 0x7FFF7FFFu);
@@ -756,7 +843,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) k_compress_lm(
             if (tid == 0) {
                 const int j = m + 2 < nwin ? m + 2 : m + 2 - nwin;  // the coding pass starts over at 0 and 1
                 if (m + 2 < nwin || (j < 2 && j < nwin))
-                    tma_load(b ? buf1 : buf0, tm, j * kW, t0, l, b ? bar1 : bar0, box_bytes);
+                    tma_load(b ? buf1 : buf0, tm, j * kW, ty, l, b ? bar1 : bar0, box_bytes);
             }
         }
         uint32_t mine = 0;
@@ -771,16 +858,16 @@ __global__ void __launch_bounds__(kLmThreads, 1) k_compress_lm(
         }
         bool nonfinite = false;
         const int r = rb + 2 * kq;
-        if (kq < 8 && r < Tk) {
+        if (kq < 8 && r < nr) {
             s_m1[r] = (uint16_t)mine;
-            max1_out[group_index(d, kv, l, t0 + r)] = (uint16_t)mine;
+            max1_out[group_index(d, kv, l, ty + r)] = (uint16_t)mine;
             nonfinite = mine >= 0x7C00u;
         }
-        for (int n = tid; n <= Tk; n += kLmThreads)
+        for (int n = tid; n <= Tk; n += NTH)
             s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kTotal - (uint32_t)A)) / (uint32_t)Tk);
-        for (int i = tid; i < kCntBytes / 4; i += kLmThreads) cnt32[i] = 0;
+        for (int i = tid; i < NC * kCntBytes / 4; i += NTH) cnt32[i] = 0;
         nonfinite = __syncthreads_or(nonfinite) != 0;
-        if (tid < Tk) {
+        if (tid < nr) {
             const unsigned mb = s_m1[tid];
             s_fac[tid] = mb ? __fdiv_rn((float)MAX, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
         }
@@ -791,55 +878,66 @@ __global__ void __launch_bounds__(kLmThreads, 1) k_compress_lm(
     }
     const bool safe = timed_out;
 
-    if (warp >= kNW) {
+    if (warp >= NCW) {
         // producers: window i's symbols, counts and CDF rows into buffers i & 1
-        const int pt = tid - kNT;
-        const int pw = warp - kNW;
+        const int pt = tid - NCOD;
+        const int pw = warp - NCW;
         const int rbase = 32 * pw + (lane >> 4);
         const unsigned long long fm = pair((float)MAX, (float)MAX);
         const unsigned long long mg = pair(12582912.0f, 12582912.0f);
         const uint32_t qmax = 2u * (uint32_t)MAX;
         const uint32_t cnt_lane = smem_u32(cnt32) + 8u * (uint32_t)kq - (uint32_t)(kCntRow * 2) * kMagic;
+        // the peer's word for window i arrives on s_bar[2 + (i & 1)], phase i >> 1:
+        // it cannot run a phase ahead, as its word for window i + 2 needs this
+        // CTA's word for window i + 1, sent after this wait
+        const uint32_t xb0 = smem_u32(&s_bar[2]), xb1 = smem_u32(&s_bar[3]);
+        const uint32_t xp0 = NC == 2 ? peer_addr(xb0, rank ^ 1u) : 0u, xp1 = NC == 2 ? peer_addr(xb1, rank ^ 1u) : 0u;
         bool late = false;
         for (int i = 0; i < nwin; i++) {
             const int c0 = i * kW;
             const int Wc = min(kW, d.C - c0);
+            const int tb = NC == 2 ? (i & 1) * (kCntBytes / 2) : 0;  // this window's counter table (elements)
             const bool b = ((nwin + i) & 1) != 0;  // box buffer of window i in the coding pass
             if (!mbar_wait(b ? bar1 : bar0, b ? ph1 : ph0)) late = true;
             if (b)
                 ph1 ^= 1u;
             else
                 ph0 ^= 1u;
-            uint8_t *sym = sym2 + (i & 1) * kSymBytes;
+            uint8_t *sym = sym2 + (i & 1) * S::sym_bytes;
             const unsigned char *box = sm + ((b ? buf1 : buf0) - base);
             if (4 * kq < Wc) {
                 if (safe || late)
-                    quantise_window<true>(box, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                    quantise_window<true>(box, s_fac, sym, cnt_lane + 2u * tb, rbase, kq, nr, fm, mg, qmax);
                 else
-                    quantise_window<false>(box, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                    quantise_window<false>(box, s_fac, sym, cnt_lane + 2u * tb, rbase, kq, nr, fm, mg, qmax);
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kNT) : "memory");  // counts in, box read
-            if (pt == 0 && i + 2 < nwin) tma_load(b ? buf1 : buf0, tm, (i + 2) * kW, t0, l, b ? bar1 : bar0, box_bytes);
-            build_cdf_window<V2>(pt, cnt16, s_ftab, cdfw2 + (i & 1) * (kCdfwBytes / 8), side_out, side_base, c0,
-                                 Wc, A);
-            asm volatile("bar.sync 2, %0;" ::"n"(kLmThreads) : "memory");  // window i handed over
+            if (pt == 0 && i + 2 < nwin) tma_load(b ? buf1 : buf0, tm, (i + 2) * kW, ty, l, b ? bar1 : bar0, box_bytes);
+            if constexpr (NC == 2) {
+                const bool odd = (i & 1) != 0;
+                if (pt == 0) mbar_arrive_remote(odd ? xp1 : xp0);  // this CTA's counts of window i are in
+                if (!mbar_wait_cluster(odd ? xb1 : xb0, (uint32_t)(i >> 1) & 1u)) late = true;  // and the peer's
+            }
+            build_cdf_window<V2, NC>(pt, cnt16, s_ftab, cdfw2 + (i & 1) * (kCdfwBytes / 8), side_out, side_base, c0,
+                                     Wc, A, tb, rank);
+            asm volatile("bar.sync 2, %0;" ::"n"(NTH) : "memory");  // window i handed over
         }
         if (late && lane == 0 && status) atomicOr(status, CG_FLAG_TIMEOUT);
     } else {
         // coders: window i from buffers i & 1
         Enc e;
         enc_init(e);
-        uint8_t *stream = stage_stream(stage, sid0 + (tid < Tk ? tid : 0), d);
-        asm volatile("bar.sync 2, %0;" ::"n"(kLmThreads) : "memory");  // window 0 is ready
+        uint8_t *stream = stage_stream(stage, sid0 + (tid < nr ? tid : 0), d);
+        asm volatile("bar.sync 2, %0;" ::"n"(NTH) : "memory");  // window 0 is ready
         for (int i = 0; i < nwin; i++) {
             const int Wc = min(kW, d.C - i * kW);
-            if (tid < Tk)
-                encode_window(e, stream, sym2 + (i & 1) * kSymBytes + tid * kSymRow,
+            if (tid < nr)
+                encode_window(e, stream, sym2 + (i & 1) * S::sym_bytes + tid * kSymRow,
                               cdfw2 + (i & 1) * (kCdfwBytes / 8), Wc);
-            if (i + 1 < nwin) asm volatile("bar.sync 2, %0;" ::"n"(kLmThreads) : "memory");
+            if (i + 1 < nwin) asm volatile("bar.sync 2, %0;" ::"n"(NTH) : "memory");
         }
-        const uint32_t mylen = tid < Tk ? enc_finish(e, stream) : 0u;
-        if (tid < Tk) len[sid0 + tid] = mylen;
+        const uint32_t mylen = tid < nr ? enc_finish(e, stream) : 0u;
+        if (tid < nr) len[sid0 + tid] = mylen;
         uint32_t tot = mylen;
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
@@ -849,8 +947,15 @@ __global__ void __launch_bounds__(kLmThreads, 1) k_compress_lm(
     if (tid == 0) {
         unsigned long long run = 0;
 #pragma unroll
-        for (int w = 0; w < kNW; w++) run += s_scan[w];
-        state[2 + 2LL * d.L * d.nch + slice] = run;
+        for (int w = 0; w < NCW; w++) run += s_scan[w];
+        s_scan[NCW] = run;
+        if (NC == 1) state[2 + 2LL * d.L * d.nch + slice] = run;
+    }
+    if constexpr (NC == 2) {
+        cluster_sync();  // both CTAs' totals are in
+        if (rank == 0 && tid == 0)
+            state[2 + 2LL * d.L * d.nch + slice] = s_scan[NCW] + ld_peer_u64(peer_addr(smem_u32(&s_scan[NCW]), 1u));
+        cluster_sync();  // the peer's shared memory is read before either CTA exits
     }
 }
 
@@ -1113,15 +1218,41 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
     cudaError_t err;
     const int sms = device_sm_count();
     if (d.G == 1 && sms > 0 && nslices <= sms) {
-        // latency mode: one CTA of coders and producers per slice, one slice per
-        // SM; the slice totals go to state[2 + nslices ..], which the packing
-        // reads directly (no tickets, no look-back)
-        const int dyn = LmSmem::bytes(box_rows * kW * 2);
-        auto kern = v2 ? k_compress_lm<true> : k_compress_lm<false>;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-        if (err != cudaSuccess) return err;
-        kern<<<(unsigned)nslices, kLmThreads, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, side, stage, len, state,
-                                                        status);
+        // latency mode: coders and producers per slice, one slice per SM (or a
+        // cluster of two CTAs per slice, one slice per two SMs); the slice
+        // totals go to state[2 + nslices ..], which the packing reads directly
+        // (no tickets, no look-back)
+        const int tmax = d.Tc < d.T ? d.Tc : d.T;
+        if (2 * nslices <= sms && tmax >= 2) {
+            const int rows = (tmax + 1) / 2;
+            CUtensorMap hk, hv;
+            if (!make_map(&hk, k, d, rows) || !make_map(&hv, v, d, rows)) return cudaErrorNotSupported;
+            const int dyn = LmSmem<2>::bytes(rows * kW * 2);
+            auto kern = v2 ? k_compress_lm<true, 2> : k_compress_lm<false, 2>;
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+            if (err != cudaSuccess) return err;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(2 * nslices));
+            cfg.blockDim = dim3(kNT / 2 + kNT);
+            cfg.dynamicSmemBytes = (size_t)dyn;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            err = cudaLaunchKernelEx(&cfg, kern, hk, hv, d, mt, rows, max1, side, stage, len, state, status);
+            if (err != cudaSuccess) return err;
+        } else {
+            const int dyn = LmSmem<1>::bytes(box_rows * kW * 2);
+            auto kern = v2 ? k_compress_lm<true, 1> : k_compress_lm<false, 1>;
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+            if (err != cudaSuccess) return err;
+            kern<<<(unsigned)nslices, 2 * kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, side, stage, len, state,
+                                                       status);
+        }
         k_pack_lm<<<(unsigned)(kPackParts * nslices), kNT, 0, s>>>(d, stage, len, off, packed, capacity,
                                                                    state + 2 + nslices, status);
         return cudaGetLastError();

@@ -725,12 +725,13 @@ __global__ void __launch_bounds__(kThreads + kHelpers, 4) k_decode_pipe(
 }
 
 // Latency mode: launches of at most one slice per SM, where a slice's time is
-// set by the serial chain of each token stream. A CTA of 2 DEC threads splits
-// the work by warp: the first DEC threads only decode (thread t decodes token
-// R0 + t, searching four ways per level: fewer dependent loads per symbol), the
-// other DEC build window i + 1's CDF rows and write window i - 1's dequantised
-// rows out while window i is decoded, from double-buffered rows and symbol
-// tiles; one named barrier of all 2 DEC threads per window hands them over.
+// set by the serial chain of each token stream. A CTA of DEC + 256 threads
+// splits the work by warp: the first DEC threads only decode (thread t decodes
+// token R0 + t, searching four ways per level: fewer dependent loads per
+// symbol), the other 256 build window i + 1's CDF rows and write window i - 1's
+// dequantised rows out while window i is decoded, from double-buffered rows
+// and symbol tiles; one named barrier of all threads per window hands them
+// over.
 // DEC = 256: a CTA per slice (at most one slice per SM). DEC = 128 (at most
 // one slice per two SMs, no delta): two CTAs per slice, each decoding half of
 // its token streams (rows [R0, R0 + h), h = ceil(Tc_k / 2)) with its own copy
@@ -748,7 +749,7 @@ struct LmDecSmem {
 };
 
 template <int P, int MODE, bool V2, bool DELTA, int DEC>
-__global__ void __launch_bounds__(2 * DEC, 1) k_decode_lm(
+__global__ void __launch_bounds__(DEC + kThreads, 1) k_decode_lm(
     const uint8_t *__restrict__ packed, long long packed_bytes, const uint64_t *__restrict__ off,
     const uint32_t *__restrict__ len, const uint16_t *__restrict__ cdf, const uint8_t *__restrict__ rec,
     const uint16_t *__restrict__ max1, Dims d, MaxTab mt, void *__restrict__ out_k, void *__restrict__ out_v,
@@ -756,7 +757,8 @@ __global__ void __launch_bounds__(2 * DEC, 1) k_decode_lm(
     using L = LmDecSmem<P, DEC>;
     constexpr int W = L::W;
     constexpr int TS = L::TS;
-    constexpr int NT = 2 * DEC;            // threads
+    constexpr int SUP = kThreads;          // support threads
+    constexpr int NT = DEC + SUP;          // threads
     constexpr int NP = kThreads / DEC;     // CTAs per slice
     static_assert(!DELTA || NP == 1, "a token's anchor row must be in the same CTA");
     __shared__ __align__(256) float s_unit[256];  // (s - MAX) / MAX
@@ -780,7 +782,7 @@ __global__ void __launch_bounds__(2 * DEC, 1) k_decode_lm(
     const int nr = min(hrows, Tk - R0);  // this CTA's rows of the slice
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool dec = tid < DEC;
-    const int st = tid - DEC;  // support thread 0 .. DEC - 1
+    const int st = tid - DEC;  // support thread 0 .. SUP - 1
     const long long t0 = (long long)k * d.Tc + R0;  // first row of this CTA
     const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
     const long long sid = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk + R0 + tid;
@@ -834,8 +836,8 @@ __global__ void __launch_bounds__(2 * DEC, 1) k_decode_lm(
             const int nb = Wc * A;
             const int lead = (int)((16 - (reinterpret_cast<uintptr_t>(rw) & 15)) & 15);  // bytes before a 16-byte boundary
             const int head = min(lead, nb), nvec = (nb - head) >> 4;
-            for (int i = st; i < head; i += DEC) srec[i] = __ldg(rw + i);
-            for (int i = st; i < nvec; i += DEC) {
+            for (int i = st; i < head; i += SUP) srec[i] = __ldg(rw + i);
+            for (int i = st; i < nvec; i += SUP) {
                 const uint4 q = __ldg(reinterpret_cast<const uint4 *>(rw + head) + i);
                 uint8_t *dst = srec + head + 16 * i;
 #pragma unroll
@@ -845,11 +847,9 @@ __global__ void __launch_bounds__(2 * DEC, 1) k_decode_lm(
                     for (int y = 0; y < 4; y++) dst[4 * b + y] = (uint8_t)(w >> (8 * y));
                 }
             }
-            for (int i = head + 16 * nvec + st; i < nb; i += DEC) srec[i] = __ldg(rw + i);
-            asm volatile("bar.sync 1, %0;" ::"n"(DEC) : "memory");  // the records are in
-#pragma unroll
-            for (int t = st; t < kThreads; t += DEC)  // the row builder's 256 parts
-                bad_rec |= build_rows_v2<P>(cb, fb, srec, A, (uint32_t)Tk, W, Wc, t, s_ftab);
+            for (int i = head + 16 * nvec + st; i < nb; i += SUP) srec[i] = __ldg(rw + i);
+            asm volatile("bar.sync 1, %0;" ::"n"(SUP) : "memory");  // the records are in
+            bad_rec |= build_rows_v2<P>(cb, fb, srec, A, (uint32_t)Tk, W, Wc, st, s_ftab);
         } else if (warp == DEC / 32) {
             stage_rows<P>(cb, fb, cdf + side_base + (long long)c0 * A, A, Wc, lane, vec);
         }
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(2 * DEC, 1) k_decode_lm(
                 write_window_delta<P, MODE>(tb, s_unit, m1s, s_m1a, s_anchor, d, kv, l, t0, 32 * sw, rows, c0, Wc,
                                             out_k, out_v, ols, ovec, lane);
         } else {
-            write_window<P, MODE, DEC>(tb, s_unit, m1s, d, kv, l, t0, nr, c0, Wc, out_k, out_v, ols, ovec, st);
+            write_window<P, MODE, SUP>(tb, s_unit, m1s, d, kv, l, t0, nr, c0, Wc, out_k, out_v, ols, ovec, st);
         }
     };
     if (!dec) build(0);
@@ -922,7 +922,7 @@ cudaError_t launch_pm(const uint8_t *packed, uint64_t packed_bytes, const uint64
             cudaError_t err = cudaFuncSetAttribute(k_decode_lm<P, MODE, V2, false, 128>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, lsmem);
             if (err != cudaSuccess) return err;
-            k_decode_lm<P, MODE, V2, false, 128><<<2 * nslices, 256, lsmem, s>>>(
+            k_decode_lm<P, MODE, V2, false, 128><<<2 * nslices, 128 + kThreads, lsmem, s>>>(
                 packed, (long long)packed_bytes, off, len, cdf, rec, max1, d, mt, out_k, out_v, ols, status);
             return cudaGetLastError();
         }
