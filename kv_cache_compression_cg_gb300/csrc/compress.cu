@@ -71,6 +71,22 @@ constexpr int kBoxBytesMax = kNT * kW * 2;
 constexpr int kCodeBytes = kCdfwBytes + kCntBytes + kSymBytes;
 constexpr int kUnionBytes = kCodeBytes > kBoxBytesMax ? kCodeBytes : kBoxBytesMax;
 
+// Sizes of the throughput kernel for alphabets up to AM symbols (32, or 64 for
+// layers of up to 64 bins, format 1, or 65, format 2): rows of AM + 1 (lo, f)
+// entries, AM / 4 symbols per CDF thread, an AM-row counter table. Tile bytes
+// hold q << SH, an offset into a row of 8-byte entries that fits a byte
+// (8q for q < 32; 4q, doubled on use, for q < 64).
+template <int AM>
+struct Alpha {
+    static constexpr int AS = AM + 1;
+    static constexpr int SP = AM / 4;
+    static constexpr int SH = AM <= 32 ? 3 : 2;
+    static constexpr int cdfw_bytes = kW * AS * 8;
+    static constexpr int cnt_bytes = AM * kCntRow * 2;
+    static constexpr int code_bytes = cdfw_bytes + cnt_bytes + kSymBytes;
+    static constexpr int union_bytes = code_bytes > kBoxBytesMax ? code_bytes : kBoxBytesMax;
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -267,7 +283,7 @@ __global__ void k_compress_init(unsigned long long *state, long long nslices) {
 // the symbol tile and count q. SAFE (a slice with a non-finite max1, or a box
 // whose wait ran out) clamps q to [0, 2 MAX] before using it; finite input
 // under its own max1 needs no clamp.
-template <bool SAFE>
+template <bool SAFE, int SH = 3>
 __device__ __forceinline__ void quantise_window(const unsigned char *box, const float *fac, uint8_t *sym,
                                                 uint32_t cnt_lane, int rbase, int kq, int Tk,
                                                 unsigned long long fm, unsigned long long mg, uint32_t qmax) {
@@ -287,7 +303,7 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
             b3 = min(b3 - kMagic, qmax) + kMagic;
         }
         const uint32_t lo2 = __byte_perm(b0, b1, 0x0040), hi2 = __byte_perm(b2, b3, 0x0040);
-        *reinterpret_cast<uint32_t *>(sym + r * kSymRow + 4 * kq) = __byte_perm(lo2, hi2, 0x5410) << 3;
+        *reinterpret_cast<uint32_t *>(sym + r * kSymRow + 4 * kq) = __byte_perm(lo2, hi2, 0x5410) << SH;
         // counter word of (q, channel pair) = cnt_lane + 132 q (+4 for the second pair)
         red_add(b0 * (kCntRow * 2) + cnt_lane, 1u);
         red_add(b1 * (kCntRow * 2) + cnt_lane, 1u << 16);
@@ -304,16 +320,20 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
 // elements) plus the same table of the peer CTA (rank ^ 1), read through
 // distributed shared memory; the other table (the last window's, which both
 // CTAs have read) is cleared instead; only rank 0 writes the side output.
-template <bool V2, int NC = 1>
+template <bool V2, int NC = 1, int AM = kAmax>
 __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const uint16_t *ftab, uint2 *cdfw,
                                                  void *side_out, long long side_base, int c0, int Wc, int A,
                                                  int tb = 0, uint32_t rank = 0) {
+    constexpr int kSP = Alpha<AM>::SP;
+    constexpr int kAS = Alpha<AM>::AS;
+    constexpr int kCntBytes = Alpha<AM>::cnt_bytes;
     const int c = ct >> 2, p = ct & 3;
     // a warp covers eight channels and Wc is a multiple of 8, so a warp
     // is entirely inside or entirely outside the window
     if (c >= Wc) return;
     uint32_t fj[kSP], pre[kSP];
-    uint32_t sum = 0, key = 0, nlo = 0, nhi = 0;  // counts, one byte each (capped)
+    uint32_t sum = 0, key = 0;
+    uint32_t nb[(kSP + 3) / 4] = {};  // counts, one byte each (capped)
 #pragma unroll
     for (int j = 0; j < kSP; j++) {
         const int s = kSP * p + j;
@@ -330,12 +350,7 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
             }
             fv = ftab[n];
             key = max(key, (n << 8) | (255u - (uint32_t)s));  // largest n, then smallest s
-            if (V2) {
-                if (j < 4)
-                    nlo |= min(n, 255u) << (8 * j);
-                else
-                    nhi |= min(n, 255u) << (8 * (j - 4));
-            }
+            if (V2) nb[j / 4] |= min(n, 255u) << (8 * (j % 4));
         }
         pre[j] = sum;
         sum += fv;
@@ -365,8 +380,7 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
                 const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
                 const uint32_t f = fj[j] + (s == best ? extra : 0u);
                 row[s] = make_uint2(lo, f);
-                if (s != best && out)
-                    g[s + (s < best ? 1u : 0u)] = (uint8_t)((j < 4 ? nlo >> (8 * j) : nhi >> (8 * (j - 4))) & 0xFFu);
+                if (s != best && out) g[s + (s < best ? 1u : 0u)] = (uint8_t)((nb[j / 4] >> (8 * (j % 4))) & 0xFFu);
             }
         }
     } else {
@@ -386,8 +400,11 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
 
 // Step 4 for one window: code this thread's row of the symbol tile (bytes 8q)
 // with the window's (lo, f) rows.
+template <int AM = kAmax>
 __device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uint8_t *symrow, const uint2 *cdfw,
                                               int Wc) {
+    constexpr int kAS = Alpha<AM>::AS;
+    constexpr uint32_t U = 1u << (3 - Alpha<AM>::SH);  // tile byte -> byte offset of the (lo, f) entry
     const unsigned char *rows = reinterpret_cast<const unsigned char *>(cdfw);
     if (Wc == kW) {
 #pragma unroll
@@ -396,10 +413,10 @@ __device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uin
             // (lo, f) offset in its row: byte loads, no unpacking
             const unsigned char *m4 = symrow + 4 * g;
             const unsigned char *r0 = rows + (4 * g) * kAS * 8;
-            const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + m4[0]);
-            const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + m4[1]);
-            const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + m4[2]);
-            const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + m4[3]);
+            const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + U * m4[0]);
+            const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + U * m4[1]);
+            const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + U * m4[2]);
+            const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + U * m4[3]);
             if (e.nbits >= 32) enc_flush_word(e, stream);
             enc_symbol_lf(e, e0.x, e0.y);
             enc_symbol_lf(e, e1.x, e1.y);
@@ -409,7 +426,7 @@ __device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uin
         }
     } else {
         for (int c = 0; c < Wc; c++) {
-            const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + (symrow[c] & 0xF8u));
+            const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + U * (symrow[c] & (0xFFu << Alpha<AM>::SH)));
             if (e.nbits >= 32) enc_flush_word(e, stream);
             enc_symbol_lf(e, en.x, en.y);
         }
@@ -424,6 +441,7 @@ __device__ __forceinline__ float anchor_m1(const uint16_t *m1, int ra, int r) {
 
 // Step 2 with the delta: every row as d = x - a^ (anchors against +-0), q
 // clamped to [0, 2 MAX] (max1 rounded to 65504 can sit below max |d|).
+template <int SH = 3>
 __device__ __forceinline__ void quantise_window_delta(const unsigned char *box, const float *fac,
                                                       const uint8_t *anchor, const uint16_t *m1, uint32_t us,
                                                       uint8_t *sym, uint32_t cnt_lane, int rbase, int kq, int Tk,
@@ -446,7 +464,7 @@ __device__ __forceinline__ void quantise_window_delta(const unsigned char *box, 
         b2 = (uint32_t)min(max((int)(b2 - kMagic), 0), (int)qmax) + kMagic;
         b3 = (uint32_t)min(max((int)(b3 - kMagic), 0), (int)qmax) + kMagic;
         const uint32_t lo2 = __byte_perm(b0, b1, 0x0040), hi2 = __byte_perm(b2, b3, 0x0040);
-        *reinterpret_cast<uint32_t *>(sym + r * kSymRow + 4 * kq) = __byte_perm(lo2, hi2, 0x5410) << 3;
+        *reinterpret_cast<uint32_t *>(sym + r * kSymRow + 4 * kq) = __byte_perm(lo2, hi2, 0x5410) << SH;
         red_add(b0 * (kCntRow * 2) + cnt_lane, 1u);
         red_add(b1 * (kCntRow * 2) + cnt_lane, 1u << 16);
         red_add(b2 * (kCntRow * 2) + cnt_lane + 4, 1u);
@@ -459,13 +477,17 @@ __device__ __forceinline__ void quantise_window_delta(const unsigned char *box, 
 // DELTA: the token-locality delta [CG §1.2(1)] with groups of d.G tokens; the
 // anchors' max1 comes from a pre-pass over the anchor rows (plain loads of
 // kin / vin), then pass 1 takes max |x - a^| per row and step 2 quantises d.
-template <bool V2, bool DELTA>
-__global__ void __launch_bounds__(kNT, 3) k_compress_tma(
+template <bool V2, bool DELTA, int AM>
+__global__ void __launch_bounds__(kNT, AM <= 32 ? 3 : 2) k_compress_tma(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const uint16_t *kin,
     const uint16_t *vin, Dims d, MaxTab mt, int box_rows, uint16_t *__restrict__ max1_out,
     void *__restrict__ side_out, uint8_t *__restrict__ stage, uint32_t *__restrict__ len,
     unsigned long long *state, int32_t *status) {
-    __shared__ __align__(1024) unsigned char s_union[kUnionBytes];
+    using AL = Alpha<AM>;
+    // the union: static for 32-symbol alphabets (its addresses are constants);
+    // for 64 it is larger than static shared memory may be and follows the box
+    // buffer in dynamic shared memory
+    __shared__ __align__(1024) unsigned char s_union_st[AM <= 32 ? AL::union_bytes : 16];
     __shared__ unsigned long long s_scan[kNW + 4];
     __shared__ unsigned long long s_bar[2];
     __shared__ float s_fac[kNT];
@@ -479,10 +501,15 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     __shared__ float s_unitc[DELTA ? 64 : 1];
     extern __shared__ __align__(128) unsigned char dsm[];
 
+    unsigned char *s_union = s_union_st;
+    if constexpr (AM > 32) {
+        const uint32_t dy = smem_u32(dsm);
+        s_union = dsm + ((((dy + 127u) & ~127u) + (uint32_t)box_rows * (kW * 2) + 1023u) & ~1023u) - dy;
+    }
     uint2 *cdfw = reinterpret_cast<uint2 *>(s_union);
-    uint16_t *cnt16 = reinterpret_cast<uint16_t *>(s_union + kCdfwBytes);
-    uint32_t *cnt32 = reinterpret_cast<uint32_t *>(s_union + kCdfwBytes);
-    uint8_t *sym = s_union + kCdfwBytes + kCntBytes;
+    uint16_t *cnt16 = reinterpret_cast<uint16_t *>(s_union + AL::cdfw_bytes);
+    uint32_t *cnt32 = reinterpret_cast<uint32_t *>(s_union + AL::cdfw_bytes);
+    uint8_t *sym = s_union + AL::cdfw_bytes + AL::cnt_bytes;
     const uint32_t dyn = smem_u32(dsm);
     const uint32_t buf0 = (dyn + 127u) & ~127u;  // box buffer 0 (dynamic, 128-byte aligned)
     const uint32_t buf1 = smem_u32(s_union);     // box buffer 1 (max1 pass only)
@@ -566,7 +593,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     // read back by the rows of its group; otherwise each row recomputes its
     // anchor's quad.
     const int na = DELTA ? (Tk + d.G - 1) / d.G : 0;
-    const bool ahat_shared = DELTA && na * (kW * 4) <= kUnionBytes - (int)box_bytes;
+    const bool ahat_shared = DELTA && na * (kW * 4) <= AL::union_bytes - (int)box_bytes;
     float4 *ahat = reinterpret_cast<float4 *>(s_union + box_bytes);
     uint32_t ph0 = 0, ph1 = 0;
     uint32_t mx[16];
@@ -664,7 +691,7 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
     }
     for (int n = tid; n <= Tk; n += kNT)
         s_ftab[n] = (uint16_t)(1u + ((uint32_t)n * (kTotal - (uint32_t)A)) / (uint32_t)Tk);
-    for (int i = tid; i < kCntBytes / 4; i += kNT) cnt32[i] = 0;
+    for (int i = tid; i < AL::cnt_bytes / 4; i += kNT) cnt32[i] = 0;
     nonfinite = __syncthreads_or(nonfinite) != 0;
     if (tid < Tk) {
         const unsigned mb = s_m1[tid];
@@ -686,19 +713,20 @@ __global__ void __launch_bounds__(kNT, 3) k_compress_tma(
         if (4 * kq < Wc) {
             // a box that did not arrive in time holds stale values: clamp those too
             if (DELTA)
-                quantise_window_delta(box0, s_fac, s_anchor, s_m1, us, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                quantise_window_delta<AL::SH>(box0, s_fac, s_anchor, s_m1, us, sym, cnt_lane, rbase, kq, Tk, fm, mg,
+                                              qmax);
             else if (nonfinite || timed_out)
-                quantise_window<true>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                quantise_window<true, AL::SH>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
             else
-                quantise_window<false>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                quantise_window<false, AL::SH>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
         }
         __syncthreads();
         if (tid == 0 && w + 1 < nwin) tma_load(buf0, tm, c0 + kW, t0, l, bar0, box_bytes);
         // 3. CDF rows: thread (channel c, part p) owns symbols 8p .. 8p + 7
-        build_cdf_window<V2>(tid, cnt16, s_ftab, cdfw, side_out, side_base, c0, Wc, A);
+        build_cdf_window<V2, 1, AM>(tid, cnt16, s_ftab, cdfw, side_out, side_base, c0, Wc, A);
         __syncthreads();
         // 4. code my token's symbols of this window
-        if (tid < Tk) encode_window(e, stream, sym + tid * kSymRow, cdfw, Wc);
+        if (tid < Tk) encode_window<AM>(e, stream, sym + tid * kSymRow, cdfw, Wc);
     }
 
     // 5. stream lengths and the slice's total (offsets and packing follow in
@@ -1202,7 +1230,7 @@ bool compress_fused_applies(const Dims &d, const uint16_t *k, const uint16_t *v)
     const int A = d.A[0] > d.A[1] ? d.A[0] : d.A[1];
     const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0 &&
                          d.layer_stride % 8 == 0;
-    return d.T > 0 && tmax <= kNT && A <= kAmax && d.C % 8 == 0 && aligned;
+    return d.T > 0 && tmax <= kNT && A <= 64 && d.C % 8 == 0 && aligned;
 }
 
 cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Dims &d, const MaxTab &mt,
@@ -1217,7 +1245,15 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
     const long long nslices = 2LL * d.L * d.nch;
     cudaError_t err;
     const int sms = device_sm_count();
-    if (d.G == 1 && sms > 0 && nslices <= sms) {
+    // the largest alphabet the kernel codes: the tensors' (format 1) or the
+    // largest layer alphabet 2 MAX + 1 (format 2)
+    int amax = d.A[0] > d.A[1] ? d.A[0] : d.A[1];
+    if (v2) {
+        amax = 0;
+        for (int kv = 0; kv < 2; kv++)
+            for (int l = 0; l < d.L; l++) amax = 2 * mt.v[kv][l] + 1 > amax ? 2 * mt.v[kv][l] + 1 : amax;
+    }
+    if (d.G == 1 && sms > 0 && nslices <= sms && amax <= 32) {
         // latency mode: coders and producers per slice, one slice per SM (or a
         // cluster of two CTAs per slice, one slice per two SMs); the slice
         // totals go to state[2 + nslices ..], which the packing reads directly
@@ -1259,9 +1295,18 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
     }
     k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
     {
-        const int dyn = 128 + box_rows * kW * 2;
-        auto kern = d.G > 1 ? (v2 ? k_compress_tma<true, true> : k_compress_tma<false, true>)
-                            : (v2 ? k_compress_tma<true, false> : k_compress_tma<false, false>);
+        // AM = 64: the union follows the box buffer (1024-byte aligned)
+        const int dyn = amax <= 32 ? 128 + box_rows * kW * 2
+                                   : 128 + ((box_rows * kW * 2 + 1023) & ~1023) + Alpha<64>::union_bytes + 1024;
+        using Kern = void (*)(const CUtensorMap, const CUtensorMap, const uint16_t *, const uint16_t *, Dims, MaxTab,
+                              int, uint16_t *, void *, uint8_t *, uint32_t *, unsigned long long *, int32_t *);
+        Kern kern;
+        if (amax <= 32)
+            kern = d.G > 1 ? (v2 ? k_compress_tma<true, true, 32> : k_compress_tma<false, true, 32>)
+                           : (v2 ? k_compress_tma<true, false, 32> : k_compress_tma<false, false, 32>);
+        else
+            kern = d.G > 1 ? (v2 ? k_compress_tma<true, true, 64> : k_compress_tma<false, true, 64>)
+                           : (v2 ? k_compress_tma<true, false, 64> : k_compress_tma<false, false, 64>);
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
         if (err != cudaSuccess) return err;
         err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

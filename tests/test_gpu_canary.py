@@ -64,7 +64,8 @@ def _case(synth_mod, name):
     rng = np.random.default_rng(len(name) + 7)
     shapes = {"ragged": (3, 150, 40, 64, [32, 16, 8], [4, 16, 255]),   # wide alphabet: the step path
               "odd_c": (2, 70, 13, 64, [16, 32], [8, 33]),             # C % 8 != 0: the step path
-              "long_chunk": (2, 1300, 24, 600, [255, 16], [32, 8])}    # chunks of 600 tokens, format 1
+              "long_chunk": (2, 1300, 24, 600, [255, 16], [32, 8]),    # chunks of 600 tokens, format 1
+              "bins64": (3, 300, 136, 256, [64, 40, 16], [33, 64, 8])}  # the 64-symbol fused kernel
     L, T, C_, Tc, bk, bv = shapes[name]
     k = (rng.standard_normal((L, T, C_)) * rng.lognormal(0, 0.5, (1, 1, C_))).astype(np.float16)
     v = rng.standard_t(3, size=(L, T, C_)).astype(np.float16)
@@ -102,7 +103,7 @@ def _guard_codec(cd):
 
 CASES = [("tiny", 1, 1), ("tiny", 2, 1), ("tiny", 3, 1), ("mistral_chunk", 2, 1), ("mistral_chunk", 2, 10),
          ("mistral_chunk", 3, 10), ("mistral_chunk", 1, 4), ("ragged", 1, 1), ("ragged", 2, 1), ("odd_c", 2, 1),
-         ("odd_c", 3, 10), ("long_chunk", 1, 1)]
+         ("odd_c", 3, 10), ("long_chunk", 1, 1), ("bins64", 1, 1), ("bins64", 2, 10)]
 
 
 @pytest.mark.parametrize("name,fmt,group", CASES)

@@ -66,6 +66,7 @@ FUSED_CASES = {
     "g3_tc256": (2, 520, 128, 256, [16, 16], [32, 32], 3),
     "g256": (1, 256, 64, 256, [32], [16], 256),
     "g2_t1": (2, 1, 16, 64, [16, 8], [8, 16], 2),
+    "g10_bins64": (2, 300, 136, 256, [64, 34], [48, 16], 10),  # the fused kernel's 64-symbol form
 }
 
 

@@ -72,7 +72,7 @@ def _synth(synth_mod, name, T=None):
 
 
 CASES = ["tiny", "ragged", "c48_tc32_bins256", "c24_tc70", "c8_t1", "c16_tc1", "mistral_chunk",
-         "uniform", "c24_tc600_bins255"]
+         "uniform", "c24_tc600_bins255", "c136_bins64"]
 
 
 def make_case(name, synth_mod):
@@ -90,6 +90,8 @@ def make_case(name, synth_mod):
         return _shape_case(1, 5, 16, 1, [32], [32], 4)
     if name == "c24_tc600_bins255":  # chunks longer than 256 tokens (600, 600, then a ragged 100)
         return _shape_case(2, 1300, 24, 600, [255, 16], [32, 8], 5)
+    if name == "c136_bins64":  # alphabets 33 .. 64: the fused kernel's 64-symbol form (a ragged last chunk)
+        return _shape_case(3, 300, 136, 256, [64, 40, 16], [33, 64, 8], 6)
     raise KeyError(name)
 
 

@@ -33,14 +33,16 @@ def _case(synth_mod, name):
               "tc1": (1, 5, 16, 1, [32], [32]),
               # past the fused kernel: alphabets up to 255 symbols, C % 8 != 0
               "wide_bins": (3, 300, 40, 128, [256, 64, 255], [128, 34, 4]),
-              "odd_c": (2, 70, 13, 64, [16, 32], [8, 4])}
+              "odd_c": (2, 70, 13, 64, [16, 32], [8, 4]),
+              # the fused kernel's 64-symbol form: layer alphabets 33 .. 63 (bins up to 65)
+              "bins65": (3, 300, 136, 256, [65, 48, 16], [34, 64, 8])}
     L, T, C_, Tc, bk, bv = shapes[name]
     k = (rng.standard_normal((L, T, C_)) * rng.lognormal(0, 0.5, (1, 1, C_))).astype(np.float16)
     v = (rng.standard_normal((L, T, C_)) * 0.5).astype(np.float16)
     return k, v, Tc, bk, bv
 
 
-CASES = ["tiny", "ragged", "odd_bins", "t1", "tc1", "wide_bins", "odd_c", "mistral_chunk", "uniform"]
+CASES = ["tiny", "ragged", "odd_bins", "t1", "tc1", "wide_bins", "odd_c", "bins65", "mistral_chunk", "uniform"]
 
 
 @pytest.mark.parametrize("case", CASES + [pytest.param("ctx4096", marks=pytest.mark.slow)])
