@@ -248,10 +248,10 @@ uint64_t cg_record_bytes(const cg_shape *shape, const int32_t *bins_k,
 /* cg_compress_chunk in format 2: max1 as in format 1, rec gets the count
  * records (cg_record_bytes bytes), packed/len/off the streams coded with the
  * per-layer CDFs. Workspace: cg_compress_workspace_bytes. Any bins in
- * [4, 256] and any C; requires chunk_tokens <= 256. (Every bins <= 33 with
- * C % 8 == 0, k and v 16-byte aligned and layer_stride % 8 == 0 takes one
- * fused kernel; other shapes take the quantise, count-and-code and pack
- * steps, with the same output.) */
+ * [4, 256] and any C; requires chunk_tokens <= 256. (Every layer alphabet
+ * 2 MAX + 1 <= 64 (bins <= 65) with C % 8 == 0, k and v 16-byte aligned and
+ * layer_stride % 8 == 0 takes one fused kernel; other shapes take the
+ * quantise, count-and-code and pack steps, with the same output.) */
 cg_status cg_compress_chunk_v2(const uint16_t *k, const uint16_t *v,
                                const cg_shape *shape, const int32_t *bins_k,
                                const int32_t *bins_v, uint16_t *max1,

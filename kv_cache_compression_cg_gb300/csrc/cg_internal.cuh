@@ -72,9 +72,10 @@ __host__ __device__ inline long long cdf_slice_offset(const Dims &d, int k, int 
 // Format 2: byte offset of the count records of slice (k, kv, l). Records of
 // a chunk are K layer 0 [C][A_0], layer 1 [C][A_1], ..., then V, with
 // A_j = 2 * MAX_j + 1. Every thread of the CTA calls this (block reduction
-// over the layers; two barriers); every thread gets the offset.
-__device__ __forceinline__ long long record_slice_offset(const Dims &d, const MaxTab &mt, int k, int kv, int l) {
-    __shared__ unsigned long long red[3 * 32];
+// over the layers; two barriers); every thread gets the offset. red is
+// shared scratch of 3 * (warps) words, free again when this returns.
+__device__ __forceinline__ long long record_slice_offset(const Dims &d, const MaxTab &mt, int k, int kv, int l,
+                                                         unsigned long long *red) {
     unsigned long long tk = 0, tv = 0, pre = 0;
     for (int j = threadIdx.x; j < d.L; j += blockDim.x) {
         const unsigned long long ak = 2ull * mt.v[0][j] + 1, av = 2ull * mt.v[1][j] + 1;
@@ -103,6 +104,11 @@ __device__ __forceinline__ long long record_slice_offset(const Dims &d, const Ma
     }
     __syncthreads();
     return (long long)d.C * ((long long)k * (long long)(tk + tv) + (kv ? (long long)tk : 0LL) + (long long)pre);
+}
+
+__device__ __forceinline__ long long record_slice_offset(const Dims &d, const MaxTab &mt, int k, int kv, int l) {
+    __shared__ unsigned long long red[3 * 32];
+    return record_slice_offset(d, mt, k, kv, l, red);
 }
 
 // Symbols [2][L][T][C] and max1 [2][L][T].

@@ -119,6 +119,30 @@ __device__ __forceinline__ void enc_symbol_lf(Enc &e, uint32_t lo, uint32_t f) {
         : "r"(lo), "r"(f));
 }
 
+// The same step with the entry packed as lo | (f - 1) << 16, which holds every
+// f up to 65536: range = r (f - 1) + r.
+__device__ __forceinline__ void enc_symbol_m1(Enc &e, uint32_t entry) {
+    asm("{\n\t"
+        ".reg .u32 r, lo, fm, sh;\n\t"
+        "shr.b32 r, %1, 16;\n\t"
+        "and.b32 lo, %5, 65535;\n\t"
+        "shr.b32 fm, %5, 16;\n\t"
+        "mad.lo.cc.u32 %0, r, lo, %0;\n\t"
+        "addc.cc.u32 %2, %2, 0;\n\t"
+        "addc.u32 %3, %3, 0;\n\t"
+        "mad.lo.u32 %1, r, fm, r;\n\t"
+        "clz.b32 sh, %1;\n\t"
+        "and.b32 sh, sh, 24;\n\t"
+        "shf.l.clamp.b32 %3, %2, %3, sh;\n\t"
+        "shf.l.clamp.b32 %2, %0, %2, sh;\n\t"
+        "shl.b32 %0, %0, sh;\n\t"
+        "shl.b32 %1, %1, sh;\n\t"
+        "add.u32 %4, %4, sh;\n\t"
+        "}"
+        : "+r"(e.low), "+r"(e.range), "+r"(e.alo), "+r"(e.ahi), "+r"(e.nbits)
+        : "r"(entry));
+}
+
 // Flush byte and final words; returns the stream length in bytes.
 __device__ __forceinline__ uint32_t enc_finish(Enc &e, uint8_t *stream) {
     if (e.nbits >= 32) enc_flush_word(e, stream);

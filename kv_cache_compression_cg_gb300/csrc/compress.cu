@@ -72,16 +72,18 @@ constexpr int kCodeBytes = kCdfwBytes + kCntBytes + kSymBytes;
 constexpr int kUnionBytes = kCodeBytes > kBoxBytesMax ? kCodeBytes : kBoxBytesMax;
 
 // Sizes of the throughput kernel for alphabets up to AM symbols (32, or 64 for
-// layers of up to 64 bins, format 1, or 65, format 2): rows of AM + 1 (lo, f)
-// entries, AM / 4 symbols per CDF thread, an AM-row counter table. Tile bytes
-// hold q << SH, an offset into a row of 8-byte entries that fits a byte
-// (8q for q < 32; 4q, doubled on use, for q < 64).
+// layers of up to 64 bins, format 1, or 65, format 2): rows of AM + 1 CDF
+// entries, AM / 4 symbols per CDF thread, an AM-row counter table. An entry is
+// (lo, f) as two words for 32 symbols, one word lo | (f - 1) << 16 for 64 (so
+// that three CTAs fit an SM). Tile bytes hold q << SH, the byte offset of the
+// entry in its row (8q for q < 32, 4q for q < 64).
 template <int AM>
 struct Alpha {
     static constexpr int AS = AM + 1;
     static constexpr int SP = AM / 4;
     static constexpr int SH = AM <= 32 ? 3 : 2;
-    static constexpr int cdfw_bytes = kW * AS * 8;
+    static constexpr int EB = 1 << SH;  // bytes per CDF entry
+    static constexpr int cdfw_bytes = kW * AS * EB;
     static constexpr int cnt_bytes = AM * kCntRow * 2;
     static constexpr int code_bytes = cdfw_bytes + cnt_bytes + kSymBytes;
     static constexpr int union_bytes = code_bytes > kBoxBytesMax ? code_bytes : kBoxBytesMax;
@@ -283,7 +285,9 @@ __global__ void k_compress_init(unsigned long long *state, long long nslices) {
 // the symbol tile and count q. SAFE (a slice with a non-finite max1, or a box
 // whose wait ran out) clamps q to [0, 2 MAX] before using it; finite input
 // under its own max1 needs no clamp.
-template <bool SAFE, int SH = 3>
+// fac[r * FS] is row r's factor (FS = 17: the factors sit in the symbol tile's
+// row padding).
+template <bool SAFE, int SH = 3, int FS = 1>
 __device__ __forceinline__ void quantise_window(const unsigned char *box, const float *fac, uint8_t *sym,
                                                 uint32_t cnt_lane, int rbase, int kq, int Tk,
                                                 unsigned long long fm, unsigned long long mg, uint32_t qmax) {
@@ -292,7 +296,7 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
         const int r = rbase + 2 * i;
         if (r >= Tk) break;
         const uint2 x = *reinterpret_cast<const uint2 *>(box + r * (kW * 2) + 8 * kq);
-        const float f = fac[r];
+        const float f = fac[r * FS];
         uint32_t b0, b1, b2, b3;
         quant_pair(x.x, f, fm, mg, b0, b1);
         quant_pair(x.y, f, fm, mg, b2, b3);
@@ -321,7 +325,7 @@ __device__ __forceinline__ void quantise_window(const unsigned char *box, const 
 // distributed shared memory; the other table (the last window's, which both
 // CTAs have read) is cleared instead; only rank 0 writes the side output.
 template <bool V2, int NC = 1, int AM = kAmax>
-__device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const uint16_t *ftab, uint2 *cdfw,
+__device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const uint16_t *ftab, void *cdfw,
                                                  void *side_out, long long side_base, int c0, int Wc, int A,
                                                  int tb = 0, uint32_t rank = 0) {
     constexpr int kSP = Alpha<AM>::SP;
@@ -367,8 +371,14 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
     const uint32_t base = incl - sum;
     const uint32_t best = 255u - (key & 255u);
     const uint32_t extra = kTotal - total;
-    uint2 *row = cdfw + c * kAS;
+    unsigned char *row = static_cast<unsigned char *>(cdfw) + c * kAS * Alpha<AM>::EB;
     const bool out = NC == 1 || rank == 0;
+    auto put = [&](uint32_t s, uint32_t lo, uint32_t f) {
+        if constexpr (Alpha<AM>::EB == 8)
+            reinterpret_cast<uint2 *>(row)[s] = make_uint2(lo, f);
+        else
+            reinterpret_cast<uint32_t *>(row)[s] = lo | ((f - 1u) << 16);
+    };
     if (V2) {
         // count record: the mode, then the other symbols' counts
         uint8_t *g = static_cast<uint8_t *>(side_out) + side_base + (long long)(c0 + c) * A;
@@ -379,7 +389,7 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
             if ((int)s < A) {
                 const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
                 const uint32_t f = fj[j] + (s == best ? extra : 0u);
-                row[s] = make_uint2(lo, f);
+                put(s, lo, f);
                 if (s != best && out) g[s + (s < best ? 1u : 0u)] = (uint8_t)((nb[j / 4] >> (8 * (j % 4))) & 0xFFu);
             }
         }
@@ -391,44 +401,61 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
             if ((int)s < A) {
                 const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
                 const uint32_t f = fj[j] + (s == best ? extra : 0u);
-                row[s] = make_uint2(lo, f);
+                put(s, lo, f);
                 if (out) g[s] = (uint16_t)lo;
             }
         }
     }
 }
 
-// Step 4 for one window: code this thread's row of the symbol tile (bytes 8q)
-// with the window's (lo, f) rows.
+// Step 4 for one window: code this thread's row of the symbol tile (bytes
+// q << SH) with the window's CDF rows: two-word (lo, f) entries for 32 symbols,
+// one-word lo | (f - 1) << 16 entries for 64.
+template <int AM>
+__device__ __forceinline__ uint2 ld_entry(const unsigned char *at) {
+    if constexpr (Alpha<AM>::EB == 8)
+        return *reinterpret_cast<const uint2 *>(at);
+    else
+        return make_uint2(*reinterpret_cast<const uint32_t *>(at), 0u);
+}
+
+template <int AM>
+__device__ __forceinline__ void enc_entry(Enc &e, uint2 en) {
+    if constexpr (Alpha<AM>::EB == 8)
+        enc_symbol_lf(e, en.x, en.y);
+    else
+        enc_symbol_m1(e, en.x);
+}
+
 template <int AM = kAmax>
-__device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uint8_t *symrow, const uint2 *cdfw,
+__device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uint8_t *symrow, const void *cdfw,
                                               int Wc) {
-    constexpr int kAS = Alpha<AM>::AS;
-    constexpr uint32_t U = 1u << (3 - Alpha<AM>::SH);  // tile byte -> byte offset of the (lo, f) entry
-    const unsigned char *rows = reinterpret_cast<const unsigned char *>(cdfw);
+    constexpr int kRow = Alpha<AM>::AS * Alpha<AM>::EB;  // bytes per CDF row
+    const unsigned char *rows = static_cast<const unsigned char *>(cdfw);
     if (Wc == kW) {
 #pragma unroll
         for (int g = 0; g < kW / 4; g++) {
-            // every tile byte is 8q (q <= 30, written by the quantiser), an aligned
-            // (lo, f) offset in its row: byte loads, no unpacking
+            // every tile byte is q << SH (written by the quantiser), the aligned
+            // offset of q's entry in its row: byte loads, no unpacking
             const unsigned char *m4 = symrow + 4 * g;
-            const unsigned char *r0 = rows + (4 * g) * kAS * 8;
-            const uint2 e0 = *reinterpret_cast<const uint2 *>(r0 + U * m4[0]);
-            const uint2 e1 = *reinterpret_cast<const uint2 *>(r0 + kAS * 8 + U * m4[1]);
-            const uint2 e2 = *reinterpret_cast<const uint2 *>(r0 + 2 * kAS * 8 + U * m4[2]);
-            const uint2 e3 = *reinterpret_cast<const uint2 *>(r0 + 3 * kAS * 8 + U * m4[3]);
+            const unsigned char *r0 = rows + (4 * g) * kRow;
+            // (the four entries are loaded ahead of the flush's stores)
+            const uint2 e0 = ld_entry<AM>(r0 + m4[0]);
+            const uint2 e1 = ld_entry<AM>(r0 + kRow + m4[1]);
+            const uint2 e2 = ld_entry<AM>(r0 + 2 * kRow + m4[2]);
+            const uint2 e3 = ld_entry<AM>(r0 + 3 * kRow + m4[3]);
             if (e.nbits >= 32) enc_flush_word(e, stream);
-            enc_symbol_lf(e, e0.x, e0.y);
-            enc_symbol_lf(e, e1.x, e1.y);
+            enc_entry<AM>(e, e0);
+            enc_entry<AM>(e, e1);
             if (e.nbits >= 32) enc_flush_word(e, stream);
-            enc_symbol_lf(e, e2.x, e2.y);
-            enc_symbol_lf(e, e3.x, e3.y);
+            enc_entry<AM>(e, e2);
+            enc_entry<AM>(e, e3);
         }
     } else {
         for (int c = 0; c < Wc; c++) {
-            const uint2 en = *reinterpret_cast<const uint2 *>(rows + c * kAS * 8 + U * (symrow[c] & (0xFFu << Alpha<AM>::SH)));
+            const uint2 en = ld_entry<AM>(rows + c * kRow + (symrow[c] & (0xFFu << Alpha<AM>::SH)));
             if (e.nbits >= 32) enc_flush_word(e, stream);
-            enc_symbol_lf(e, en.x, en.y);
+            enc_entry<AM>(e, en);
         }
     }
 }
@@ -478,20 +505,19 @@ __device__ __forceinline__ void quantise_window_delta(const unsigned char *box, 
 // anchors' max1 comes from a pre-pass over the anchor rows (plain loads of
 // kin / vin), then pass 1 takes max |x - a^| per row and step 2 quantises d.
 template <bool V2, bool DELTA, int AM>
-__global__ void __launch_bounds__(kNT, AM <= 32 ? 3 : 2) k_compress_tma(
+__global__ void __launch_bounds__(kNT, AM <= 32 || !DELTA ? 3 : 2) k_compress_tma(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const uint16_t *kin,
     const uint16_t *vin, Dims d, MaxTab mt, int box_rows, uint16_t *__restrict__ max1_out,
     void *__restrict__ side_out, uint8_t *__restrict__ stage, uint32_t *__restrict__ len,
     unsigned long long *state, int32_t *status) {
     using AL = Alpha<AM>;
-    // the union: static for 32-symbol alphabets (its addresses are constants);
-    // for 64 it is larger than static shared memory may be and follows the box
-    // buffer in dynamic shared memory
-    __shared__ __align__(1024) unsigned char s_union_st[AM <= 32 ? AL::union_bytes : 16];
+    // 64 symbols without the delta: the row factors sit in the symbol tile's
+    // row padding and max1 in the CDF rows until the coding starts, so that
+    // three CTAs fit an SM
+    constexpr bool kLean = AM > 32 && !DELTA;
+    constexpr int FS = kLean ? kSymRow / 4 : 1;  // float stride of the row factors
     __shared__ unsigned long long s_scan[kNW + 4];
     __shared__ unsigned long long s_bar[2];
-    __shared__ float s_fac[kNT];
-    __shared__ uint16_t s_m1[kNT];
     __shared__ uint16_t s_ftab[kNT + 2];
     __shared__ int s_ticket;
     // the delta: each row's anchor row and the table (q - MAX) / MAX (an
@@ -501,15 +527,31 @@ __global__ void __launch_bounds__(kNT, AM <= 32 ? 3 : 2) k_compress_tma(
     __shared__ float s_unitc[DELTA ? 64 : 1];
     extern __shared__ __align__(128) unsigned char dsm[];
 
-    unsigned char *s_union = s_union_st;
-    if constexpr (AM > 32) {
+    // the union: static for 32-symbol alphabets (its addresses are constants);
+    // for 64 it follows the box buffer in dynamic shared memory
+    unsigned char *s_union;
+    if constexpr (AM <= 32) {
+        __shared__ __align__(1024) unsigned char s_union_st[AL::union_bytes];
+        s_union = s_union_st;
+    } else {
         const uint32_t dy = smem_u32(dsm);
-        s_union = dsm + ((((dy + 127u) & ~127u) + (uint32_t)box_rows * (kW * 2) + 1023u) & ~1023u) - dy;
+        s_union = dsm + (((dy + 127u) & ~127u) + (uint32_t)box_rows * (kW * 2)) - dy;
     }
-    uint2 *cdfw = reinterpret_cast<uint2 *>(s_union);
+    unsigned char *cdfw = s_union;
     uint16_t *cnt16 = reinterpret_cast<uint16_t *>(s_union + AL::cdfw_bytes);
     uint32_t *cnt32 = reinterpret_cast<uint32_t *>(s_union + AL::cdfw_bytes);
     uint8_t *sym = s_union + AL::cdfw_bytes + AL::cnt_bytes;
+    float *s_fac;
+    uint16_t *s_m1;
+    if constexpr (kLean) {
+        s_fac = reinterpret_cast<float *>(sym + kW);
+        s_m1 = reinterpret_cast<uint16_t *>(s_union);
+    } else {
+        __shared__ float s_fac_st[kNT];
+        __shared__ uint16_t s_m1_st[kNT];
+        s_fac = s_fac_st;
+        s_m1 = s_m1_st;
+    }
     const uint32_t dyn = smem_u32(dsm);
     const uint32_t buf0 = (dyn + 127u) & ~127u;  // box buffer 0 (dynamic, 128-byte aligned)
     const uint32_t buf1 = smem_u32(s_union);     // box buffer 1 (max1 pass only)
@@ -535,7 +577,9 @@ __global__ void __launch_bounds__(kNT, AM <= 32 ? 3 : 2) k_compress_tma(
     const int t0 = k * d.Tc;
     const int nwin = (d.C + kW - 1) / kW;
     const uint32_t box_bytes = (uint32_t)box_rows * (kW * 2);
-    const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l) : cdf_slice_offset(d, k, kv, l);
+    // (the union is free until the first boxes are asked for)
+    const long long side_base = V2 ? record_slice_offset(d, mt, k, kv, l, reinterpret_cast<unsigned long long *>(s_union))
+                                   : cdf_slice_offset(d, k, kv, l);
     const long long sid0 = chunk_stream_base(d, k) + ((long long)kv * d.L + l) * Tk;
     const long long sid = sid0 + tid;
     uint8_t *stream = stage_stream(stage, tid < Tk ? sid : sid0, d);
@@ -695,7 +739,7 @@ __global__ void __launch_bounds__(kNT, AM <= 32 ? 3 : 2) k_compress_tma(
     nonfinite = __syncthreads_or(nonfinite) != 0;
     if (tid < Tk) {
         const unsigned mb = s_m1[tid];
-        s_fac[tid] = mb ? __fdiv_rn(fmax, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
+        s_fac[tid * FS] = mb ? __fdiv_rn(fmax, __half2float(__ushort_as_half((unsigned short)mb))) : 0.0f;
     }
     __syncthreads();
 
@@ -716,9 +760,9 @@ __global__ void __launch_bounds__(kNT, AM <= 32 ? 3 : 2) k_compress_tma(
                 quantise_window_delta<AL::SH>(box0, s_fac, s_anchor, s_m1, us, sym, cnt_lane, rbase, kq, Tk, fm, mg,
                                               qmax);
             else if (nonfinite || timed_out)
-                quantise_window<true, AL::SH>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                quantise_window<true, AL::SH, FS>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
             else
-                quantise_window<false, AL::SH>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
+                quantise_window<false, AL::SH, FS>(box0, s_fac, sym, cnt_lane, rbase, kq, Tk, fm, mg, qmax);
         }
         __syncthreads();
         if (tid == 0 && w + 1 < nwin) tma_load(buf0, tm, c0 + kW, t0, l, bar0, box_bytes);
@@ -987,6 +1031,50 @@ __global__ void __launch_bounds__(kNT / NC + kNT, 1) k_compress_lm(
     }
 }
 
+// Copy one staged stream (n bytes; this lane's first word already loaded)
+// to byte position dst of the packed buffer, a warp per stream, lane i taking
+// the words i, i + 32, ... For streams past 128 bytes a full word goes out as
+// one, two or three stores by the destination's alignment (the same for
+// every word of the stream); the last word, and every word of shorter streams,
+// byte by byte.
+__device__ __forceinline__ void copy_stream(const uint8_t *src, uint32_t n, unsigned long long dst, uint8_t *packed,
+                                            unsigned long long capacity, uint32_t first, int lane) {
+    if (n > 128u) {
+        const uint32_t al = (uint32_t)((reinterpret_cast<uintptr_t>(packed) + dst) & 3u);
+        for (uint32_t b = 4u * lane; b < n; b += 128u) {
+            const uint32_t wv = b < 128u ? first : *reinterpret_cast<const uint32_t *>(src + b);
+            const unsigned long long pos = dst + b;
+            if (b + 4u <= n && pos + 4u <= capacity) {
+                uint8_t *pp = packed + pos;
+                if (al == 0) {
+                    *reinterpret_cast<uint32_t *>(pp) = wv;
+                } else if (al == 2) {
+                    reinterpret_cast<uint16_t *>(pp)[0] = (uint16_t)wv;
+                    reinterpret_cast<uint16_t *>(pp)[1] = (uint16_t)(wv >> 16);
+                } else {
+                    pp[0] = (uint8_t)wv;
+                    *reinterpret_cast<uint16_t *>(pp + 1) = (uint16_t)(wv >> 8);
+                    pp[3] = (uint8_t)(wv >> 24);
+                }
+            } else {
+                const uint32_t nb = min(4u, n - b);
+#pragma unroll
+                for (uint32_t q = 0; q < 4; q++)
+                    if (q < nb && pos + q < capacity) packed[pos + q] = (uint8_t)(wv >> (8 * q));
+            }
+        }
+    } else {
+        for (uint32_t b = 4u * lane; b < n; b += 128u) {
+            const uint32_t nb = min(4u, n - b);
+#pragma unroll
+            for (uint32_t q = 0; q < 4; q++) {
+                const unsigned long long pos = dst + b + q;
+                if (q < nb && pos < capacity) packed[pos] = (uint8_t)(first >> (8 * q));
+            }
+        }
+    }
+}
+
 // Offsets and packing: CTA per slice in stream order (by ticket). Every
 // slice's byte total is known when this kernel starts, so each CTA publishes
 // its aggregate at once and its decoupled look-back (32 predecessors per step,
@@ -1092,15 +1180,7 @@ __global__ void __launch_bounds__(kNT) k_pack(Dims d, const uint8_t *__restrict_
             const uint32_t n = s_len[t];
             const unsigned long long dst = sbase + s_loc[t];
             const uint8_t *src = stage_stream(const_cast<uint8_t *>(stage), sid0 + t, d);
-            for (uint32_t b = 4u * lane; b < n; b += 128u) {
-                const uint32_t wv = b < 128u ? held[u] : *reinterpret_cast<const uint32_t *>(src + b);
-                const uint32_t nb = min(4u, n - b);
-#pragma unroll
-                for (uint32_t q = 0; q < 4; q++) {
-                    const unsigned long long pos = dst + b + q;
-                    if (q < nb && pos < capacity) packed[pos] = (uint8_t)(wv >> (8 * q));
-                }
-            }
+            copy_stream(src, n, dst, packed, capacity, held[u], lane);
         }
     }
     if (timed_out && status && lane == 0) atomicOr(status, CG_FLAG_TIMEOUT);
@@ -1178,15 +1258,7 @@ __global__ void __launch_bounds__(kNT, 4) k_pack_lm(Dims d, const uint8_t *__res
             const uint32_t n = s_len[t];
             const unsigned long long dst = sbase + s_loc[t];
             const uint8_t *src = stage_stream(const_cast<uint8_t *>(stage), sid0 + t, d);
-            for (uint32_t bb = 4u * lane; bb < n; bb += 128u) {
-                const uint32_t wv = bb < 128u ? held[u] : *reinterpret_cast<const uint32_t *>(src + bb);
-                const uint32_t nb = min(4u, n - bb);
-#pragma unroll
-                for (uint32_t q = 0; q < 4; q++) {
-                    const unsigned long long pos = dst + bb + q;
-                    if (q < nb && pos < capacity) packed[pos] = (uint8_t)(wv >> (8 * q));
-                }
-            }
+            copy_stream(src, n, dst, packed, capacity, held[u], lane);
         }
     }
 }
@@ -1295,9 +1367,9 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
     }
     k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);
     {
-        // AM = 64: the union follows the box buffer (1024-byte aligned)
+        // AM = 64: the union follows the box buffer
         const int dyn = amax <= 32 ? 128 + box_rows * kW * 2
-                                   : 128 + ((box_rows * kW * 2 + 1023) & ~1023) + Alpha<64>::union_bytes + 1024;
+                                   : 128 + box_rows * kW * 2 + Alpha<64>::union_bytes;
         using Kern = void (*)(const CUtensorMap, const CUtensorMap, const uint16_t *, const uint16_t *, Dims, MaxTab,
                               int, uint16_t *, void *, uint8_t *, uint32_t *, unsigned long long *, int32_t *);
         Kern kern;
