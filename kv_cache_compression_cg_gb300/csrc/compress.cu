@@ -395,15 +395,30 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
         }
     } else {
         uint16_t *g = static_cast<uint16_t *>(side_out) + side_base + (long long)(c0 + c) * A;
+        // rows of a multiple of 8 entries (C % 8 == 0, so every row and every
+        // thread's part of one starts 16-byte aligned): the part leaves as
+        // 16-byte stores instead of one store per entry
+        const bool vec = (A & 7) == 0 && (reinterpret_cast<uintptr_t>(side_out) & 15) == 0;
+        uint32_t pk[kSP / 2];
 #pragma unroll
         for (int j = 0; j < kSP; j++) {
             const uint32_t s = (uint32_t)(kSP * p + j);
+            uint32_t lo = 0;
             if ((int)s < A) {
-                const uint32_t lo = base + pre[j] + (s > best ? extra : 0u);
+                lo = base + pre[j] + (s > best ? extra : 0u);
                 const uint32_t f = fj[j] + (s == best ? extra : 0u);
                 put(s, lo, f);
-                if (out) g[s] = (uint16_t)lo;
+                if (out && !vec) g[s] = (uint16_t)lo;
             }
+            if (j & 1)
+                pk[j / 2] |= lo << 16;
+            else
+                pk[j / 2] = lo & 0xFFFFu;
+        }
+        if (out && vec && kSP * p < A) {
+            uint4 *gv = reinterpret_cast<uint4 *>(g + kSP * p);
+#pragma unroll
+            for (int q = 0; q < kSP / 8; q++) gv[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
     }
 }
