@@ -1079,12 +1079,23 @@ __device__ __forceinline__ void copy_stream(const uint8_t *src, uint32_t n, unsi
             }
         }
     } else {
-        for (uint32_t b = 4u * lane; b < n; b += 128u) {
-            const uint32_t nb = min(4u, n - b);
+        // one word per lane at most; a stream inside the capacity (every
+        // stream of a buffer large enough) needs no per-byte check against it
+        const uint32_t b = 4u * lane;
+        if (b < n) {
+            if (dst + n <= capacity) {
+                uint8_t *pp = packed + dst + b;
+                pp[0] = (uint8_t)first;
+                if (b + 1u < n) pp[1] = (uint8_t)(first >> 8);
+                if (b + 2u < n) pp[2] = (uint8_t)(first >> 16);
+                if (b + 3u < n) pp[3] = (uint8_t)(first >> 24);
+            } else {
+                const uint32_t nb = min(4u, n - b);
 #pragma unroll
-            for (uint32_t q = 0; q < 4; q++) {
-                const unsigned long long pos = dst + b + q;
-                if (q < nb && pos < capacity) packed[pos] = (uint8_t)(first >> (8 * q));
+                for (uint32_t q = 0; q < 4; q++) {
+                    const unsigned long long pos = dst + b + q;
+                    if (q < nb && pos < capacity) packed[pos] = (uint8_t)(first >> (8 * q));
+                }
             }
         }
     }
