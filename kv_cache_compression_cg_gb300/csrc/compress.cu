@@ -415,10 +415,13 @@ __device__ __forceinline__ void build_cdf_window(int ct, uint16_t *cnt16, const 
             else
                 pk[j / 2] = lo & 0xFFFFu;
         }
-        if (out && vec && kSP * p < A) {
+        if (out && vec) {
+            // eight entries a store; A is a multiple of 8, so each store is
+            // wholly inside the row or wholly past it
             uint4 *gv = reinterpret_cast<uint4 *>(g + kSP * p);
 #pragma unroll
-            for (int q = 0; q < kSP / 8; q++) gv[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < kSP / 8; q++)
+                if (kSP * p + 8 * q < A) gv[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
     }
 }

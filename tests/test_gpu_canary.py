@@ -65,7 +65,9 @@ def _case(synth_mod, name):
     shapes = {"ragged": (3, 150, 40, 64, [32, 16, 8], [4, 16, 255]),   # wide alphabet: the step path
               "odd_c": (2, 70, 13, 64, [16, 32], [8, 33]),             # C % 8 != 0: the step path
               "long_chunk": (2, 1300, 24, 600, [255, 16], [32, 8]),    # chunks of 600 tokens, format 1
-              "bins64": (3, 300, 136, 256, [64, 40, 16], [33, 64, 8])}  # the 64-symbol fused kernel
+              "bins64": (3, 300, 136, 256, [64, 40, 16], [33, 64, 8]),  # the 64-symbol fused kernel
+              "bins20": (2, 300, 40, 128, [20, 12], [12, 20]),         # format-1 rows of 20 entries
+              "bins24_36": (2, 260, 64, 256, [24, 16], [36, 10])}      # rows of 24 (16-byte stores) and 36
     L, T, C_, Tc, bk, bv = shapes[name]
     k = (rng.standard_normal((L, T, C_)) * rng.lognormal(0, 0.5, (1, 1, C_))).astype(np.float16)
     v = rng.standard_t(3, size=(L, T, C_)).astype(np.float16)
@@ -103,7 +105,8 @@ def _guard_codec(cd):
 
 CASES = [("tiny", 1, 1), ("tiny", 2, 1), ("tiny", 3, 1), ("mistral_chunk", 2, 1), ("mistral_chunk", 2, 10),
          ("mistral_chunk", 3, 10), ("mistral_chunk", 1, 4), ("ragged", 1, 1), ("ragged", 2, 1), ("odd_c", 2, 1),
-         ("odd_c", 3, 10), ("long_chunk", 1, 1), ("bins64", 1, 1), ("bins64", 2, 10)]
+         ("odd_c", 3, 10), ("long_chunk", 1, 1), ("bins64", 1, 1), ("bins64", 2, 10), ("bins20", 1, 1),
+         ("bins24_36", 1, 1)]
 
 
 @pytest.mark.parametrize("name,fmt,group", CASES)

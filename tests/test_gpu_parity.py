@@ -72,7 +72,7 @@ def _synth(synth_mod, name, T=None):
 
 
 CASES = ["tiny", "ragged", "c48_tc32_bins256", "c24_tc70", "c8_t1", "c16_tc1", "mistral_chunk",
-         "uniform", "c24_tc600_bins255", "c136_bins64"]
+         "uniform", "c24_tc600_bins255", "c136_bins64", "c40_bins20", "c64_bins24_36"]
 
 
 def make_case(name, synth_mod):
@@ -92,6 +92,11 @@ def make_case(name, synth_mod):
         return _shape_case(2, 1300, 24, 600, [255, 16], [32, 8], 5)
     if name == "c136_bins64":  # alphabets 33 .. 64: the fused kernel's 64-symbol form (a ragged last chunk)
         return _shape_case(3, 300, 136, 256, [64, 40, 16], [33, 64, 8], 6)
+    if name == "c40_bins20":  # format-1 alphabets of 20 (not a multiple of 8): CDF entries stored one
+        # by one; 176 slices, so the throughput kernel (the canary test runs a latency-mode size)
+        return _shape_case(8, 1300, 40, 128, [20, 12] * 4, [12, 20] * 4, 7)
+    if name == "c64_bins24_36":  # K rows of 24 entries (16-byte stores), V rows of 36 in the 64-symbol form
+        return _shape_case(2, 260, 64, 256, [24, 16], [36, 10], 8)
     raise KeyError(name)
 
 
