@@ -143,6 +143,29 @@ __device__ __forceinline__ void enc_symbol_m1(Enc &e, uint32_t entry) {
         : "r"(entry));
 }
 
+// enc_flush_word when nbits >= 32, without a branch, for the latency-mode
+// coders, where each stream's dependent chain sets the time: the word's store
+// is predicated and the state updates are selects; only a carry out of the
+// pending word (rare) branches, to the stored bytes. The throughput coder keeps
+// the branch (there every unconditional instruction costs issue slots).
+__device__ __forceinline__ void enc_flush_sel(Enc &e, uint8_t *stream) {
+    const bool need = e.nbits >= 32;
+    const uint32_t k = need ? e.nbits - 32 : 0u;  // bits left after the word
+    uint32_t word, mask;
+    asm("shf.r.clamp.b32 %0, %1, %2, %3;" : "=r"(word) : "r"(e.alo), "r"(e.ahi), "r"(k));
+    const uint32_t ovf = need ? (e.ahi >> k) & 1u : 0u;
+    asm("bmsk.clamp.b32 %0, 0, %1;" : "=r"(mask) : "r"(k));
+    e.alo = need ? (e.alo & mask) : e.alo;
+    e.ahi = need ? 0u : e.ahi;
+    e.nbits = need ? k : e.nbits;
+    // enc_push_word's steps, predicated
+    const uint32_t pv = e.prev + ovf;
+    if (ovf != 0u && pv == 0u) carry_into_stored(stream, 4 * (e.npush - 1));
+    if (need) store_be(stream, e.npush - 1, pv);
+    e.npush += need ? 1 : 0;
+    e.prev = need ? word : e.prev;
+}
+
 // Flush byte and final words; returns the stream length in bytes.
 __device__ __forceinline__ uint32_t enc_finish(Enc &e, uint8_t *stream) {
     if (e.nbits >= 32) enc_flush_word(e, stream);

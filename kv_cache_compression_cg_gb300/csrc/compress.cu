@@ -445,7 +445,8 @@ __device__ __forceinline__ void enc_entry(Enc &e, uint2 en) {
         enc_symbol_m1(e, en.x);
 }
 
-template <int AM = kAmax>
+// SEL: the flush without a branch (enc_flush_sel), for the latency-mode coders.
+template <int AM = kAmax, bool SEL = false>
 __device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uint8_t *symrow, const void *cdfw,
                                               int Wc) {
     constexpr int kRow = Alpha<AM>::AS * Alpha<AM>::EB;  // bytes per CDF row
@@ -462,10 +463,16 @@ __device__ __forceinline__ void encode_window(Enc &e, uint8_t *stream, const uin
             const uint2 e1 = ld_entry<AM>(r0 + kRow + m4[1]);
             const uint2 e2 = ld_entry<AM>(r0 + 2 * kRow + m4[2]);
             const uint2 e3 = ld_entry<AM>(r0 + 3 * kRow + m4[3]);
-            if (e.nbits >= 32) enc_flush_word(e, stream);
+            if (SEL)
+                enc_flush_sel(e, stream);
+            else if (e.nbits >= 32)
+                enc_flush_word(e, stream);
             enc_entry<AM>(e, e0);
             enc_entry<AM>(e, e1);
-            if (e.nbits >= 32) enc_flush_word(e, stream);
+            if (SEL)
+                enc_flush_sel(e, stream);
+            else if (e.nbits >= 32)
+                enc_flush_word(e, stream);
             enc_entry<AM>(e, e2);
             enc_entry<AM>(e, e3);
         }
@@ -1022,7 +1029,7 @@ __global__ void __launch_bounds__(kNT / NC + kNT, 1) k_compress_lm(
         for (int i = 0; i < nwin; i++) {
             const int Wc = min(kW, d.C - i * kW);
             if (tid < nr)
-                encode_window(e, stream, sym2 + (i & 1) * S::sym_bytes + tid * kSymRow,
+                encode_window<kAmax, true>(e, stream, sym2 + (i & 1) * S::sym_bytes + tid * kSymRow,
                               cdfw2 + (i & 1) * (kCdfwBytes / 8), Wc);
             if (i + 1 < nwin) asm volatile("bar.sync 2, %0;" ::"n"(NTH) : "memory");
         }

@@ -96,6 +96,26 @@ __device__ __forceinline__ void refill(Stream &s) {
     }
 }
 
+// refill<false> without a branch, for the latency-mode decoder, where each
+// stream's dependent chain sets the time: the append is a select, and the next
+// word's load runs every time (at the same address when nothing was appended,
+// so it stays inside the stream's words). The throughput decoder keeps the
+// branch (there every unconditional instruction costs issue slots).
+__device__ __forceinline__ void refill_sel(Stream &s) {
+    const bool need = s.nb < 32;
+    uint32_t v = __byte_perm(s.raw, 0, 0x0123);
+    const int t = max(32 - 8 * s.rem, 0);  // bits past the stream's end
+    v &= s.rem >= 4 ? 0xFFFFFFFFu : (t >= 32 ? 0u : (0xFFFFFFFFu << t));
+    v = need ? v : 0u;
+    const uint32_t nbs = need ? (uint32_t)s.nb : 0u;
+    s.bhi |= v >> nbs;
+    s.blo |= __funnelshift_r(0u, v, nbs);  // v << (32 - nb), 0 for nb = 0
+    s.nb += need ? 32 : 0;
+    s.wp += (need && s.rem > 4) ? 1 : 0;
+    s.rem -= need ? 4 : 0;
+    s.raw = __ldg(s.wp);
+}
+
 // Stream over bytes [start, end) of the packed buffer (4-byte aligned); the
 // first words come byte by byte.
 __device__ __forceinline__ void stream_init(Stream &s, const uint8_t *packed, long long start, long long end) {
@@ -187,7 +207,9 @@ __device__ __forceinline__ uint32_t decode_symbol(Stream &s, uint32_t cum, uint3
     asm("ld.shared.u16 %0, [%1];" : "=r"(f) : "r"(addr + frq_off));
     s.code -= r * lo;
     s.range = r * f;
-    const uint32_t sh = __clz(s.range) & 24;
+    // bits to shift out, 0, 8 or 16 (range >= 2^8 here): by compares on the
+    // latency path (no count-leading-zeros in the chain), else by clz
+    const uint32_t sh = WIDE ? (s.range < 0x10000u ? 16u : (s.range < 0x1000000u ? 8u : 0u)) : (__clz(s.range) & 24);
     s.code = __funnelshift_l(s.bhi, s.code, sh);
     s.bhi = __funnelshift_l(s.blo, s.bhi, sh);
     s.blo <<= sh;
@@ -518,10 +540,10 @@ __device__ __forceinline__ void decode_window(Stream &s, uint32_t cb, uint32_t f
 #pragma unroll 4
         for (int c = 0; c < W; c += 4) {
             const uint32_t rc = cb + 2 * P * c;
-            refill<TAIL>(s);
+            if (WIDE) refill_sel(s); else refill<TAIL>(s);
             const uint32_t e0 = decode_symbol<PS, CLAMP, WIDE>(s, rc, fo, amax2);
             const uint32_t e1 = decode_symbol<PS, CLAMP, WIDE>(s, rc + 2 * P, fo, amax2);
-            refill<TAIL>(s);
+            if (WIDE) refill_sel(s); else refill<TAIL>(s);
             const uint32_t e2 = decode_symbol<PS, CLAMP, WIDE>(s, rc + 4 * P, fo, amax2);
             const uint32_t e3 = decode_symbol<PS, CLAMP, WIDE>(s, rc + 6 * P, fo, amax2);
             // e = 2s: store 4s (SH == 2) or s
