@@ -2,15 +2,17 @@
 // [CG §2.3(1)], per-channel CDF [CG §2.3(2)], range encoding [CG §1.2(3)] and
 // packing of one (chunk, kv, layer) slice per CTA, straight from fp16.
 //
-// Used for chunks of up to 256 tokens, alphabets up to 32, C % 8 == 0 and
-// 16-byte aligned rows (other shapes take the quantise + slice-coder + scan
-// kernels). One thread per token stream, 256 threads, three CTAs per SM.
+// Used for chunks of up to 256 tokens, alphabets up to 64 (a 32-symbol and a
+// 64-symbol form of the kernel), C % 8 == 0 and 16-byte aligned rows (other
+// shapes take the quantise + slice-coder + scan kernels). One thread per
+// token stream, 256 threads, three CTAs per SM (two for the 64-symbol form
+// with the delta). Launches of at most one slice per SM take the latency-mode
+// kernels further down instead.
 //
 // The fp16 slice [Tc_k][C] arrives in [rows][64-channel] boxes by TMA
 // (cp.async.bulk.tensor, completion on an mbarrier; every wait is bounded and
 // sets CG_FLAG_TIMEOUT when it runs out). Per CTA:
-//   0. take a slice ticket (so every slice a CTA waits on below belongs to a
-//      CTA that is already running);
+//   0. take a slice ticket (slices start in stream order);
 //   1. max1 pass: the slice's boxes stream through two buffers; each lane
 //      keeps the running max of the fp16 magnitude bits of its rows, then a
 //      half-warp reduction gives max1 per token and factor = MAX / max1
@@ -22,11 +24,13 @@
 //      sync separates its coding of one window from its writes of the next).
 //      y = RN(RN(x * factor) + MAX) in binary32 (the adds two at a time as
 //      f32x2); adding 1.5 * 2^23 rounds y to the nearest integer, ties to even, into
-//      the low bits. Symbols go to a shared tile as 8q (a byte offset into a
-//      CDF row), counts to a [symbol][channel] table of 16-bit counters;
+//      the low bits. Symbols go to a shared tile as 8q (4q for 64 symbols: a
+//      byte offset into a CDF row), counts to a [symbol][channel] table of
+//      16-bit counters;
 //   3. four threads per channel turn its counts into a CDF row in one pass
-//      (own eight symbols, then a four-lane scan), zeroing the counters they
-//      read, and write (lo, f) pairs to shared memory and lo to the output;
+//      (own eight (sixteen) symbols, then a four-lane scan), zeroing the
+//      counters they read, and write the row's entries to shared memory and
+//      lo (format 1) or the count record (format 2) to the output;
 //   4. every thread codes its token's 64 symbols;
 //   after the last window:
 //   5. each stream's length and the slice's byte total go out; no CTA of this

@@ -15,7 +15,9 @@
 // (q - MAX) / MAX. One barrier per window (for the row buffers); the tile
 // rows are warp-private, except with the delta, where a row's anchor may
 // belong to another warp and the decoder threads meet at a second barrier
-// before the writes.
+// before the writes. Launches of at most one slice per SM take k_decode_lm
+// further down instead (decoding threads fed by support threads, and a slice
+// split over two SMs where the launch leaves room).
 //
 // Stream state is 32-bit: code, range, a 64-bit bit buffer held as two words,
 // and a prefetched word whose load has the next ~32 coded bits to land. Bytes
