@@ -16,6 +16,7 @@ scaling); rank 0 prints the line with the max over ranks of the timed region.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -56,6 +57,9 @@ def parse():
                     help="skip the oracle's chunk-parallel timing on all host cores")
     ap.add_argument("--group", type=int, default=1,
                     help="token-locality delta group size (1: none, the page's LMCache code path)")
+    ap.add_argument("--bins", type=int, default=0,
+                    help="the same bins for every layer of K and V instead of the workload's (a wider "
+                         "alphabet on the same values; reports no committed traffic)")
     return ap.parse_args()
 
 
@@ -326,6 +330,8 @@ def run_reference(args):
         return
     from kv_cache_compression_cg_gb300 import synth
     w = synth.WORKLOADS[args.workload]
+    if args.bins:
+        w = dataclasses.replace(w, bins_k=(args.bins,) * w.L, bins_v=(args.bins,) * w.L)
     tokens = min(w.T, w.chunk_tokens)
     k, v = synth.generate(w, T=tokens)
     for _ in range(args.warmup):
@@ -370,11 +376,12 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     from kv_cache_compression_cg_gb300 import codec, synth
-    import dataclasses
 
     base = synth.WORKLOADS[args.workload]
     if args.tokens:
         base = dataclasses.replace(base, T=min(args.tokens, base.T))
+    if args.bins:
+        base = dataclasses.replace(base, bins_k=(args.bins,) * base.L, bins_v=(args.bins,) * base.L)
     w = dataclasses.replace(base, seed=base.seed + 1000 * rank) if rank else base
     k, v = synth.generate_device(w)  # same bytes as the host generator
     fp16_bytes = 2 * k.numel() * k.element_size()
@@ -474,7 +481,8 @@ def run_ours(args):
             "kernel": kname, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
             "measured" else "fallback", "algorithmic_bytes": kbytes, "ms": kms,
-            "traffic": kernel_traffic(f"{kname.split()[0]}_{args.workload}_f{args.format}_g{args.group}", srcs),
+            "traffic": None if args.bins else kernel_traffic(
+                f"{kname.split()[0]}_{args.workload}_f{args.format}_g{args.group}", srcs),
             "alu": {"achieved": alu, "peak": peak_tops, "unit": "Tops/s", "frac": alu / peak_tops,
                     "ops_per_symbol": ops,
                     "peak_kind": f"derived: {props.multi_processor_count} SMs x 4 schedulers x 32 lanes x "
