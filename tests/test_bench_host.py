@@ -50,3 +50,9 @@ def test_reference_arm_prints_one_contract_line():
 def test_reference_arm_silent_on_other_ranks():
     assert _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3", "--workload", "tiny",
                       "--no-chunk-parallel", env={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
+
+
+def test_bins_override_reaches_the_config():
+    (d,) = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3", "--workload", "tiny",
+                      "--bins", "64", "--no-chunk-parallel")
+    assert d["config"]["bins_k"] == [64]
