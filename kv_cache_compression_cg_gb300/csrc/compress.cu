@@ -869,6 +869,9 @@ __global__ void __launch_bounds__(kNT / NC + kNT, 1) k_compress_lm(
     __shared__ uint16_t s_m1[NCOD];
     __shared__ uint16_t s_ftab[kNT + 2];
 
+    // the packing launch (programmatic dependent launch) may start placing its
+    // CTAs now; they wait in griddepcontrol.wait until this grid has finished
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t dyn = smem_u32(dsm);
     const uint32_t base = (dyn + 127u) & ~127u;
     unsigned char *sm = dsm + (base - dyn);
@@ -1238,6 +1241,9 @@ __global__ void __launch_bounds__(kNT, 4) k_pack_lm(Dims d, const uint8_t *__res
                                                  const unsigned long long *__restrict__ totals, int32_t *status) {
     __shared__ unsigned long long s_red[kNW];
     __shared__ uint32_t s_len[kNT], s_loc[kNT], s_wtot[kNW];
+    // launched as a programmatic dependent of the compress kernel: wait until
+    // that grid has finished and its writes are visible (a no-op otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int slice = blockIdx.x / kPackParts, part = blockIdx.x % kPackParts;
     const long long nslices = 2LL * d.L * d.nch;
@@ -1401,8 +1407,23 @@ cudaError_t launch_compress_fused(const uint16_t *k, const uint16_t *v, const Di
             kern<<<(unsigned)nslices, 2 * kNT, dyn, s>>>(tmk, tmv, d, mt, box_rows, max1, side, stage, len, state,
                                                        status);
         }
-        k_pack_lm<<<(unsigned)(kPackParts * nslices), kNT, 0, s>>>(d, stage, len, off, packed, capacity,
-                                                                   state + 2 + nslices, status);
+        // the packing as a programmatic dependent launch: its CTAs are placed
+        // while the compress grid runs and start as soon as it has finished
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3((unsigned)(kPackParts * nslices));
+        pcfg.blockDim = dim3(kNT);
+        pcfg.dynamicSmemBytes = 0;
+        pcfg.stream = s;
+        cudaLaunchAttribute pattr[1];
+        pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pattr[0].val.programmaticStreamSerializationAllowed = 1;
+        pcfg.attrs = pattr;
+        pcfg.numAttrs = 1;
+        const unsigned long long *totals = state + 2 + nslices;
+        err = cudaLaunchKernelEx(&pcfg, k_pack_lm, d, static_cast<const uint8_t *>(stage),
+                                 static_cast<const uint32_t *>(len), off, packed, (unsigned long long)capacity, totals,
+                                 status);
+        if (err != cudaSuccess) return err;
         return cudaGetLastError();
     }
     k_compress_init<<<(unsigned)((nslices + 2 + 255) / 256), 256, 0, s>>>(state, nslices);

@@ -25,10 +25,13 @@ def _snapshot(cd, out, ok, ov):
             ok.clone(), ov.clone(), out.status.clone(), cd.dstatus.clone()]
 
 
-@pytest.mark.parametrize("fmt,group", [(1, 1), (2, 1), (3, 1), (2, 10)])
-def test_graph_replay_equals_eager(cg, synth_mod, fmt, group):
+# T = 1024 (four chunks, 256 slices) takes the throughput kernels; T = 256 (one
+# chunk, 64 slices) the latency-mode ones, whose packing is a programmatic
+# dependent launch
+@pytest.mark.parametrize("fmt,group,T", [(1, 1, 1024), (2, 1, 1024), (3, 1, 1024), (2, 10, 1024), (1, 1, 256),
+                                         (2, 1, 256)])
+def test_graph_replay_equals_eager(cg, synth_mod, fmt, group, T):
     w = synth_mod.WORKLOADS["ctx4096"]
-    T = 1024  # four chunks
     k0, v0 = synth_mod.generate_device(w, T=T)
     k1, v1 = synth_mod.generate_device(synth_mod.WORKLOADS["mistral_chunk"], T=T)  # other values, same shape
     cd = cg.Codec(w.L, T, w.C, w.bins_k, w.bins_v, chunk_tokens=w.chunk_tokens, fmt=fmt, group=group)
